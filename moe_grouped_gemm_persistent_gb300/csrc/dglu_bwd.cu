@@ -1,0 +1,324 @@
+// Grouped GEMM + dGLU backward ("Grouped GEMM + dGLU (SM100)", BF16 contract):
+//
+//   R_g = alpha_g^2 * A_g * B_g^T           rows of expert g: [padded_offsets[g-1], padded_offsets[g])
+//   X_g = beta_g * C_g                      alternating 32-wide gate / input blocks
+//   D_row = interleaved (dgate, dinput)     dSwiGLU or dGeGLU (clamp +-7, filters)
+//   dprob[m] += sum_j R[m, j] * act[m, j]   act = unscaled forward activation
+//   dbias[g, :] += sum_{m in g} D_row[m, :] (optional)
+//
+// One persistent kernel computes the GEMM on the tensor cores and applies the whole
+// epilogue from TMEM: no intermediate R tensor ever reaches global memory.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "mgg_internal.h"
+#include "mgg_pipeline.cuh"
+
+namespace mgg {
+
+constexpr int kDgluStages = 4;
+
+struct DgluParams {
+  CUtensorMap tmap_a;           // A (M, K): dims {K, M}, box {64, 128}, 128B swizzle
+  CUtensorMap tmap_b;           // dense B (N, K, L): dims {K, N, L}, box {64, BN, 1}
+  const CUtensorMap* b_maps;    // discrete B: one map per expert in the workspace, else null
+  const int32_t* offsets;
+  const float* alpha;
+  const float* beta;
+  const float* prob;
+  const void* c;
+  void* d;
+  float* dprob;
+  float* dbias_ws;              // fp32 partial sums (L, 2N), null = no dbias
+  int* status;
+  int32_t* tile_log;
+  long long tile_log_cap;
+  long long total_tiles;
+  int M, K, N, L;
+  int num_n, num_kb;
+  int a_mn, b_mn;
+  int c_dtype, d_dtype, act, indicator, gate_first;
+};
+
+__device__ __forceinline__ float fast_sigmoid(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+
+template <int BN>
+struct DgluPolicy {
+  const DgluParams& p;
+  long long total_tiles;
+  int* status;
+  int a_mn, b_mn;
+
+  __device__ DgluPolicy(const DgluParams& prm)
+      : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(0), b_mn(prm.b_mn) {}
+
+  __device__ void load_tables(int* s_table) const {
+    for (int i = threadIdx.x; i < p.L; i += blockDim.x) s_table[i] = p.offsets[i];
+  }
+
+  // Tile order: expert-major; inside an expert, column panels of BN, and inside a panel
+  // the expert's 128-row blocks, so concurrently running CTAs share one B panel and the
+  // expert's A rows in L2.  Tile t belongs to the expert containing row
+  // floor(t / num_n) * 128 (its tiles occupy [begin/128 * num_n, end/128 * num_n)).
+  __device__ TileWork tile(long long t, const int* offs) const {
+    const int row = (int)(t / p.num_n) * BM;
+    int lo = 0, hi = p.L - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (offs[mid] > row) hi = mid;
+      else lo = mid + 1;
+    }
+    const int g = lo;
+    const int begin = g ? offs[g - 1] : 0;
+    const int mblocks = (offs[g] - begin) / BM;
+    const long long u = t - (long long)(begin / BM) * p.num_n;
+    TileWork w;
+    w.active = 1;
+    w.expert = g;
+    w.n0 = (int)(u / mblocks) * BN;
+    w.m0 = begin + (int)(u % mblocks) * BM;
+    w.k0 = 0;
+    w.num_kb = p.num_kb;
+    return w;
+  }
+
+  __device__ void issue_loads(const TileWork& w, int kb, uint32_t sa, uint32_t sb, uint32_t bar) const {
+    tma_load_2d(sa, &p.tmap_a, bar, kb * BK, w.m0);
+    if (p.b_maps == nullptr) {
+      tma_load_3d(sb, &p.tmap_b, bar, kb * BK, w.n0, w.expert);
+    } else {
+      const CUtensorMap* m = p.b_maps + w.expert;
+      if (kb == 0) tmap_acquire(m);
+      if (!p.b_mn) {
+        tma_load_2d(sb, m, bar, kb * BK, w.n0);
+      } else {
+#pragma unroll
+        for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, m, bar, w.n0 + 64 * j, kb * BK);
+      }
+    }
+  }
+
+  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, int q, int lane, bool have_acc,
+                           const int*) const {
+    const int g = w.expert;
+    const float alpha_g = p.alpha[g];
+    const float alpha2 = alpha_g * alpha_g;
+    const float beta_g = p.beta[g];
+    const int row = w.m0 + q * 32 + lane;
+    const float pr = p.prob[row];
+    const size_t two_n = 2 * (size_t)p.N;
+    const size_t row_off = (size_t)row * two_n;
+    const bool geglu = p.act == MGG_ACT_DGEGLU;
+    float dprob_acc = 0.f;
+
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int j0 = w.n0 + c * 32;
+      if (j0 >= p.N) break;
+      uint32_t r[32];
+      tmem_load_32cols(taddr + c * 32, r);
+      const int first = 2 * j0, second = 2 * j0 + 32;
+      const int gcol = p.gate_first ? first : second;
+      const int icol = p.gate_first ? second : first;
+      float gv[32], iv[32];
+      load32(p.c, p.c_dtype, row_off + gcol, gv);
+      load32(p.c, p.c_dtype, row_off + icol, iv);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float R = __fmul_rn(alpha2, __uint_as_float(r[k]));
+        const float x_g = __fmul_rn(beta_g, gv[k]);  // one fp32 product, never contracted
+        const float x_i = __fmul_rn(beta_g, iv[k]);
+        const float Rp = R * pr;
+        float dg, di, act;
+        if (!geglu) {
+          const float s = fast_sigmoid(x_g);
+          di = Rp * (x_g * s);
+          dg = Rp * x_i * s * (1.0f + x_g * (1.0f - s));
+          act = x_g * s * x_i;
+        } else {
+          const float cg = fminf(x_g, 7.0f);
+          const float ci = fminf(fmaxf(x_i, -7.0f), 7.0f);
+          const bool g_in = x_g <= 7.0f;
+          const bool i_in = (x_i >= -7.0f) && (x_i <= 7.0f);
+          const float gf = g_in ? (p.indicator ? 1.0f : x_g) : 0.0f;
+          const float inf_ = i_in ? (p.indicator ? 1.0f : x_i) : 0.0f;
+          const float s = fast_sigmoid(1.702f * cg);
+          const float ci1 = ci + 1.0f;
+          dg = Rp * ci1 * s * (1.0f + 1.702f * cg * (1.0f - s)) * gf;
+          di = Rp * cg * s * inf_;
+          act = cg * s * ci1;
+        }
+        dprob_acc += R * act;
+        gv[k] = dg;
+        iv[k] = di;
+      }
+      store32(p.d, p.d_dtype, row_off + gcol, gv);
+      store32(p.d, p.d_dtype, row_off + icol, iv);
+      if (p.dbias_ws != nullptr) {
+        float* ws = p.dbias_ws + (size_t)g * two_n;
+        const float sg = warp_column_sums(gv, lane);
+        const float si = warp_column_sums(iv, lane);
+        atomicAdd(ws + gcol + lane, sg);
+        atomicAdd(ws + icol + lane, si);
+      }
+    }
+    atomicAdd(p.dprob + row, dprob_acc);
+    if (p.tile_log != nullptr && q == 0 && lane == 0 && t < p.tile_log_cap) {
+      int32_t* e = p.tile_log + 4 * t;
+      e[0] = g;
+      e[1] = w.m0;
+      e[2] = w.n0;
+      e[3] = (int32_t)blockIdx.x;
+    }
+    (void)have_acc;
+  }
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1) dglu_bwd_kernel(const __grid_constant__ DgluParams prm) {
+  const DgluPolicy<BN> pol(prm);
+  persistent_gemm<BN, STAGES>(pol);
+}
+
+// Checks the device-resident arguments and builds the per-expert weight maps.
+__global__ void dglu_prep_kernel(const int32_t* offsets, int L, long long M, const int64_t* b_ptrs,
+                                 const __grid_constant__ CUtensorMap tmpl, CUtensorMap* maps, int* status) {
+  bool bad_off = false, bad_ptr = false;
+  for (int e = threadIdx.x; e < L; e += blockDim.x) {
+    const int prev = e ? offsets[e - 1] : 0;
+    const int cur = offsets[e];
+    if (cur < prev || ((cur - prev) & 255) != 0) bad_off = true;
+    if (e == L - 1 && (long long)cur != M) bad_off = true;
+    if (b_ptrs != nullptr) {
+      const long long ptr = b_ptrs[e];
+      if (ptr == 0 || (ptr & 15) != 0) bad_ptr = true;
+    }
+  }
+  const int any_off = __syncthreads_or(bad_off);
+  const int any_ptr = __syncthreads_or(bad_ptr);
+  if (threadIdx.x == 0) {
+    status[0] = any_off ? (int)MGG_ERR_DEVICE_OFFSETS : any_ptr ? (int)MGG_ERR_DEVICE_POINTER : 0;
+    status[1] = 0;
+    status[2] = 0;
+    status[3] = 0;
+  }
+  if (any_off || any_ptr || b_ptrs == nullptr) return;
+  const uint4* src = reinterpret_cast<const uint4*>(&tmpl);
+  for (int e = threadIdx.x; e < L; e += blockDim.x) {
+    uint4* dst = reinterpret_cast<uint4*>(maps + e);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = src[i];
+    tmap_replace_address(maps + e, reinterpret_cast<const void*>(b_ptrs[e]));
+  }
+  tmap_release();
+}
+
+// dbias (bf16) = bf16(dbias + fp32 partial sums): a single rounding of old + sum.
+__global__ void dbias_finalize_kernel(const float* ws, __nv_bfloat16* dbias, long long n, const int* status) {
+  if (*status != 0) return;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    dbias[i] = __float2bfloat16_rn(__bfloat162float(dbias[i]) + ws[i]);
+}
+
+cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
+  const mgg_dglu_bwd_args& a = *Lc.args;
+  constexpr int BN = kDgluTileN;
+  constexpr int STAGES = kDgluStages;
+  using S = SmemLayout<BN, STAGES>;
+  static_assert(S::DYN_BYTES <= 232448, "shared memory");
+
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(ws + kWsHeaderBytes);
+  float* dbias_ws = reinterpret_cast<float*>(ws + kWsHeaderBytes + kTmapBytes * (size_t)a.L);
+
+  dglu_prep_kernel<<<1, 1024, 0, stream>>>(a.padded_offsets, (int)a.L, (long long)a.M, a.b_ptrs, Lc.tmap_b, maps,
+                                          status);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (a.dbias != nullptr) {
+    err = cudaMemsetAsync(dbias_ws, 0, sizeof(float) * (size_t)a.L * 2 * (size_t)a.N, stream);
+    if (err != cudaSuccess) return err;
+  }
+  const long long num_n = (a.N + BN - 1) / BN;
+  const long long total = (a.M / BM) * num_n;
+  if (a.tile_log != nullptr && a.tile_log_capacity > 0) {
+    err = cudaMemsetAsync(a.tile_log, 0xff, sizeof(int32_t) * 4 * (size_t)a.tile_log_capacity, stream);
+    if (err != cudaSuccess) return err;
+  }
+  if (total > 0) {
+    DgluParams prm;
+    prm.tmap_a = Lc.tmap_a;
+    prm.tmap_b = Lc.tmap_b;
+    prm.b_maps = a.b_ptrs != nullptr ? maps : nullptr;
+    prm.offsets = a.padded_offsets;
+    prm.alpha = a.alpha;
+    prm.beta = a.beta;
+    prm.prob = a.prob;
+    prm.c = a.c;
+    prm.d = a.d_row;
+    prm.dprob = a.dprob;
+    prm.dbias_ws = a.dbias != nullptr ? dbias_ws : nullptr;
+    prm.status = status;
+    prm.tile_log = a.tile_log;
+    prm.tile_log_cap = a.tile_log != nullptr ? a.tile_log_capacity : 0;
+    prm.total_tiles = total;
+    prm.M = (int)a.M;
+    prm.K = (int)a.K;
+    prm.N = (int)a.N;
+    prm.L = (int)a.L;
+    prm.num_n = (int)num_n;
+    prm.num_kb = (int)((a.K + BK - 1) / BK);
+    prm.a_mn = 0;
+    prm.b_mn = (a.b_ptrs != nullptr && a.b_major == MGG_MAJOR_MN) ? 1 : 0;
+    prm.c_dtype = a.c_dtype;
+    prm.d_dtype = a.d_dtype;
+    prm.act = a.act;
+    prm.indicator = a.geglu_filter == MGG_FILTER_INDICATOR;
+    prm.gate_first = a.gate_first != 0;
+
+    auto kern = dglu_bwd_kernel<BN, STAGES>;
+    static bool attr_set = false;
+    if (!attr_set) {
+      err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);
+      if (err != cudaSuccess) return err;
+      attr_set = true;
+    }
+    const int grid = (int)(total < Lc.num_sms ? total : Lc.num_sms);
+    kern<<<grid, kThreads, S::DYN_BYTES, stream>>>(prm);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  if (a.dbias != nullptr) {
+    const long long n = a.L * 2 * a.N;
+    const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+    dbias_finalize_kernel<<<blocks > 0 ? blocks : 1, 256, 0, stream>>>(dbias_ws, static_cast<__nv_bfloat16*>(a.dbias),
+                                                                       n, status);
+    err = cudaGetLastError();
+  }
+  return err;
+}
+
+// ------------------------------------------------------------------------------------
+// tensormap.replace probe (test hook)
+// ------------------------------------------------------------------------------------
+__global__ void tmap_replace_probe_kernel(const __grid_constant__ CUtensorMap tmpl, CUtensorMap* out,
+                                          const void* addr, uint32_t dim0, uint64_t stride1, int fields) {
+  if (threadIdx.x != 0) return;
+  const uint4* src = reinterpret_cast<const uint4*>(&tmpl);
+  uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) dst[i] = src[i];
+  if (fields & 1) tmap_replace_address(out, addr);
+  if (fields & 2) tmap_replace_dim(out, 0, dim0);
+  if (fields & 4) tmap_replace_stride0(out, stride1);
+  tmap_release();
+}
+
+cudaError_t launch_tmap_replace_probe(const CUtensorMap& tmpl, void* out, const void* addr, uint32_t dim0,
+                                      uint64_t stride1, int fields, cudaStream_t stream) {
+  tmap_replace_probe_kernel<<<1, 32, 0, stream>>>(tmpl, static_cast<CUtensorMap*>(out), addr, dim0, stride1, fields);
+  return cudaGetLastError();
+}
+
+}  // namespace mgg

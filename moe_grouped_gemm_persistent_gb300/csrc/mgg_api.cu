@@ -1,0 +1,351 @@
+// C ABI of libmgg: host-side validation, TMA descriptor encoding, device checks, launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+
+#include "mgg.h"
+#include "mgg_internal.h"
+#include "mgg_testing.h"
+
+namespace mgg {
+namespace {
+
+thread_local std::string g_err;
+
+mgg_status fail(mgg_status s, const std::string& msg) {
+  g_err = msg;
+  return s;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+// ---------------------------------------------------------------- driver entry point
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 tiled map with 128-byte swizzle; dims[0] innermost; strides in bytes for dims 1..rank-1.
+mgg_status encode_bf16(CUtensorMap* map, const void* addr, int rank, const uint64_t* dims, const uint64_t* strides,
+                       const uint32_t* box, const char* what) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return fail(MGG_ERR_RUNTIME, "cuTensorMapEncodeTiled is not available from the CUDA driver");
+  cuuint64_t gdim[3], gstr[2];
+  cuuint32_t bdim[3], estr[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) gstr[i] = strides[i];
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(addr), gdim, gstr,
+                        bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MGG_ERR_RUNTIME, std::string("cuTensorMapEncodeTiled rejected the ") + what + " map (CUresult " +
+                                     std::to_string((int)r) + ")");
+  return MGG_OK;
+}
+
+// ---------------------------------------------------------------- device check
+struct DevInfo {
+  int num_sms;
+};
+
+mgg_status check_device(DevInfo* info) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MGG_ERR_ARCH, std::string("no CUDA device: ") + cudaGetErrorString(e));
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || minor != 3)
+    return fail(MGG_ERR_ARCH, "libmgg is built for sm_103a; the current device has compute capability " +
+                                  std::to_string(major) + "." + std::to_string(minor));
+  info->num_sms = sms;
+  return MGG_OK;
+}
+
+bool valid_dtype(int d) { return d == MGG_BF16 || d == MGG_FP16 || d == MGG_FP32; }
+
+// ---------------------------------------------------------------- dGLU validation
+mgg_status validate_dglu(const mgg_dglu_bwd_args& a) {
+  if (a.L < 1 || a.L > 1024) return fail(MGG_ERR_VALUE, "expert count L must be in [1, 1024]");
+  if (a.M < 0 || a.M % 256 != 0) return fail(MGG_ERR_VALUE, "M (padded rows) must be a non-negative multiple of 256");
+  if (a.M > (int64_t)1 << 30) return fail(MGG_ERR_UNSUPPORTED, "M above 2^30 rows is not supported");
+  if (a.K < 8 || a.K % 8 != 0) return fail(MGG_ERR_VALUE, "K must be a positive multiple of 8 (16-byte rows)");
+  if (a.K > (int64_t)1 << 24) return fail(MGG_ERR_UNSUPPORTED, "K above 2^24 is not supported");
+  if (a.N < 32 || a.N % 32 != 0) return fail(MGG_ERR_VALUE, "N must be a positive multiple of 32");
+  if (a.N > (int64_t)1 << 24) return fail(MGG_ERR_UNSUPPORTED, "N above 2^24 is not supported");
+  if ((a.b == nullptr) == (a.b_ptrs == nullptr))
+    return fail(MGG_ERR_VALUE, "exactly one of the dense weights b and the pointer array b_ptrs must be given");
+  if (a.b_major != MGG_MAJOR_K && a.b_major != MGG_MAJOR_MN) return fail(MGG_ERR_VALUE, "b_major must be K or MN");
+  if (a.b != nullptr && a.b_major != MGG_MAJOR_K) return fail(MGG_ERR_VALUE, "dense weights (N, K, L) are K-major");
+  if (!valid_dtype(a.c_dtype) || !valid_dtype(a.d_dtype)) return fail(MGG_ERR_VALUE, "c_dtype/d_dtype out of range");
+  if (a.act != MGG_ACT_DSWIGLU && a.act != MGG_ACT_DGEGLU) return fail(MGG_ERR_VALUE, "act must be DSWIGLU or DGEGLU");
+  if (a.geglu_filter != MGG_FILTER_VALUE && a.geglu_filter != MGG_FILTER_INDICATOR)
+    return fail(MGG_ERR_VALUE, "geglu_filter must be VALUE or INDICATOR");
+  if (a.gate_first != 0 && a.gate_first != 1) return fail(MGG_ERR_VALUE, "gate_first must be 0 or 1");
+  if (a.sched != MGG_SCHED_STATIC && a.sched != MGG_SCHED_DYNAMIC) return fail(MGG_ERR_VALUE, "sched out of range");
+  if (a.sched == MGG_SCHED_DYNAMIC) return fail(MGG_ERR_UNSUPPORTED, "dynamic scheduling is not available yet");
+  if (a.reserved != 0) return fail(MGG_ERR_VALUE, "reserved field must be 0");
+  const void* req[] = {a.a, a.c, a.padded_offsets, a.alpha, a.beta, a.prob, a.dprob, a.d_row, a.workspace};
+  const char* names[] = {"a", "c", "padded_offsets", "alpha", "beta", "prob", "dprob", "d_row", "workspace"};
+  for (int i = 0; i < 9; ++i) {
+    if (req[i] == nullptr) return fail(MGG_ERR_VALUE, std::string(names[i]) + " must not be NULL");
+    if (!aligned16(req[i])) return fail(MGG_ERR_VALUE, std::string(names[i]) + " must be 16-byte aligned");
+  }
+  if (a.b && !aligned16(a.b)) return fail(MGG_ERR_VALUE, "b must be 16-byte aligned");
+  if (a.b_ptrs && !aligned16(a.b_ptrs)) return fail(MGG_ERR_VALUE, "b_ptrs must be 16-byte aligned");
+  if (a.dbias && !aligned16(a.dbias)) return fail(MGG_ERR_VALUE, "dbias must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(a.workspace) & 255u) != 0)
+    return fail(MGG_ERR_VALUE, "workspace must be 256-byte aligned");
+  if ((size_t)a.workspace_bytes < mgg_dglu_bwd_workspace_size(a.L, a.N))
+    return fail(MGG_ERR_VALUE, "workspace too small: need " + std::to_string(mgg_dglu_bwd_workspace_size(a.L, a.N)) +
+                                   " bytes");
+  if (a.tile_log != nullptr) {
+    if (!aligned16(a.tile_log)) return fail(MGG_ERR_VALUE, "tile_log must be 16-byte aligned");
+    if (a.tile_log_capacity < mgg_dglu_bwd_num_tiles(a.M, a.N))
+      return fail(MGG_ERR_VALUE, "tile_log_capacity smaller than the number of tiles");
+  }
+  return MGG_OK;
+}
+
+// ---------------------------------------------------------------- wgrad validation
+mgg_status validate_wgrad(const mgg_wgrad_args& a) {
+  if (a.L < 1 || a.L > 1024) return fail(MGG_ERR_VALUE, "expert count L must be in [1, 1024]");
+  if (a.hidden < 8 || a.hidden % 8 != 0) return fail(MGG_ERR_VALUE, "hidden must be a positive multiple of 8");
+  if (a.inter < 8 || a.inter % 8 != 0) return fail(MGG_ERR_VALUE, "intermediate must be a positive multiple of 8");
+  if (a.hidden > (int64_t)1 << 24 || a.inter > (int64_t)1 << 24)
+    return fail(MGG_ERR_UNSUPPORTED, "hidden/intermediate above 2^24 is not supported");
+  if (a.tokens_sum < 0 || a.tokens_sum % 256 != 0)
+    return fail(MGG_ERR_VALUE, "tokens_sum must be a non-negative multiple of 256");
+  if (a.tokens_sum > (int64_t)1 << 30) return fail(MGG_ERR_UNSUPPORTED, "tokens_sum above 2^30 is not supported");
+  if ((a.out == nullptr) == (a.out_ptrs == nullptr))
+    return fail(MGG_ERR_VALUE, "exactly one of the dense output and the pointer array out_ptrs must be given");
+  if (a.a_major != MGG_MAJOR_K && a.a_major != MGG_MAJOR_MN) return fail(MGG_ERR_VALUE, "a_major must be K or MN");
+  if (a.b_major != MGG_MAJOR_K && a.b_major != MGG_MAJOR_MN) return fail(MGG_ERR_VALUE, "b_major must be K or MN");
+  if (a.input_order != MGG_ORDER_TENSOR2D && a.input_order != MGG_ORDER_TENSOR_RAGGED)
+    return fail(MGG_ERR_VALUE, "input_order out of range");
+  if (!valid_dtype(a.out_dtype)) return fail(MGG_ERR_VALUE, "out_dtype out of range");
+  if (a.accumulate != 0 && a.accumulate != 1) return fail(MGG_ERR_VALUE, "accumulate must be 0 or 1");
+  if (a.sched != MGG_SCHED_STATIC && a.sched != MGG_SCHED_DYNAMIC) return fail(MGG_ERR_VALUE, "sched out of range");
+  if (a.sched == MGG_SCHED_DYNAMIC) return fail(MGG_ERR_UNSUPPORTED, "dynamic scheduling is not available yet");
+  if (a.reserved0 != 0 || a.reserved1 != 0) return fail(MGG_ERR_VALUE, "reserved fields must be 0");
+  const void* req[] = {a.a, a.b, a.offsets, a.workspace};
+  const char* names[] = {"a", "b", "offsets", "workspace"};
+  for (int i = 0; i < 4; ++i) {
+    if (req[i] == nullptr) return fail(MGG_ERR_VALUE, std::string(names[i]) + " must not be NULL");
+    if (!aligned16(req[i])) return fail(MGG_ERR_VALUE, std::string(names[i]) + " must be 16-byte aligned");
+  }
+  if (a.out && !aligned16(a.out)) return fail(MGG_ERR_VALUE, "out must be 16-byte aligned");
+  if (a.out_ptrs && !aligned16(a.out_ptrs)) return fail(MGG_ERR_VALUE, "out_ptrs must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(a.workspace) & 255u) != 0)
+    return fail(MGG_ERR_VALUE, "workspace must be 256-byte aligned");
+  if ((size_t)a.workspace_bytes < mgg_wgrad_workspace_size(a.L))
+    return fail(MGG_ERR_VALUE, "workspace too small: need " + std::to_string(mgg_wgrad_workspace_size(a.L)) + " bytes");
+  if (a.tile_log != nullptr) {
+    if (!aligned16(a.tile_log)) return fail(MGG_ERR_VALUE, "tile_log must be 16-byte aligned");
+    if (a.tile_log_capacity < mgg_wgrad_num_tiles(a.L, a.hidden, a.inter))
+      return fail(MGG_ERR_VALUE, "tile_log_capacity smaller than the number of tiles");
+  }
+  return MGG_OK;
+}
+
+mgg_status from_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return MGG_OK;
+  return fail(MGG_ERR_RUNTIME, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+}  // namespace
+}  // namespace mgg
+
+using namespace mgg;
+
+extern "C" {
+
+int mgg_abi_version(void) { return MGG_ABI_VERSION; }
+
+size_t mgg_sizeof_dglu_bwd_args(void) { return sizeof(mgg_dglu_bwd_args); }
+
+size_t mgg_sizeof_wgrad_args(void) { return sizeof(mgg_wgrad_args); }
+
+const char* mgg_last_error(void) { return g_err.c_str(); }
+
+const char* mgg_status_string(int s) {
+  switch (s) {
+    case MGG_OK: return "MGG_OK";
+    case MGG_ERR_VALUE: return "MGG_ERR_VALUE";
+    case MGG_ERR_UNSUPPORTED: return "MGG_ERR_UNSUPPORTED";
+    case MGG_ERR_RUNTIME: return "MGG_ERR_RUNTIME";
+    case MGG_ERR_ARCH: return "MGG_ERR_ARCH";
+    case MGG_ERR_DEVICE_OFFSETS: return "MGG_ERR_DEVICE_OFFSETS";
+    case MGG_ERR_DEVICE_POINTER: return "MGG_ERR_DEVICE_POINTER";
+    case MGG_ERR_DEVICE_TIMEOUT: return "MGG_ERR_DEVICE_TIMEOUT";
+    default: return "MGG_UNKNOWN_STATUS";
+  }
+}
+
+size_t mgg_dglu_bwd_workspace_size(int64_t L, int64_t N) {
+  if (L < 0 || N < 0) return 0;
+  return round_up(kWsHeaderBytes + kTmapBytes * (size_t)L + sizeof(float) * (size_t)L * 2 * (size_t)N, 256);
+}
+
+size_t mgg_wgrad_workspace_size(int64_t L) {
+  if (L < 0) return 0;
+  return round_up(kWsHeaderBytes + 2 * kTmapBytes * (size_t)L + sizeof(int32_t) * (size_t)L, 256);
+}
+
+int64_t mgg_dglu_bwd_num_tiles(int64_t M, int64_t N) {
+  if (M < 0 || N < 0) return 0;
+  return (M / 128) * ((N + kDgluTileN - 1) / kDgluTileN);
+}
+
+int64_t mgg_wgrad_num_tiles(int64_t L, int64_t hidden, int64_t inter) {
+  if (L < 0 || hidden < 0 || inter < 0) return 0;
+  const int64_t bn = wgrad_tile_n(inter);
+  return L * ((hidden + 127) / 128) * ((inter + bn - 1) / bn);
+}
+
+void mgg_dglu_bwd_tile_shape(int32_t* tile_m, int32_t* tile_n) {
+  if (tile_m) *tile_m = 128;
+  if (tile_n) *tile_n = kDgluTileN;
+}
+
+void mgg_wgrad_tile_shape(int64_t inter, int32_t* tile_m, int32_t* tile_n) {
+  if (tile_m) *tile_m = 128;
+  if (tile_n) *tile_n = wgrad_tile_n(inter);
+}
+
+mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream) {
+  g_err.clear();
+  if (args == nullptr) return fail(MGG_ERR_VALUE, "args is NULL");
+  const mgg_dglu_bwd_args& a = *args;
+  mgg_status s = validate_dglu(a);
+  if (s != MGG_OK) return s;
+  DevInfo dev;
+  if ((s = check_device(&dev)) != MGG_OK) return s;
+
+  DgluLaunch Lc;
+  memset(&Lc, 0, sizeof(Lc));
+  Lc.args = args;
+  Lc.num_sms = dev.num_sms;
+  Lc.tile_n = kDgluTileN;
+  const uint64_t M = (uint64_t)(a.M > 0 ? a.M : 256), K = (uint64_t)a.K, N = (uint64_t)a.N, L = (uint64_t)a.L;
+  {
+    const uint64_t dims[2] = {K, M}, strides[1] = {K * 2};
+    const uint32_t box[2] = {64, 128};
+    if ((s = encode_bf16(&Lc.tmap_a, a.a, 2, dims, strides, box, "A")) != MGG_OK) return s;
+  }
+  if (a.b != nullptr) {
+    const uint64_t dims[3] = {K, N, L}, strides[2] = {K * 2, N * K * 2};
+    const uint32_t box[3] = {64, (uint32_t)kDgluTileN, 1};
+    if ((s = encode_bf16(&Lc.tmap_b, a.b, 3, dims, strides, box, "dense B")) != MGG_OK) return s;
+  } else if (a.b_major == MGG_MAJOR_K) {
+    const uint64_t dims[2] = {K, N}, strides[1] = {K * 2};
+    const uint32_t box[2] = {64, (uint32_t)kDgluTileN};
+    if ((s = encode_bf16(&Lc.tmap_b, a.a, 2, dims, strides, box, "discrete K-major B")) != MGG_OK) return s;
+  } else {
+    const uint64_t dims[2] = {N, K}, strides[1] = {N * 2};
+    const uint32_t box[2] = {64, 64};
+    if ((s = encode_bf16(&Lc.tmap_b, a.a, 2, dims, strides, box, "discrete N-major B")) != MGG_OK) return s;
+  }
+  return from_cuda(launch_dglu_bwd(Lc, static_cast<cudaStream_t>(stream)), "mgg_dglu_bwd launch");
+}
+
+mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {
+  g_err.clear();
+  if (args == nullptr) return fail(MGG_ERR_VALUE, "args is NULL");
+  const mgg_wgrad_args& a = *args;
+  mgg_status s = validate_wgrad(a);
+  if (s != MGG_OK) return s;
+  DevInfo dev;
+  if ((s = check_device(&dev)) != MGG_OK) return s;
+
+  WgradLaunch Lc;
+  memset(&Lc, 0, sizeof(Lc));
+  Lc.args = args;
+  Lc.num_sms = dev.num_sms;
+  Lc.tile_n = wgrad_tile_n(a.inter);
+  const bool ragged = a.input_order == MGG_ORDER_TENSOR_RAGGED;
+  Lc.a_ragged = ragged && a.a_major == MGG_MAJOR_K;
+  Lc.b_ragged = ragged && a.b_major == MGG_MAJOR_K;
+  const uint64_t T = (uint64_t)(a.tokens_sum > 0 ? a.tokens_sum : 256), H = (uint64_t)a.hidden, I = (uint64_t)a.inter;
+  if (a.a_major == MGG_MAJOR_K) {  // (hidden, T), T contiguous
+    const uint64_t dims[2] = {T, H}, strides[1] = {T * 2};
+    const uint32_t box[2] = {64, 128};
+    if ((s = encode_bf16(&Lc.tmap_a, a.a, 2, dims, strides, box, "A (K-major)")) != MGG_OK) return s;
+  } else {  // (hidden, T) with hidden contiguous: rows of T
+    const uint64_t dims[2] = {H, T}, strides[1] = {H * 2};
+    const uint32_t box[2] = {64, 64};
+    if ((s = encode_bf16(&Lc.tmap_a, a.a, 2, dims, strides, box, "A (M-major)")) != MGG_OK) return s;
+  }
+  if (a.b_major == MGG_MAJOR_MN) {  // (T, inter), inter contiguous
+    const uint64_t dims[2] = {I, T}, strides[1] = {I * 2};
+    const uint32_t box[2] = {64, 64};
+    if ((s = encode_bf16(&Lc.tmap_b, a.b, 2, dims, strides, box, "B (N-major)")) != MGG_OK) return s;
+  } else {  // (T, inter) with T contiguous: rows of T
+    const uint64_t dims[2] = {T, I}, strides[1] = {T * 2};
+    const uint32_t box[2] = {64, (uint32_t)Lc.tile_n};
+    if ((s = encode_bf16(&Lc.tmap_b, a.b, 2, dims, strides, box, "B (K-major)")) != MGG_OK) return s;
+  }
+  return from_cuda(launch_wgrad(Lc, static_cast<cudaStream_t>(stream)), "mgg_wgrad launch");
+}
+
+mgg_status mgg_read_device_status(const void* workspace, void* stream) {
+  g_err.clear();
+  if (workspace == nullptr) return fail(MGG_ERR_VALUE, "workspace is NULL");
+  int h[4] = {0, 0, 0, 0};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return from_cuda(e, "reading the device status");
+  if (h[0] != 0) {
+    g_err = std::string(mgg_status_string(h[0])) + " (where=" + std::to_string(h[1]) +
+            ", detail=" + std::to_string(h[2]) + ")";
+  }
+  return static_cast<mgg_status>(h[0]);
+}
+
+mgg_status mgg_test_encode_tmap_2d(void* out128, const void* addr, uint64_t dim0, uint64_t dim1,
+                                   uint64_t stride1_bytes, uint32_t box0, uint32_t box1) {
+  g_err.clear();
+  if (out128 == nullptr || (reinterpret_cast<uintptr_t>(out128) & 63u) != 0)
+    return fail(MGG_ERR_VALUE, "out128 must be 64-byte aligned host memory");
+  const uint64_t dims[2] = {dim0, dim1}, strides[1] = {stride1_bytes};
+  const uint32_t box[2] = {box0, box1};
+  return encode_bf16(static_cast<CUtensorMap*>(out128), addr, 2, dims, strides, box, "test");
+}
+
+mgg_status mgg_test_tmap_replace(const void* tmpl128, void* out_dev128, const void* addr, uint32_t dim0,
+                                 uint64_t stride1_bytes, int fields, void* stream) {
+  g_err.clear();
+  if (tmpl128 == nullptr || out_dev128 == nullptr) return fail(MGG_ERR_VALUE, "NULL descriptor");
+  if ((reinterpret_cast<uintptr_t>(out_dev128) & 127u) != 0)
+    return fail(MGG_ERR_VALUE, "out_dev128 must be 128-byte aligned");
+  CUtensorMap t;
+  memcpy(&t, tmpl128, sizeof(t));
+  return from_cuda(launch_tmap_replace_probe(t, out_dev128, addr, dim0, stride1_bytes, fields,
+                                             static_cast<cudaStream_t>(stream)),
+                   "tensormap replace probe");
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// Host-side declarations shared by the C-ABI layer and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "mgg.h"
+
+namespace mgg {
+
+// Workspace header (first 256 bytes of every workspace):
+//   int32 [0] status (0 = ok, else an mgg_status), [1] where, [2] detail,
+//   [3] dynamic tile counter, [4] number of active experts (wgrad)
+constexpr size_t kWsHeaderBytes = 256;
+constexpr size_t kTmapBytes = 128;
+
+struct DgluLaunch {
+  CUtensorMap tmap_a;
+  CUtensorMap tmap_b;  // dense 3-D map, or the per-expert template (discrete)
+  const mgg_dglu_bwd_args* args;
+  int num_sms;
+  int tile_n;
+};
+
+struct WgradLaunch {
+  CUtensorMap tmap_a;  // tensor2d map, or the per-expert template (ragged K-major)
+  CUtensorMap tmap_b;
+  const mgg_wgrad_args* args;
+  int num_sms;
+  int tile_n;
+  bool a_ragged;  // per-expert A maps built on the device
+  bool b_ragged;
+};
+
+// Launchers (queue the prep kernel, the persistent kernel and finalisers on `stream`).
+cudaError_t launch_dglu_bwd(const DgluLaunch& L, cudaStream_t stream);
+cudaError_t launch_wgrad(const WgradLaunch& L, cudaStream_t stream);
+
+// Test hook: copies `tmpl` into `out` on the device and replaces address / dim0 / stride of
+// dimension 1 there with tensormap.replace (the same code path the prep kernels use).
+cudaError_t launch_tmap_replace_probe(const CUtensorMap& tmpl, void* out, const void* addr, uint32_t dim0,
+                                      uint64_t stride1, int fields, cudaStream_t stream);
+
+constexpr int kDgluTileN = 256;
+int wgrad_tile_n(int64_t inter);
+
+}  // namespace mgg

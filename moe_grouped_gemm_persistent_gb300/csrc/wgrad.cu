@@ -1,0 +1,275 @@
+// Grouped weight gradient ("Grouped GEMM + WGrad (Unified)", "Operation"):
+//
+//   Wgrad[e] = A[:, begin:end] @ B[begin:end, :]    begin = offsets[e-1] (0 for e = 0), end = offsets[e]
+//
+// with A (hidden, T) and B (T, inter) in bf16, fp32 accumulation in TMEM, and the result
+// written (overwrite; zeros for an empty expert) or added (accumulate_on_output) to a
+// dense (L, hidden, inter) tensor or to per-expert output pointers.
+//
+// Scheduling: the preparation kernel orders experts by decreasing token count; the
+// persistent CTAs walk the (expert, hidden tile, inter tile) space in that order, so the
+// longest reductions start first (longest-processing-time-first).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "mgg_internal.h"
+#include "mgg_pipeline.cuh"
+
+namespace mgg {
+
+struct WgradParams {
+  CUtensorMap tmap_a;          // tensor2d A: K-major dims {T, h} box {64, 128}; M-major dims {h, T} box {64, 64}
+  CUtensorMap tmap_b;          // tensor2d B: N-major dims {i, T} box {64, 64}; K-major dims {T, i} box {64, BN}
+  const CUtensorMap* a_maps;   // tensor_ragged K-major A: per-expert maps (dims {K_e, h}), else null
+  const CUtensorMap* b_maps;   // tensor_ragged K-major B: per-expert maps (dims {K_e, i}), else null
+  const int32_t* offsets;
+  const int32_t* order;        // experts by decreasing token count (workspace)
+  void* out;
+  const int64_t* out_ptrs;
+  int* status;
+  int32_t* tile_log;
+  long long tile_log_cap;
+  long long total_tiles;
+  int hidden, inter, L;
+  int tiles_n, tiles_per_expert;
+  int a_mn, b_mn, out_dtype, accumulate;
+};
+
+template <int BN>
+struct WgradPolicy {
+  const WgradParams& p;
+  long long total_tiles;
+  int* status;
+  int a_mn, b_mn;
+
+  __device__ WgradPolicy(const WgradParams& prm)
+      : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(prm.a_mn), b_mn(prm.b_mn) {}
+
+  // s_table[0, L): offsets; s_table[1024, 1024 + L): expert order.
+  __device__ void load_tables(int* s_table) const {
+    for (int i = threadIdx.x; i < p.L; i += blockDim.x) {
+      s_table[i] = p.offsets[i];
+      s_table[1024 + i] = p.order[i];
+    }
+  }
+
+  __device__ TileWork tile(long long t, const int* s) const {
+    const int slot = (int)(t / p.tiles_per_expert);
+    const int local = (int)(t % p.tiles_per_expert);
+    const int e = s[1024 + slot];
+    const int begin = e ? s[e - 1] : 0;
+    const int end = s[e];
+    TileWork w;
+    w.expert = e;
+    w.active = (end > begin) || !p.accumulate;
+    w.m0 = (local / p.tiles_n) * BM;
+    w.n0 = (local % p.tiles_n) * BN;
+    w.k0 = begin;
+    w.num_kb = (end - begin) / BK;
+    return w;
+  }
+
+  __device__ void issue_loads(const TileWork& w, int kb, uint32_t sa, uint32_t sb, uint32_t bar) const {
+    const int k = w.k0 + kb * BK;
+    if (p.a_maps != nullptr) {
+      const CUtensorMap* m = p.a_maps + w.expert;
+      if (kb == 0) tmap_acquire(m);
+      tma_load_2d(sa, m, bar, kb * BK, w.m0);
+    } else if (!p.a_mn) {
+      tma_load_2d(sa, &p.tmap_a, bar, k, w.m0);
+    } else {
+      tma_load_2d(sa, &p.tmap_a, bar, w.m0, k);
+      tma_load_2d(sa + 8192, &p.tmap_a, bar, w.m0 + 64, k);
+    }
+    if (p.b_maps != nullptr) {
+      const CUtensorMap* m = p.b_maps + w.expert;
+      if (kb == 0) tmap_acquire(m);
+      tma_load_2d(sb, m, bar, kb * BK, w.n0);
+    } else if (p.b_mn) {
+#pragma unroll
+      for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, &p.tmap_b, bar, w.n0 + 64 * j, k);
+    } else {
+      tma_load_2d(sb, &p.tmap_b, bar, k, w.n0);
+    }
+  }
+
+  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, int q, int lane, bool have_acc,
+                           const int*) const {
+    const int e = w.expert;
+    const int row = w.m0 + q * 32 + lane;
+    const size_t inter = (size_t)p.inter;
+    char* base;
+    const size_t esz = p.out_dtype == MGG_FP32 ? 4 : 2;
+    if (p.out_ptrs != nullptr) base = reinterpret_cast<char*>(p.out_ptrs[e]);
+    else base = static_cast<char*>(p.out) + (size_t)e * (size_t)p.hidden * inter * esz;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int col0 = w.n0 + c * 32;
+      if (col0 >= p.inter) break;
+      float v[32];
+      if (have_acc) {
+        uint32_t r[32];
+        tmem_load_32cols(taddr + c * 32, r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = 0.f;
+      }
+      if (row < p.hidden) {
+        const int n = p.inter - col0 < 32 ? p.inter - col0 : 32;
+        const size_t idx = (size_t)row * inter + col0;
+        if (p.accumulate) {
+          float old[32];
+          load32_n(base, p.out_dtype, idx, old, n);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = old[k] + v[k];
+        }
+        store32(base, p.out_dtype, idx, v, n);
+      }
+    }
+    if (p.tile_log != nullptr && q == 0 && lane == 0 && t < p.tile_log_cap) {
+      int32_t* l = p.tile_log + 4 * t;
+      l[0] = e;
+      l[1] = w.m0;
+      l[2] = w.n0;
+      l[3] = (int32_t)blockIdx.x;
+    }
+  }
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constant__ WgradParams prm) {
+  const WgradPolicy<BN> pol(prm);
+  persistent_gemm<BN, STAGES>(pol);
+}
+
+// Checks offsets / output pointers, orders experts by decreasing token count and builds
+// the per-expert maps of tensor_ragged K-major operands.
+__global__ void wgrad_prep_kernel(const int32_t* offsets, int L, long long T, const int64_t* out_ptrs,
+                                  const __grid_constant__ CUtensorMap tmpl_a, const __grid_constant__ CUtensorMap tmpl_b,
+                                  const void* a, const void* b, int hidden, int inter, int a_ragged, int b_ragged,
+                                  CUtensorMap* a_maps, CUtensorMap* b_maps, int32_t* order, int* status) {
+  __shared__ int s_cnt[1024];
+  bool bad_off = false, bad_ptr = false;
+  for (int e = threadIdx.x; e < L; e += blockDim.x) {
+    const int prev = e ? offsets[e - 1] : 0;
+    const int cur = offsets[e];
+    if (cur < prev || ((cur - prev) & 255) != 0) bad_off = true;
+    if (e == L - 1 && (long long)cur != T) bad_off = true;
+    if (out_ptrs != nullptr) {
+      const long long ptr = out_ptrs[e];
+      if (ptr == 0 || (ptr & 15) != 0) bad_ptr = true;
+    }
+    s_cnt[e] = cur - prev;
+  }
+  const int any_off = __syncthreads_or(bad_off);
+  const int any_ptr = __syncthreads_or(bad_ptr);
+  if (threadIdx.x == 0) {
+    status[0] = any_off ? (int)MGG_ERR_DEVICE_OFFSETS : any_ptr ? (int)MGG_ERR_DEVICE_POINTER : 0;
+    status[1] = 0;
+    status[2] = 0;
+    status[3] = 0;
+  }
+  if (any_off || any_ptr) return;
+  // stable rank by decreasing count
+  for (int e = threadIdx.x; e < L; e += blockDim.x) {
+    const int ce = s_cnt[e];
+    int rank = 0;
+    for (int f = 0; f < L; ++f) {
+      const int cf = s_cnt[f];
+      rank += (cf > ce) || (cf == ce && f < e);
+    }
+    order[rank] = e;
+  }
+  if (!a_ragged && !b_ragged) return;
+  for (int e = threadIdx.x; e < L; e += blockDim.x) {
+    const int ke = s_cnt[e];
+    if (ke == 0) continue;
+    const int begin = e ? offsets[e - 1] : 0;
+    if (a_ragged) {
+      uint4* dst = reinterpret_cast<uint4*>(a_maps + e);
+      const uint4* src = reinterpret_cast<const uint4*>(&tmpl_a);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[i] = src[i];
+      tmap_replace_address(a_maps + e, static_cast<const __nv_bfloat16*>(a) + (size_t)begin * hidden);
+      tmap_replace_dim(a_maps + e, 0, (uint32_t)ke);
+      tmap_replace_stride0(a_maps + e, (uint64_t)ke * 2);
+    }
+    if (b_ragged) {
+      uint4* dst = reinterpret_cast<uint4*>(b_maps + e);
+      const uint4* src = reinterpret_cast<const uint4*>(&tmpl_b);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[i] = src[i];
+      tmap_replace_address(b_maps + e, static_cast<const __nv_bfloat16*>(b) + (size_t)begin * inter);
+      tmap_replace_dim(b_maps + e, 0, (uint32_t)ke);
+      tmap_replace_stride0(b_maps + e, (uint64_t)ke * 2);
+    }
+  }
+  tmap_release();
+}
+
+int wgrad_tile_n(int64_t inter) { return (inter % 256 == 0 || inter > 2048) ? 256 : 128; }
+
+template <int BN, int STAGES>
+static cudaError_t launch_wgrad_bn(const WgradLaunch& Lc, WgradParams& prm, cudaStream_t stream) {
+  using S = SmemLayout<BN, STAGES>;
+  static_assert(S::DYN_BYTES <= 232448, "shared memory");
+  auto kern = wgrad_kernel<BN, STAGES>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);
+  if (err != cudaSuccess) return err;
+  const int grid = (int)(prm.total_tiles < Lc.num_sms ? prm.total_tiles : Lc.num_sms);
+  kern<<<grid, kThreads, S::DYN_BYTES, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {
+  const mgg_wgrad_args& a = *Lc.args;
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  CUtensorMap* a_maps = reinterpret_cast<CUtensorMap*>(ws + kWsHeaderBytes);
+  CUtensorMap* b_maps = a_maps + a.L;
+  int32_t* order = reinterpret_cast<int32_t*>(ws + kWsHeaderBytes + 2 * kTmapBytes * (size_t)a.L);
+
+  wgrad_prep_kernel<<<1, 1024, 0, stream>>>(a.offsets, (int)a.L, (long long)a.tokens_sum, a.out_ptrs, Lc.tmap_a,
+                                            Lc.tmap_b, a.a, a.b, (int)a.hidden, (int)a.inter, Lc.a_ragged, Lc.b_ragged,
+                                            a_maps, b_maps, order, status);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+
+  const int BN = Lc.tile_n;
+  const long long tiles_m = (a.hidden + BM - 1) / BM;
+  const long long tiles_n = (a.inter + BN - 1) / BN;
+  const long long total = a.L * tiles_m * tiles_n;
+  if (a.tile_log != nullptr && a.tile_log_capacity > 0) {
+    err = cudaMemsetAsync(a.tile_log, 0xff, sizeof(int32_t) * 4 * (size_t)a.tile_log_capacity, stream);
+    if (err != cudaSuccess) return err;
+  }
+  if (total == 0) return cudaSuccess;
+  WgradParams prm;
+  prm.tmap_a = Lc.tmap_a;
+  prm.tmap_b = Lc.tmap_b;
+  prm.a_maps = Lc.a_ragged ? a_maps : nullptr;
+  prm.b_maps = Lc.b_ragged ? b_maps : nullptr;
+  prm.offsets = a.offsets;
+  prm.order = order;
+  prm.out = a.out;
+  prm.out_ptrs = a.out_ptrs;
+  prm.status = status;
+  prm.tile_log = a.tile_log;
+  prm.tile_log_cap = a.tile_log != nullptr ? a.tile_log_capacity : 0;
+  prm.total_tiles = total;
+  prm.hidden = (int)a.hidden;
+  prm.inter = (int)a.inter;
+  prm.L = (int)a.L;
+  prm.tiles_n = (int)tiles_n;
+  prm.tiles_per_expert = (int)(tiles_m * tiles_n);
+  prm.a_mn = (a.a_major == MGG_MAJOR_MN) ? 1 : 0;
+  prm.b_mn = (a.b_major == MGG_MAJOR_MN) ? 1 : 0;
+  prm.out_dtype = a.out_dtype;
+  prm.accumulate = a.accumulate != 0;
+  if (BN == 256) return launch_wgrad_bn<256, 4>(Lc, prm, stream);
+  return launch_wgrad_bn<128, 6>(Lc, prm, stream);
+}
+
+}  // namespace mgg

@@ -1,0 +1,122 @@
+"""The C-ABI library: it loads, exports what include/*.h declares, and its host-side
+validation rejects malformed arguments before anything is queued (no GPU needed)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from moe_grouped_gemm_persistent_gb300 import _lib
+from moe_grouped_gemm_persistent_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _lib.load()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(mgg_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "mgg_dglu_bwd" in names and "mgg_wgrad" in names and len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    bound = {s[0] for s in _lib.SIGNATURES}
+    assert names <= bound, names - bound
+
+
+def test_struct_layouts_match_library(lib):
+    assert lib.mgg_abi_version() == 1
+    assert lib.mgg_sizeof_dglu_bwd_args() == ctypes.sizeof(_lib.DgluBwdArgs)
+    assert lib.mgg_sizeof_wgrad_args() == ctypes.sizeof(_lib.WgradArgs)
+
+
+def test_sizes_and_tile_counts(lib):
+    assert lib.mgg_dglu_bwd_workspace_size(4, 128) == 256 + 4 * 128 + 4 * 256 * 4
+    assert lib.mgg_wgrad_workspace_size(64) % 256 == 0
+    assert lib.mgg_wgrad_workspace_size(64) >= 256 + 2 * 64 * 128 + 64 * 4
+    assert lib.mgg_dglu_bwd_num_tiles(1024, 128) == 8
+    assert lib.mgg_dglu_bwd_num_tiles(33536, 14336) == 262 * 56
+    assert lib.mgg_wgrad_num_tiles(64, 2048, 1408) == 64 * 16 * 11
+    assert lib.mgg_wgrad_num_tiles(256, 7168, 2048) == 256 * 56 * 8
+    for s in range(8):
+        assert lib.mgg_status_string(s).decode().startswith("MGG_")
+
+
+FAKE = 1 << 20  # an aligned address; validation never dereferences pointers
+
+
+def dglu_args(**over):
+    a = _lib.DgluBwdArgs()
+    a.M, a.K, a.N, a.L = 1024, 256, 128, 4
+    for f in ("a", "b", "c", "padded_offsets", "alpha", "beta", "prob", "dprob", "d_row", "workspace"):
+        setattr(a, f, FAKE)
+    a.workspace_bytes = 1 << 20
+    a.gate_first = 1
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def wgrad_args(**over):
+    a = _lib.WgradArgs()
+    a.hidden, a.inter, a.L, a.tokens_sum = 256, 128, 4, 1024
+    for f in ("a", "b", "offsets", "out", "workspace"):
+        setattr(a, f, FAKE)
+    a.workspace_bytes = 1 << 20
+    a.out_dtype = 2
+    a.b_major = 1
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(L=0), 1), (dict(L=1025), 1), (dict(M=1000), 1), (dict(K=100), 1), (dict(N=48), 1),
+    (dict(b_ptrs=FAKE), 1), (dict(b=None), 1), (dict(b_major=1), 1), (dict(c_dtype=3), 1),
+    (dict(d_dtype=-1), 1), (dict(act=2), 1), (dict(geglu_filter=5), 1), (dict(gate_first=2), 1),
+    (dict(a=FAKE + 8), 1), (dict(c=None), 1), (dict(dprob=FAKE + 4), 1), (dict(workspace=FAKE + 16), 1),
+    (dict(workspace_bytes=100), 1), (dict(reserved=1), 1), (dict(dbias=FAKE + 2), 1),
+    (dict(sched=1), 2), (dict(sched=7), 1),
+])
+def test_dglu_validation_rejects_before_launch(lib, over, expect):
+    st = lib.mgg_dglu_bwd(dglu_args(**over), None)
+    assert st == expect, lib.mgg_last_error()
+    assert lib.mgg_last_error()
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(L=0), 1), (dict(hidden=100), 1), (dict(inter=4), 1), (dict(tokens_sum=1000), 1),
+    (dict(out_ptrs=FAKE), 1), (dict(out=None), 1), (dict(a_major=3), 1), (dict(input_order=2), 1),
+    (dict(out_dtype=9), 1), (dict(accumulate=2), 1), (dict(b=FAKE + 8), 1), (dict(offsets=None), 1),
+    (dict(workspace_bytes=8), 1), (dict(reserved1=1), 1), (dict(sched=1), 2),
+])
+def test_wgrad_validation_rejects_before_launch(lib, over, expect):
+    st = lib.mgg_wgrad(wgrad_args(**over), None)
+    assert st == expect, lib.mgg_last_error()
+
+
+def test_null_args(lib):
+    assert lib.mgg_dglu_bwd(None, None) == 1
+    assert lib.mgg_wgrad(None, None) == 1
+
+
+def test_valid_args_without_device_report_arch(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.mgg_dglu_bwd(dglu_args(), None) == _lib.MGG_ERR_ARCH
+    assert lib.mgg_wgrad(wgrad_args(), None) == _lib.MGG_ERR_ARCH

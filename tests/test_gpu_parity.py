@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element by element,
+on seeded inputs that span several tiles and ragged tails, in every supported mode."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_grouped_gemm_persistent_gb300 import api, synth
+from moe_grouped_gemm_persistent_gb300.build import build
+
+from gpu_helpers import (TOL, TOL_DPROB, check_close, rel_fro, run_dglu_gpu, run_dglu_oracle, run_wgrad_gpu,
+                         run_wgrad_oracle, tiles_from_log, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    build()
+    return torch.device("cuda", 0)
+
+
+def _ranges(spec):
+    return oracle.expert_ranges(np.cumsum(spec.counts))
+
+
+# ------------------------------------------------------------------------------ tensor maps
+def test_tensormap_replace_matches_host_encoding(dev):
+    """Device-side rewriting of a descriptor equals the driver's encoding of the target (bytes)."""
+    from moe_grouped_gemm_persistent_gb300 import _lib
+    lib = _lib.load()
+    buf = torch.empty(1 << 22, dtype=torch.bfloat16, device=dev)
+    base = buf.data_ptr()
+    import ctypes
+    host = (ctypes.c_uint8 * 256)()
+    off = (-ctypes.addressof(host)) % 64
+    tmpl = ctypes.addressof(host) + off
+    exp_host = (ctypes.c_uint8 * 256)()
+    off2 = (-ctypes.addressof(exp_host)) % 64
+    exp = ctypes.addressof(exp_host) + off2
+    # template: dims {4096, 128}, stride 8192 B at base; target: dims {1536, 128}, stride 3072 B at base + 1 MiB
+    _lib.check(lib.mgg_test_encode_tmap_2d(tmpl, base, 4096, 128, 8192, 64, 128))
+    tgt = base + (1 << 20)
+    _lib.check(lib.mgg_test_encode_tmap_2d(exp, tgt, 1536, 128, 3072, 64, 128))
+    out = torch.zeros(256, dtype=torch.uint8, device=dev)
+    optr = out.data_ptr() + ((-out.data_ptr()) % 128)
+    _lib.check(lib.mgg_test_tmap_replace(tmpl, optr, tgt, 1536, 3072, 7, None))
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()[(optr - out.data_ptr()):(optr - out.data_ptr()) + 128]
+    want = np.frombuffer(bytes(exp_host)[off2:off2 + 128], dtype=np.uint8)
+    assert got.tobytes() == want.tobytes()
+    # address only
+    _lib.check(lib.mgg_test_encode_tmap_2d(exp, tgt, 4096, 128, 8192, 64, 128))
+    _lib.check(lib.mgg_test_tmap_replace(tmpl, optr, tgt, 0, 0, 1, None))
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()[(optr - out.data_ptr()):(optr - out.data_ptr()) + 128]
+    want = np.frombuffer(bytes(exp_host)[off2:off2 + 128], dtype=np.uint8)
+    assert got.tobytes() == want.tobytes()
+
+
+# ------------------------------------------------------------------------------ dgrad + dGLU
+DGLU_CASES = {
+    "swiglu_dense": dict(),
+    "swiglu_ktail_ntail": dict(K=328, N=160),
+    "geglu_value_fp32d_dbias": dict(act="dgeglu", c_std=4.0, d_dtype="fp32", dbias=True),
+    "swiglu_fp16": dict(c_dtype="fp16", d_dtype="fp16"),
+    "swiglu_fp32c": dict(c_dtype="fp32"),
+    "discrete_k": dict(b_mode="discrete", b_major="k"),
+    "discrete_n_geglu": dict(b_mode="discrete", b_major="n", act="dgeglu", c_std=4.0, dbias=True),
+    "wide_n": dict(N=544, K=192, counts=(512, 256)),
+}
+
+
+@pytest.mark.parametrize("case", list(DGLU_CASES))
+def test_dglu_bwd_parity(dev, case):
+    kw = dict(DGLU_CASES[case])
+    counts = kw.pop("counts", (256, 0, 512))
+    spec = synth.small_dglu_spec(case, L=len(counts), counts=counts, **kw)
+    x = synth.make_dglu_inputs(spec)
+    gpu = run_dglu_gpu(spec, x, dev, tile_log=True)
+    assert gpu["status"] == 0
+    ref = run_dglu_oracle(spec, x)
+    rows = [(lo, hi) for lo, hi in _ranges(spec)]
+    check_close("d_row", to_np(gpu["d_row"]), ref["d_row"], TOL[spec.d_dtype], rows)
+    check_close("dprob", to_np(gpu["dprob"]), ref["dprob"], TOL_DPROB, rows)
+    if spec.dbias:
+        check_close("dbias", to_np(gpu["dbias"]), ref["dbias"], TOL["bf16"])
+        for g, (lo, hi) in enumerate(rows):
+            if hi == lo:
+                assert (gpu["dbias"][g] == 0).all()
+    tm, tn = api.dglu_bwd_tile_shape()
+    want = oracle.dgrad_tiles(np.cumsum(spec.counts), spec.N, tm, tn)
+    np.testing.assert_array_equal(tiles_from_log(gpu["tile_log"]), want)
+
+
+@pytest.mark.parametrize("gate_first,filt", [(False, "value"), (True, "indicator"), (False, "indicator")])
+def test_dglu_block_order_and_filter_modes(dev, gate_first, filt):
+    spec = synth.small_dglu_spec("modes", act="dgeglu", c_std=4.0)
+    x = synth.make_dglu_inputs(spec)
+    gpu = run_dglu_gpu(spec, x, dev, gate_first=gate_first, geglu_filter=filt)
+    ref = run_dglu_oracle(spec, x, gate_first=gate_first, geglu_filter=filt)
+    check_close("d_row", to_np(gpu["d_row"]), ref["d_row"], TOL["bf16"])
+    check_close("dprob", to_np(gpu["dprob"]), ref["dprob"], TOL_DPROB)
+
+
+def test_dglu_accumulates_into_dprob_and_dbias(dev):
+    spec = synth.small_dglu_spec("acc", dbias=True)
+    x = synth.make_dglu_inputs(spec)
+    gen = torch.Generator().manual_seed(5)
+    dprob0 = torch.randn(spec.M, generator=gen)
+    dbias0 = torch.randn(spec.L, 2 * spec.N, generator=gen).to(torch.bfloat16)
+    gpu = run_dglu_gpu(spec, x, dev, dprob0=dprob0, dbias0=dbias0)
+    ref = run_dglu_oracle(spec, x, dprob0=dprob0, dbias0=dbias0)
+    check_close("dprob", to_np(gpu["dprob"]), ref["dprob"], TOL_DPROB)
+    check_close("dbias", to_np(gpu["dbias"]), ref["dbias"], TOL["bf16"])
+
+
+def test_dglu_tiny_workload(dev):
+    spec, _ = synth.workload_specs("tiny")
+    x = synth.make_dglu_inputs(spec)
+    gpu = run_dglu_gpu(spec, x, dev)
+    ref = run_dglu_oracle(spec, x)
+    check_close("d_row", to_np(gpu["d_row"]), ref["d_row"], TOL["bf16"], _ranges(spec))
+    check_close("dprob", to_np(gpu["dprob"]), ref["dprob"], TOL_DPROB)
+
+
+def test_dglu_bad_offsets_report_and_leave_outputs(dev):
+    spec = synth.small_dglu_spec("bad")
+    x = synth.make_dglu_inputs(spec)
+    x["padded_offsets"] = torch.tensor([256, 128, 768], dtype=torch.int32)  # decreasing
+    gpu = run_dglu_gpu(spec, x, dev)
+    assert gpu["status"] == 5
+    assert torch.isnan(gpu["d_row"].float()).all()
+    assert (gpu["dprob"] == 0).all()
+
+
+# ------------------------------------------------------------------------------ wgrad
+WGRAD_CASES = {
+    "k_n_fp32": dict(),
+    "k_n_fp32_acc": dict(accumulate=True),
+    "k_n_bf16": dict(out_dtype="bf16"),
+    "k_n_fp16_acc": dict(out_dtype="fp16", accumulate=True),
+    "m_n": dict(a_major="m"),
+    "k_k": dict(b_major="k"),
+    "m_k": dict(a_major="m", b_major="k"),
+    "ragged_k_n_discrete": dict(input_order="tensor_ragged", out_mode="discrete"),
+    "ragged_k_k": dict(input_order="tensor_ragged", b_major="k"),
+    "bn256": dict(inter=512, hidden=128, counts=(256, 768, 0)),
+}
+
+
+@pytest.mark.parametrize("case", list(WGRAD_CASES))
+def test_wgrad_parity(dev, case):
+    kw = dict(WGRAD_CASES[case])
+    counts = kw.pop("counts", (512, 0, 256, 768))
+    spec = synth.small_wgrad_spec(case, L=len(counts), counts=counts, **kw)
+    x = synth.make_wgrad_inputs(spec)
+    gpu = run_wgrad_gpu(spec, x, dev, tile_log=True)
+    assert gpu["status"] == 0
+    ref = run_wgrad_oracle(spec, x)
+    tol = TOL[spec.out_dtype]
+    for e in range(spec.L):
+        got = to_np(gpu["out"][e])
+        check_close(f"wgrad[{e}]", got, ref[e], tol)
+        if spec.counts[e] == 0 and not spec.accumulate:
+            assert (gpu["out"][e] == 0).all()
+    tm, tn = api.wgrad_tile_shape(spec.inter)
+    want = oracle.wgrad_tiles(np.cumsum(spec.counts), spec.hidden, spec.inter, tm, tn, spec.accumulate)
+    np.testing.assert_array_equal(tiles_from_log(gpu["tile_log"]), want)
+
+
+def test_wgrad_tiny_workload(dev):
+    _, spec = synth.workload_specs("tiny")
+    x = synth.make_wgrad_inputs(spec)
+    gpu = run_wgrad_gpu(spec, x, dev)
+    ref = run_wgrad_oracle(spec, x)
+    for e in range(spec.L):
+        check_close(f"wgrad[{e}]", to_np(gpu["out"][e]), ref[e], TOL["fp32"])
+
+
+def test_wgrad_sum_over_experts_equals_full_matmul(dev):
+    spec = synth.small_wgrad_spec("sum", counts=(256, 512, 256), L=3)
+    x = synth.make_wgrad_inputs(spec)
+    gpu = run_wgrad_gpu(spec, x, dev)
+    A = to_np(x["a"]).reshape(spec.hidden, spec.T)
+    B = to_np(x["b"]).reshape(spec.T, spec.inter)
+    total = to_np(gpu["out"]).sum(0)
+    assert rel_fro(total, A @ B) < TOL["fp32"]
+
+
+def test_wgrad_bad_pointer_reports(dev):
+    spec = synth.small_wgrad_spec("badptr", out_mode="discrete")
+    x = synth.make_wgrad_inputs(spec)
+    L, h, i = spec.L, spec.hidden, spec.inter
+    outs = [torch.zeros(h, i, device=dev) for _ in range(L)]
+    ptrs = api.pointer_array(outs, dev)
+    ptrs[1] += 4  # misaligned entry
+    ws = api.wgrad(a=x["a"].to(dev), b=x["b"].to(dev), offsets=x["offsets"].to(dev), hidden=h, inter=i,
+                   out_ptrs=ptrs, out_dtype="fp32")
+    assert api.read_device_status(ws) == 6
+    assert all((o == 0).all() for o in outs)
