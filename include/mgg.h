@@ -207,6 +207,17 @@ mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream);
 /* Grouped wgrad.  Queues its kernels on `stream` (a cudaStream_t). */
 mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream);
 
+/* Grouped wgrad for callers that cannot allocate device memory (no counterpart on the
+ * pages).  Same arguments and results as mgg_wgrad, except that `workspace` and
+ * `workspace_bytes` are ignored: the scratch lives in a fixed array inside the library's
+ * device memory, sized for at most 1024 experts (266,496 bytes, held on every GPU that loads
+ * the library until the process exits); L above that returns MGG_ERR_VALUE.  Nothing is
+ * allocated.  The first call on a device resolves the array's address with that device
+ * current: make it before any stream capture.  Every call shares the array and it keeps the
+ * last call's contents; calls that may overlap on the GPU race on it and must be ordered.
+ * The device-side status word of these calls is not exposed. */
+mgg_status mgg_wgrad_noalloc(const mgg_wgrad_args* args, void* stream);
+
 /* Waits for `stream`, then returns the device-side status word of the last call that
  * used `workspace` (MGG_OK, MGG_ERR_DEVICE_OFFSETS, MGG_ERR_DEVICE_POINTER or
  * MGG_ERR_DEVICE_TIMEOUT).  Synchronising; not for use inside stream capture. */

@@ -64,6 +64,7 @@ SIGNATURES = [
     ("mgg_wgrad_tile_shape", None, [c_int64, ctypes.POINTER(c_int32), ctypes.POINTER(c_int32)]),
     ("mgg_dglu_bwd", c_int, [ctypes.POINTER(DgluBwdArgs), c_void_p]),
     ("mgg_wgrad", c_int, [ctypes.POINTER(WgradArgs), c_void_p]),
+    ("mgg_wgrad_noalloc", c_int, [ctypes.POINTER(WgradArgs), c_void_p]),
     ("mgg_read_device_status", c_int, [c_void_p, c_void_p]),
     ("mgg_test_encode_tmap_2d", c_int, [c_void_p, c_void_p, c_uint64, c_uint64, c_uint64, c_uint32, c_uint32]),
     ("mgg_test_tmap_replace", c_int, [c_void_p, c_void_p, c_void_p, c_uint32, c_uint64, c_int, c_void_p]),

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmgg.so")
-SOURCES = ["mgg_api.cu", "dglu_bwd.cu", "wgrad.cu"]
+SOURCES = ["mgg_api.cu", "dglu_bwd.cu", "wgrad.cu", "wgrad_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
           "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

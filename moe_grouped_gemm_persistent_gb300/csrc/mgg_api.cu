@@ -176,6 +176,9 @@ mgg_status from_cuda(cudaError_t e, const char* what) {
 }
 
 }  // namespace
+
+void set_last_error(const std::string& msg) { g_err = msg; }
+
 }  // namespace mgg
 
 using namespace mgg;

@@ -44,6 +44,9 @@ cudaError_t launch_wgrad(const WgradLaunch& L, cudaStream_t stream);
 cudaError_t launch_tmap_replace_probe(const CUtensorMap& tmpl, void* out, const void* addr, uint32_t dim0,
                                       uint64_t stride1, int fields, cudaStream_t stream);
 
+// Sets the calling thread's mgg_last_error() message.
+void set_last_error(const std::string& msg);
+
 constexpr int kDgluTileN = 256;
 int wgrad_tile_n(int64_t inter);
 
