@@ -191,7 +191,7 @@ const char* mgg_status_string(int status);
 size_t mgg_dglu_bwd_workspace_size(int64_t L, int64_t N);
 
 /* Workspace bytes for mgg_wgrad with L experts (status word, per-expert tensor-map
- * slots, the expert order of the scheduler). */
+ * slots for ragged inputs and discrete outputs, the expert order of the scheduler). */
 size_t mgg_wgrad_workspace_size(int64_t L);
 
 /* Number of output tiles mgg_dglu_bwd / mgg_wgrad enumerate (tile_log capacity). */
@@ -210,7 +210,7 @@ mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream);
 /* Grouped wgrad for callers that cannot allocate device memory (no counterpart on the
  * pages).  Same arguments and results as mgg_wgrad, except that `workspace` and
  * `workspace_bytes` are ignored: the scratch lives in a fixed array inside the library's
- * device memory, sized for at most 1024 experts (266,496 bytes, held on every GPU that loads
+ * device memory, sized for at most 1024 experts (397,568 bytes, held on every GPU that loads
  * the library until the process exits); L above that returns MGG_ERR_VALUE.  Nothing is
  * allocated.  The first call on a device resolves the array's address with that device
  * current: make it before any stream capture.  Every call shares the array and it keeps the

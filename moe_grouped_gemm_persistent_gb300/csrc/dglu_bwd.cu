@@ -21,13 +21,13 @@ constexpr int kDgluStages = 4;
 struct DgluParams {
   CUtensorMap tmap_a;           // A (M, K): dims {K, M}, box {64, 128}, 128B swizzle
   CUtensorMap tmap_b;           // dense B (N, K, L): dims {K, N, L}, box {64, BN, 1}
+  CUtensorMap tmap_d;           // D_row (M, 2N): dims {2N, M}, box {128 B of columns, 32}, 128B swizzle
   const CUtensorMap* b_maps;    // discrete B: one map per expert in the workspace, else null
   const int32_t* offsets;
   const float* alpha;
   const float* beta;
   const float* prob;
   const void* c;
-  void* d;
   float* dprob;
   float* dbias_ws;              // fp32 partial sums (L, 2N), null = no dbias
   int* status;
@@ -40,10 +40,15 @@ struct DgluParams {
   int c_dtype, d_dtype, act, indicator, gate_first;
 };
 
-__device__ __forceinline__ float fast_sigmoid(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+__device__ __forceinline__ float fast_sigmoid(float x) { return rcp_approx(1.0f + __expf(-x)); }
 
-template <int BN>
+// Byte offset of 16-byte chunk `c16` of row `r` in a 128B-swizzled staging box (rows of 128 B).
+__device__ __forceinline__ uint32_t swz128(int r, int c16) { return (uint32_t)(r * 128 + ((c16 ^ (r & 7)) << 4)); }
+
+// CS / DS: element size in bytes of C and D_row (2 = bf16/fp16, 4 = fp32).
+template <int BN, int CS, int DS>
 struct DgluPolicy {
+  static constexpr int CV = 32 * CS / 16;  // 16-byte vectors per 32 elements of C
   const DgluParams& p;
   long long total_tiles;
   int* status;
@@ -52,25 +57,21 @@ struct DgluPolicy {
   __device__ DgluPolicy(const DgluParams& prm)
       : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(0), b_mn(prm.b_mn) {}
 
-  __device__ void load_tables(int* s_table) const {
-    for (int i = threadIdx.x; i < p.L; i += blockDim.x) s_table[i] = p.offsets[i];
-  }
-
   // Tile order: expert-major; inside an expert, column panels of BN, and inside a panel
   // the expert's 128-row blocks, so concurrently running CTAs share one B panel and the
   // expert's A rows in L2.  Tile t belongs to the expert containing row
   // floor(t / num_n) * 128 (its tiles occupy [begin/128 * num_n, end/128 * num_n)).
-  __device__ TileWork tile(long long t, const int* offs) const {
+  __device__ TileWork tile(long long t) const {
     const int row = (int)(t / p.num_n) * BM;
     int lo = 0, hi = p.L - 1;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (offs[mid] > row) hi = mid;
+      if (__ldg(p.offsets + mid) > row) hi = mid;
       else lo = mid + 1;
     }
     const int g = lo;
-    const int begin = g ? offs[g - 1] : 0;
-    const int mblocks = (offs[g] - begin) / BM;
+    const int begin = g ? __ldg(p.offsets + g - 1) : 0;
+    const int mblocks = (__ldg(p.offsets + g) - begin) / BM;
     const long long u = t - (long long)(begin / BM) * p.num_n;
     TileWork w;
     w.active = 1;
@@ -98,31 +99,97 @@ struct DgluPolicy {
     }
   }
 
-  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, int q, int lane, bool have_acc,
-                           const int*) const {
+  // Raw C of one row for compact columns [j0, j0 + 32): the gate block and the input block.
+  __device__ __forceinline__ void load_c(size_t row_off, int j0, uint4 (&g)[CV], uint4 (&in)[CV]) const {
+    const int first = 2 * j0, second = 2 * j0 + 32;
+    const int gcol = p.gate_first ? first : second;
+    const int icol = p.gate_first ? second : first;
+    const uint4* pg = reinterpret_cast<const uint4*>(static_cast<const char*>(p.c) + (row_off + gcol) * CS);
+    const uint4* pi = reinterpret_cast<const uint4*>(static_cast<const char*>(p.c) + (row_off + icol) * CS);
+#pragma unroll
+    for (int i = 0; i < CV; ++i) {
+      g[i] = __ldg(pg + i);
+      in[i] = __ldg(pi + i);
+    }
+  }
+
+  __device__ __forceinline__ void unpack_c(const uint4 (&raw)[CV], float (&v)[32]) const {
+    if constexpr (CS == 4) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[4 * i + 0] = __uint_as_float(raw[i].x);
+        v[4 * i + 1] = __uint_as_float(raw[i].y);
+        v[4 * i + 2] = __uint_as_float(raw[i].z);
+        v[4 * i + 3] = __uint_as_float(raw[i].w);
+      }
+    } else {
+      const bool bf = p.c_dtype == MGG_BF16;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (bf) {
+            v[8 * i + 2 * j + 0] = bf16_bits_to_float(w[j] & 0xffffu);
+            v[8 * i + 2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+          } else {
+            v[8 * i + 2 * j + 0] = __half2float(__ushort_as_half((unsigned short)(w[j] & 0xffffu)));
+            v[8 * i + 2 * j + 1] = __half2float(__ushort_as_half((unsigned short)(w[j] >> 16)));
+          }
+        }
+      }
+    }
+  }
+
+  // Writes 32 values of this lane's row into the staging box: 16-bit D uses one box of 64
+  // columns (block `blk` = chunks 4*blk .. 4*blk+3), fp32 D one box of 32 columns per block.
+  __device__ __forceinline__ void stage_block(uint32_t stg, int lane, int blk, const float (&v)[32]) const {
+    if constexpr (DS == 4) {
+      const uint32_t base = stg + blk * 4096;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        st_shared_v4(base + swz128(lane, i), __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                     __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+    } else {
+      const int dt = p.d_dtype;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        st_shared_v4(stg + swz128(lane, 4 * blk + i), pack2(v[8 * i], v[8 * i + 1], dt),
+                     pack2(v[8 * i + 2], v[8 * i + 3], dt), pack2(v[8 * i + 4], v[8 * i + 5], dt),
+                     pack2(v[8 * i + 6], v[8 * i + 7], dt));
+    }
+  }
+
+  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, int q, int lane, bool,
+                           uint8_t* stg_ptr, AccRelease rel) const {
     const int g = w.expert;
-    const float alpha_g = p.alpha[g];
+    const float alpha_g = __ldg(p.alpha + g);
     const float alpha2 = alpha_g * alpha_g;
-    const float beta_g = p.beta[g];
-    const int row = w.m0 + q * 32 + lane;
-    const float pr = p.prob[row];
+    const float beta_g = __ldg(p.beta + g);
+    const int row0 = w.m0 + q * 32;
+    const int row = row0 + lane;
+    const float pr = __ldg(p.prob + row);
     const size_t two_n = 2 * (size_t)p.N;
     const size_t row_off = (size_t)row * two_n;
     const bool geglu = p.act == MGG_ACT_DGEGLU;
+    const uint32_t stg = smem_u32(stg_ptr);
+    const int ncols = p.N - w.n0 < BN ? p.N - w.n0 : BN;
+    const int nchunks = ncols / 32;
     float dprob_acc = 0.f;
 
+    uint4 cg[CV], ci[CV];
+    load_c(row_off, w.n0, cg, ci);
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = 0; c < nchunks; ++c) {
       const int j0 = w.n0 + c * 32;
-      if (j0 >= p.N) break;
       uint32_t r[32];
       tmem_load_32cols(taddr + c * 32, r);
-      const int first = 2 * j0, second = 2 * j0 + 32;
-      const int gcol = p.gate_first ? first : second;
-      const int icol = p.gate_first ? second : first;
+      if (c == nchunks - 1) rel(lane);  // the MMA warp may reuse this accumulator now
+      uint4 ng[CV], ni[CV];
+      if (c + 1 < nchunks) load_c(row_off, j0 + 32, ng, ni);
       float gv[32], iv[32];
-      load32(p.c, p.c_dtype, row_off + gcol, gv);
-      load32(p.c, p.c_dtype, row_off + icol, iv);
+      unpack_c(cg, gv);
+      unpack_c(ci, iv);
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const float R = __fmul_rn(alpha2, __uint_as_float(r[k]));
@@ -136,30 +203,48 @@ struct DgluPolicy {
           dg = Rp * x_i * s * (1.0f + x_g * (1.0f - s));
           act = x_g * s * x_i;
         } else {
-          const float cg = fminf(x_g, 7.0f);
-          const float ci = fminf(fmaxf(x_i, -7.0f), 7.0f);
+          const float cgt = fminf(x_g, 7.0f);
+          const float cit = fminf(fmaxf(x_i, -7.0f), 7.0f);
           const bool g_in = x_g <= 7.0f;
           const bool i_in = (x_i >= -7.0f) && (x_i <= 7.0f);
           const float gf = g_in ? (p.indicator ? 1.0f : x_g) : 0.0f;
           const float inf_ = i_in ? (p.indicator ? 1.0f : x_i) : 0.0f;
-          const float s = fast_sigmoid(1.702f * cg);
-          const float ci1 = ci + 1.0f;
-          dg = Rp * ci1 * s * (1.0f + 1.702f * cg * (1.0f - s)) * gf;
-          di = Rp * cg * s * inf_;
-          act = cg * s * ci1;
+          const float s = fast_sigmoid(1.702f * cgt);
+          const float ci1 = cit + 1.0f;
+          dg = Rp * ci1 * s * (1.0f + 1.702f * cgt * (1.0f - s)) * gf;
+          di = Rp * cgt * s * inf_;
+          act = cgt * s * ci1;
         }
         dprob_acc += R * act;
         gv[k] = dg;
         iv[k] = di;
       }
-      store32(p.d, p.d_dtype, row_off + gcol, gv);
-      store32(p.d, p.d_dtype, row_off + icol, iv);
+      // the previous chunk's bulk store must have read the staging box before it is rewritten
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+      stage_block(stg, lane, p.gate_first ? 0 : 1, gv);
+      stage_block(stg, lane, p.gate_first ? 1 : 0, iv);
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.tmap_d, stg, 2 * j0, row0);
+        if constexpr (DS == 4) tma_store_2d(&p.tmap_d, stg + 4096, 2 * j0 + 32, row0);
+        bulk_commit_group();
+      }
       if (p.dbias_ws != nullptr) {
+        const int first = 2 * j0, second = 2 * j0 + 32;
+        const int gcol = p.gate_first ? first : second;
+        const int icol = p.gate_first ? second : first;
         float* ws = p.dbias_ws + (size_t)g * two_n;
         const float sg = warp_column_sums(gv, lane);
         const float si = warp_column_sums(iv, lane);
         atomicAdd(ws + gcol + lane, sg);
         atomicAdd(ws + icol + lane, si);
+      }
+#pragma unroll
+      for (int i = 0; i < CV; ++i) {
+        cg[i] = ng[i];
+        ci[i] = ni[i];
       }
     }
     atomicAdd(p.dprob + row, dprob_acc);
@@ -170,13 +255,12 @@ struct DgluPolicy {
       e[2] = w.n0;
       e[3] = (int32_t)blockIdx.x;
     }
-    (void)have_acc;
   }
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CS, int DS>
 __global__ void __launch_bounds__(kThreads, 1) dglu_bwd_kernel(const __grid_constant__ DgluParams prm) {
-  const DgluPolicy<BN> pol(prm);
+  const DgluPolicy<BN, CS, DS> pol(prm);
   persistent_gemm<BN, STAGES>(pol);
 }
 
@@ -250,13 +334,13 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     DgluParams prm;
     prm.tmap_a = Lc.tmap_a;
     prm.tmap_b = Lc.tmap_b;
+    prm.tmap_d = Lc.tmap_d;
     prm.b_maps = a.b_ptrs != nullptr ? maps : nullptr;
     prm.offsets = a.padded_offsets;
     prm.alpha = a.alpha;
     prm.beta = a.beta;
     prm.prob = a.prob;
     prm.c = a.c;
-    prm.d = a.d_row;
     prm.dprob = a.dprob;
     prm.dbias_ws = a.dbias != nullptr ? dbias_ws : nullptr;
     prm.status = status;
@@ -277,13 +361,11 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     prm.indicator = a.geglu_filter == MGG_FILTER_INDICATOR;
     prm.gate_first = a.gate_first != 0;
 
-    auto kern = dglu_bwd_kernel<BN, STAGES>;
-    static bool attr_set = false;
-    if (!attr_set) {
-      err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);
-      if (err != cudaSuccess) return err;
-      attr_set = true;
-    }
+    const int cs = a.c_dtype == MGG_FP32 ? 4 : 2, ds = a.d_dtype == MGG_FP32 ? 4 : 2;
+    void (*kern)(DgluParams) = cs == 2 ? (ds == 2 ? dglu_bwd_kernel<BN, STAGES, 2, 2> : dglu_bwd_kernel<BN, STAGES, 2, 4>)
+                                       : (ds == 2 ? dglu_bwd_kernel<BN, STAGES, 4, 2> : dglu_bwd_kernel<BN, STAGES, 4, 4>);
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);
+    if (err != cudaSuccess) return err;
     const int grid = (int)(total < Lc.num_sms ? total : Lc.num_sms);
     kern<<<grid, kThreads, S::DYN_BYTES, stream>>>(prm);
     err = cudaGetLastError();

@@ -43,9 +43,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 tiled map with 128-byte swizzle; dims[0] innermost; strides in bytes for dims 1..rank-1.
-mgg_status encode_bf16(CUtensorMap* map, const void* addr, int rank, const uint64_t* dims, const uint64_t* strides,
-                       const uint32_t* box, const char* what) {
+CUtensorMapDataType tmap_dtype(int d) {
+  return d == MGG_FP32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                       : d == MGG_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
+// Tiled map with 128-byte swizzle; dims[0] innermost; strides in bytes for dims 1..rank-1.
+mgg_status encode_map(CUtensorMap* map, int dtype, const void* addr, int rank, const uint64_t* dims,
+                      const uint64_t* strides, const uint32_t* box, const char* what) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return fail(MGG_ERR_RUNTIME, "cuTensorMapEncodeTiled is not available from the CUDA driver");
   cuuint64_t gdim[3], gstr[2];
@@ -55,13 +60,18 @@ mgg_status encode_bf16(CUtensorMap* map, const void* addr, int rank, const uint6
     bdim[i] = box[i];
   }
   for (int i = 0; i + 1 < rank; ++i) gstr[i] = strides[i];
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(addr), gdim, gstr,
+  const CUresult r = fn(map, tmap_dtype(dtype), (cuuint32_t)rank, const_cast<void*>(addr), gdim, gstr,
                         bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(MGG_ERR_RUNTIME, std::string("cuTensorMapEncodeTiled rejected the ") + what + " map (CUresult " +
                                      std::to_string((int)r) + ")");
   return MGG_OK;
+}
+
+mgg_status encode_bf16(CUtensorMap* map, const void* addr, int rank, const uint64_t* dims, const uint64_t* strides,
+                       const uint32_t* box, const char* what) {
+  return encode_map(map, MGG_BF16, addr, rank, dims, strides, box, what);
 }
 
 // ---------------------------------------------------------------- device check
@@ -214,7 +224,7 @@ size_t mgg_dglu_bwd_workspace_size(int64_t L, int64_t N) {
 
 size_t mgg_wgrad_workspace_size(int64_t L) {
   if (L < 0) return 0;
-  return round_up(kWsHeaderBytes + 2 * kTmapBytes * (size_t)L + sizeof(int32_t) * (size_t)L, 256);
+  return round_up(kWsHeaderBytes + 3 * kTmapBytes * (size_t)L + sizeof(int32_t) * (size_t)L, 256);
 }
 
 int64_t mgg_dglu_bwd_num_tiles(int64_t M, int64_t N) {
@@ -271,6 +281,12 @@ mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream) {
     const uint32_t box[2] = {64, 64};
     if ((s = encode_bf16(&Lc.tmap_b, a.a, 2, dims, strides, box, "discrete N-major B")) != MGG_OK) return s;
   }
+  {  // D_row (M, 2N): 32-row boxes of one 128-byte row of columns
+    const uint64_t esz = a.d_dtype == MGG_FP32 ? 4 : 2;
+    const uint64_t dims[2] = {2 * N, M}, strides[1] = {2 * N * esz};
+    const uint32_t box[2] = {(uint32_t)(128 / esz), 32};
+    if ((s = encode_map(&Lc.tmap_d, a.d_dtype, a.d_row, 2, dims, strides, box, "D_row")) != MGG_OK) return s;
+  }
   return from_cuda(launch_dglu_bwd(Lc, static_cast<cudaStream_t>(stream)), "mgg_dglu_bwd launch");
 }
 
@@ -309,6 +325,21 @@ mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {
     const uint64_t dims[2] = {T, I}, strides[1] = {T * 2};
     const uint32_t box[2] = {64, (uint32_t)Lc.tile_n};
     if ((s = encode_bf16(&Lc.tmap_b, a.b, 2, dims, strides, box, "B (K-major)")) != MGG_OK) return s;
+  }
+  {  // outputs: 32-row boxes of one 128-byte row of columns
+    const uint64_t esz = a.out_dtype == MGG_FP32 ? 4 : 2, L = (uint64_t)a.L;
+    const uint32_t cw = (uint32_t)(128 / esz);
+    if (a.out != nullptr) {
+      const uint64_t dims[3] = {I, H, L}, strides[2] = {I * esz, H * I * esz};
+      const uint32_t box[3] = {cw, 32, 1};
+      if ((s = encode_map(&Lc.tmap_out, a.out_dtype, a.out, 3, dims, strides, box, "dense output")) != MGG_OK)
+        return s;
+    } else {  // per-expert template; the preparation kernel substitutes each expert's address
+      const uint64_t dims[2] = {I, H}, strides[1] = {I * esz};
+      const uint32_t box[2] = {cw, 32};
+      if ((s = encode_map(&Lc.tmap_out, a.out_dtype, a.a, 2, dims, strides, box, "per-expert output")) != MGG_OK)
+        return s;
+    }
   }
   return from_cuda(launch_wgrad(Lc, static_cast<cudaStream_t>(stream)), "mgg_wgrad launch");
 }

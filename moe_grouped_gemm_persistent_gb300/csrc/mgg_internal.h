@@ -20,6 +20,7 @@ constexpr size_t kTmapBytes = 128;
 struct DgluLaunch {
   CUtensorMap tmap_a;
   CUtensorMap tmap_b;  // dense 3-D map, or the per-expert template (discrete)
+  CUtensorMap tmap_d;  // D_row store map
   const mgg_dglu_bwd_args* args;
   int num_sms;
   int tile_n;
@@ -28,6 +29,7 @@ struct DgluLaunch {
 struct WgradLaunch {
   CUtensorMap tmap_a;  // tensor2d map, or the per-expert template (ragged K-major)
   CUtensorMap tmap_b;
+  CUtensorMap tmap_out;  // dense output (3-D) map, or the per-expert template (discrete)
   const mgg_wgrad_args* args;
   int num_sms;
   int tile_n;

@@ -12,10 +12,12 @@
 //
 // The operation supplies a policy object P with
 //   total_tiles, status, a_mn, b_mn
-//   load_tables(int* s_table)                        all threads, before the roles start
-//   TileWork tile(long long t, const int* s_table)   same answer for every role
-//   issue_loads(w, kb, sa, sb, bar)                  producer thread
-//   epilogue(w, t, taddr, q, lane, have_acc, s_table) one epilogue warp
+//   TileWork tile(long long t)                      same answer for every role
+//   issue_loads(w, kb, sa, sb, bar)                 producer thread
+//   epilogue(w, t, taddr, q, lane, have_acc, stg, rel)  one epilogue warp; `stg` is this warp's
+//        1024-byte aligned staging buffer (kStageBytes) for bulk tensor stores, `rel` frees the
+//        TMEM accumulator and must be called once, after the warp's last tcgen05.ld of the tile
+//        (only when have_acc).
 #pragma once
 
 #include "mgg_ptx.cuh"
@@ -26,7 +28,8 @@ constexpr int BM = 128;     // tile rows = UMMA M (cta_group::1)
 constexpr int BK = 64;      // K elements per ring slot: one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;  // K of one kind::f16 MMA
 constexpr int kThreads = 192;
-constexpr int kTableInts = 2048;  // int32 tables staged in shared memory (offsets, order)
+constexpr int kEpiWarps = 4;
+constexpr int kStageBytes = 8192;  // per epilogue warp: output staging for bulk tensor stores
 
 struct TileWork {
   int active;   // 0: the tile is skipped by every role
@@ -41,13 +44,24 @@ struct SmemLayout {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = EPI_OFF + kEpiWarps * kStageBytes;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
-  static constexpr int TABLE_OFF = (MISC_OFF + 16 + 15) & ~15;
-  static constexpr int BYTES = TABLE_OFF + kTableInts * 4;
+  static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int DYN_BYTES = BYTES + 1024;  // slack to align the ring to 1024 B
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "ring slots must stay 1024-byte aligned");
+  static_assert(DYN_BYTES <= 232448, "shared memory per block");
+};
+
+// Frees one TMEM accumulator for the MMA warp (called by every lane of an epilogue warp).
+struct AccRelease {
+  uint64_t* bar;
+  __device__ __forceinline__ void operator()(int lane) const {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+  }
 };
 
 __host__ __device__ constexpr uint32_t tmem_cols_for(int cols) {
@@ -84,7 +98,6 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   uint64_t* done_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
-  int* s_table = reinterpret_cast<int*>(smem + S::TABLE_OFF);
 
   // The preparation kernel of this call found invalid device-side arguments.
   if (*reinterpret_cast<volatile int*>(p.status) != 0) return;
@@ -92,7 +105,6 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  p.load_tables(s_table);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -124,7 +136,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       long long issued = 0;
       bool ok = true;
       for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-        const TileWork w = p.tile(t, s_table);
+        const TileWork w = p.tile(t);
         if (!w.active) continue;
         for (int kb = 0; kb < w.num_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wg, 1)) {
@@ -159,7 +171,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       uint32_t phase = 0, local = 0;
       bool ok = true;
       for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-        const TileWork w = p.tile(t, s_table);
+        const TileWork w = p.tile(t);
         if (!w.active || w.num_kb == 0) continue;
         const uint32_t acc = local & 1u, use = local >> 1;
         if (!mbar_wait(&tempty_bar[acc], (use & 1u) ^ 1u, wg, 2)) break;
@@ -195,23 +207,24 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   } else {
     // ---------------------------------------------------------------- epilogue warps
     const int q = warp & 3;  // TMEM sub-partition this warp may access
+    uint8_t* stg = smem + S::EPI_OFF + (warp - 2) * kStageBytes;
     uint32_t local = 0;
     for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-      const TileWork w = p.tile(t, s_table);
+      const TileWork w = p.tile(t);
       if (!w.active) continue;
       if (w.num_kb == 0) {
-        p.epilogue(w, t, 0u, q, lane, false, s_table);
+        p.epilogue(w, t, 0u, q, lane, false, stg, AccRelease{nullptr});
         continue;
       }
       const uint32_t acc = local & 1u, use = local >> 1;
       if (!warp_wait(&tfull_bar[acc], use & 1u, wg, 4)) break;
       tc_fence_after();
-      p.epilogue(w, t, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, q, lane, true, s_table);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      p.epilogue(w, t, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, q, lane, true, stg,
+                 AccRelease{&tempty_bar[acc]});
       ++local;
     }
+    if (lane == 0) bulk_wait_all();  // bulk stores complete before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();

@@ -20,12 +20,14 @@ namespace mgg {
 struct WgradParams {
   CUtensorMap tmap_a;          // tensor2d A: K-major dims {T, h} box {64, 128}; M-major dims {h, T} box {64, 64}
   CUtensorMap tmap_b;          // tensor2d B: N-major dims {i, T} box {64, 64}; K-major dims {T, i} box {64, BN}
+  CUtensorMap tmap_out;        // dense output: dims {i, h, L}, box {128 B of columns, 32, 1}, 128B swizzle
   const CUtensorMap* a_maps;   // tensor_ragged K-major A: per-expert maps (dims {K_e, h}), else null
   const CUtensorMap* b_maps;   // tensor_ragged K-major B: per-expert maps (dims {K_e, i}), else null
+  const CUtensorMap* out_maps; // discrete outputs: per-expert maps (dims {i, h}), else null
   const int32_t* offsets;
   const int32_t* order;        // experts by decreasing token count (workspace)
-  void* out;
   const int64_t* out_ptrs;
+  const void* out;
   int* status;
   int32_t* tile_log;
   long long tile_log_cap;
@@ -35,8 +37,12 @@ struct WgradParams {
   int a_mn, b_mn, out_dtype, accumulate;
 };
 
-template <int BN>
+__device__ __forceinline__ uint32_t swz128w(int r, int c16) { return (uint32_t)(r * 128 + ((c16 ^ (r & 7)) << 4)); }
+
+// OS: output element size in bytes (2 = bf16/fp16, 4 = fp32).
+template <int BN, int OS>
 struct WgradPolicy {
+  static constexpr int CW = 128 / OS;  // output columns per staged chunk (one 128-byte row)
   const WgradParams& p;
   long long total_tiles;
   int* status;
@@ -45,20 +51,12 @@ struct WgradPolicy {
   __device__ WgradPolicy(const WgradParams& prm)
       : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(prm.a_mn), b_mn(prm.b_mn) {}
 
-  // s_table[0, L): offsets; s_table[1024, 1024 + L): expert order.
-  __device__ void load_tables(int* s_table) const {
-    for (int i = threadIdx.x; i < p.L; i += blockDim.x) {
-      s_table[i] = p.offsets[i];
-      s_table[1024 + i] = p.order[i];
-    }
-  }
-
-  __device__ TileWork tile(long long t, const int* s) const {
+  __device__ TileWork tile(long long t) const {
     const int slot = (int)(t / p.tiles_per_expert);
     const int local = (int)(t % p.tiles_per_expert);
-    const int e = s[1024 + slot];
-    const int begin = e ? s[e - 1] : 0;
-    const int end = s[e];
+    const int e = __ldg(p.order + slot);
+    const int begin = e ? __ldg(p.offsets + e - 1) : 0;
+    const int end = __ldg(p.offsets + e);
     TileWork w;
     w.expert = e;
     w.active = (end > begin) || !p.accumulate;
@@ -94,38 +92,77 @@ struct WgradPolicy {
   }
 
   __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, int q, int lane, bool have_acc,
-                           const int*) const {
+                           uint8_t* stg_ptr, AccRelease rel) const {
     const int e = w.expert;
-    const int row = w.m0 + q * 32 + lane;
-    const size_t inter = (size_t)p.inter;
-    char* base;
-    const size_t esz = p.out_dtype == MGG_FP32 ? 4 : 2;
-    if (p.out_ptrs != nullptr) base = reinterpret_cast<char*>(p.out_ptrs[e]);
-    else base = static_cast<char*>(p.out) + (size_t)e * (size_t)p.hidden * inter * esz;
+    const int row0 = w.m0 + q * 32;
+    const int row = row0 + lane;
+    const bool rows_in = row0 < p.hidden;
+    const uint32_t stg = smem_u32(stg_ptr);
+    const int ncols = p.inter - w.n0 < BN ? p.inter - w.n0 : BN;
+    const int nchunks = (ncols + CW - 1) / CW;
+    const bool discrete = p.out_maps != nullptr;
+    const CUtensorMap* map = discrete ? p.out_maps + e : &p.tmap_out;
+    if (discrete && lane == 0) tmap_acquire(map);
+    // fp32 accumulation is a bulk reduce-add at the memory side; 16-bit accumulation reads the old values
+    const bool reduce = p.accumulate && OS == 4;
+    const bool add_old = p.accumulate && OS == 2;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      const int col0 = w.n0 + c * 32;
-      if (col0 >= p.inter) break;
-      float v[32];
+    for (int c = 0; c < nchunks; ++c) {
+      const int col0 = w.n0 + c * CW;
+      float v[CW];
       if (have_acc) {
         uint32_t r[32];
-        tmem_load_32cols(taddr + c * 32, r);
+        tmem_load_32cols(taddr + c * CW, r);
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+        if constexpr (CW == 64) {
+          tmem_load_32cols(taddr + c * CW + 32, r);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[32 + k] = __uint_as_float(r[k]);
+        }
+        if (c == nchunks - 1) rel(lane);
       } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = 0.f;
+        for (int k = 0; k < CW; ++k) v[k] = 0.f;
       }
-      if (row < p.hidden) {
-        const int n = p.inter - col0 < 32 ? p.inter - col0 : 32;
-        const size_t idx = (size_t)row * inter + col0;
-        if (p.accumulate) {
-          float old[32];
-          load32_n(base, p.out_dtype, idx, old, n);
+      if (add_old && row < p.hidden) {
+        const char* base = discrete ? reinterpret_cast<const char*>(__ldg(p.out_ptrs + e))
+                                    : static_cast<const char*>(p.out) + (size_t)e * p.hidden * (size_t)p.inter * OS;
+        const int n = p.inter - col0 < CW ? p.inter - col0 : CW;
+        const size_t idx = (size_t)row * p.inter + col0;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = old[k] + v[k];
+        for (int h = 0; h < CW / 32; ++h) {
+          float old[32];
+          load32_n(base, p.out_dtype, idx + 32 * h, old, n - 32 * h);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[32 * h + k] += old[k];
         }
-        store32(base, p.out_dtype, idx, v, n);
+      }
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+      if constexpr (OS == 4) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          st_shared_v4(stg + swz128w(lane, i), __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                       __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+      } else {
+        const int dt = p.out_dtype;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          st_shared_v4(stg + swz128w(lane, i), pack2(v[8 * i], v[8 * i + 1], dt), pack2(v[8 * i + 2], v[8 * i + 3], dt),
+                       pack2(v[8 * i + 4], v[8 * i + 5], dt), pack2(v[8 * i + 6], v[8 * i + 7], dt));
+      }
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0 && rows_in) {
+        if (discrete) {
+          if (reduce) tma_reduce_add_2d(map, stg, col0, row0);
+          else tma_store_2d(map, stg, col0, row0);
+        } else {
+          if (reduce) tma_reduce_add_3d(map, stg, col0, row0, e);
+          else tma_store_3d(map, stg, col0, row0, e);
+        }
+        bulk_commit_group();
       }
     }
     if (p.tile_log != nullptr && q == 0 && lane == 0 && t < p.tile_log_cap) {
@@ -138,9 +175,9 @@ struct WgradPolicy {
   }
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int OS>
 __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constant__ WgradParams prm) {
-  const WgradPolicy<BN> pol(prm);
+  const WgradPolicy<BN, OS> pol(prm);
   persistent_gemm<BN, STAGES>(pol);
 }
 
@@ -148,8 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
 // the per-expert maps of tensor_ragged K-major operands.
 __global__ void wgrad_prep_kernel(const int32_t* offsets, int L, long long T, const int64_t* out_ptrs,
                                   const __grid_constant__ CUtensorMap tmpl_a, const __grid_constant__ CUtensorMap tmpl_b,
-                                  const void* a, const void* b, int hidden, int inter, int a_ragged, int b_ragged,
-                                  CUtensorMap* a_maps, CUtensorMap* b_maps, int32_t* order, int* status) {
+                                  const __grid_constant__ CUtensorMap tmpl_out, const void* a, const void* b,
+                                  int hidden, int inter, int a_ragged, int b_ragged, CUtensorMap* a_maps,
+                                  CUtensorMap* b_maps, CUtensorMap* out_maps, int32_t* order, int* status) {
   __shared__ int s_cnt[1024];
   bool bad_off = false, bad_ptr = false;
   for (int e = threadIdx.x; e < L; e += blockDim.x) {
@@ -182,8 +220,15 @@ __global__ void wgrad_prep_kernel(const int32_t* offsets, int L, long long T, co
     }
     order[rank] = e;
   }
-  if (!a_ragged && !b_ragged) return;
+  if (!a_ragged && !b_ragged && out_ptrs == nullptr) return;
   for (int e = threadIdx.x; e < L; e += blockDim.x) {
+    if (out_ptrs != nullptr) {  // every expert, empty ones included (zero-filled in overwrite mode)
+      uint4* dst = reinterpret_cast<uint4*>(out_maps + e);
+      const uint4* src = reinterpret_cast<const uint4*>(&tmpl_out);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[i] = src[i];
+      tmap_replace_address(out_maps + e, reinterpret_cast<const void*>(out_ptrs[e]));
+    }
     const int ke = s_cnt[e];
     if (ke == 0) continue;
     const int begin = e ? offsets[e - 1] : 0;
@@ -211,11 +256,11 @@ __global__ void wgrad_prep_kernel(const int32_t* offsets, int L, long long T, co
 
 int wgrad_tile_n(int64_t inter) { return (inter % 256 == 0 || inter > 2048) ? 256 : 128; }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int OS>
 static cudaError_t launch_wgrad_bn(const WgradLaunch& Lc, WgradParams& prm, cudaStream_t stream) {
   using S = SmemLayout<BN, STAGES>;
   static_assert(S::DYN_BYTES <= 232448, "shared memory");
-  auto kern = wgrad_kernel<BN, STAGES>;
+  auto kern = wgrad_kernel<BN, STAGES, OS>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);
   if (err != cudaSuccess) return err;
   const int grid = (int)(prm.total_tiles < Lc.num_sms ? prm.total_tiles : Lc.num_sms);
@@ -229,11 +274,12 @@ cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {
   int* status = reinterpret_cast<int*>(ws);
   CUtensorMap* a_maps = reinterpret_cast<CUtensorMap*>(ws + kWsHeaderBytes);
   CUtensorMap* b_maps = a_maps + a.L;
-  int32_t* order = reinterpret_cast<int32_t*>(ws + kWsHeaderBytes + 2 * kTmapBytes * (size_t)a.L);
+  CUtensorMap* out_maps = b_maps + a.L;
+  int32_t* order = reinterpret_cast<int32_t*>(ws + kWsHeaderBytes + 3 * kTmapBytes * (size_t)a.L);
 
   wgrad_prep_kernel<<<1, 1024, 0, stream>>>(a.offsets, (int)a.L, (long long)a.tokens_sum, a.out_ptrs, Lc.tmap_a,
-                                            Lc.tmap_b, a.a, a.b, (int)a.hidden, (int)a.inter, Lc.a_ragged, Lc.b_ragged,
-                                            a_maps, b_maps, order, status);
+                                            Lc.tmap_b, Lc.tmap_out, a.a, a.b, (int)a.hidden, (int)a.inter,
+                                            Lc.a_ragged, Lc.b_ragged, a_maps, b_maps, out_maps, order, status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
@@ -249,8 +295,10 @@ cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {
   WgradParams prm;
   prm.tmap_a = Lc.tmap_a;
   prm.tmap_b = Lc.tmap_b;
+  prm.tmap_out = Lc.tmap_out;
   prm.a_maps = Lc.a_ragged ? a_maps : nullptr;
   prm.b_maps = Lc.b_ragged ? b_maps : nullptr;
+  prm.out_maps = a.out_ptrs != nullptr ? out_maps : nullptr;
   prm.offsets = a.offsets;
   prm.order = order;
   prm.out = a.out;
@@ -268,8 +316,9 @@ cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {
   prm.b_mn = (a.b_major == MGG_MAJOR_MN) ? 1 : 0;
   prm.out_dtype = a.out_dtype;
   prm.accumulate = a.accumulate != 0;
-  if (BN == 256) return launch_wgrad_bn<256, 4>(Lc, prm, stream);
-  return launch_wgrad_bn<128, 6>(Lc, prm, stream);
+  const bool fp32 = a.out_dtype == MGG_FP32;
+  if (BN == 256) return fp32 ? launch_wgrad_bn<256, 4, 4>(Lc, prm, stream) : launch_wgrad_bn<256, 4, 2>(Lc, prm, stream);
+  return fp32 ? launch_wgrad_bn<128, 6, 4>(Lc, prm, stream) : launch_wgrad_bn<128, 6, 2>(Lc, prm, stream);
 }
 
 }  // namespace mgg

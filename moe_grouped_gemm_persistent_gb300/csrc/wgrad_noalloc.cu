@@ -30,9 +30,9 @@
 namespace {
 
 constexpr int kNoAllocMaxExperts = 1024;
-// 256-byte header + 2 tensor maps (128 B) per expert + 4-byte expert order entry, rounded to 256.
+// 256-byte header + 3 tensor maps (128 B) per expert + 4-byte expert order entry, rounded to 256.
 constexpr size_t kNoAllocScratchBytes =
-    ((256 + 2 * 128 * (size_t)kNoAllocMaxExperts + 4 * (size_t)kNoAllocMaxExperts) + 255) / 256 * 256;
+    ((256 + 3 * 128 * (size_t)kNoAllocMaxExperts + 4 * (size_t)kNoAllocMaxExperts) + 255) / 256 * 256;
 
 static __device__ __align__(256) unsigned char g_wgrad_scratch[kNoAllocScratchBytes];
 

@@ -47,7 +47,7 @@ def test_struct_layouts_match_library(lib):
 def test_sizes_and_tile_counts(lib):
     assert lib.mgg_dglu_bwd_workspace_size(4, 128) == 256 + 4 * 128 + 4 * 256 * 4
     assert lib.mgg_wgrad_workspace_size(64) % 256 == 0
-    assert lib.mgg_wgrad_workspace_size(64) >= 256 + 2 * 64 * 128 + 64 * 4
+    assert lib.mgg_wgrad_workspace_size(64) >= 256 + 3 * 64 * 128 + 64 * 4
     assert lib.mgg_dglu_bwd_num_tiles(1024, 128) == 8
     assert lib.mgg_dglu_bwd_num_tiles(33536, 14336) == 262 * 56
     assert lib.mgg_wgrad_num_tiles(64, 2048, 1408) == 64 * 16 * 11
