@@ -17,6 +17,7 @@
 namespace mgg {
 
 constexpr int kDgluStages = 4;
+constexpr int kDgluEpiWarps = 8;  // two warps per TMEM sub-partition: the dGLU epilogue is latency-bound
 
 struct DgluParams {
   CUtensorMap tmap_a;           // A (M, K): dims {K, M}, box {64, 128}, 128B swizzle
@@ -48,6 +49,8 @@ __device__ __forceinline__ uint32_t swz128(int r, int c16) { return (uint32_t)(r
 // CS / DS: element size in bytes of C and D_row (2 = bf16/fp16, 4 = fp32).
 template <int BN, int CS, int DS>
 struct DgluPolicy {
+  static constexpr int EPI_WARPS = kDgluEpiWarps;
+  static constexpr int kEpiHalves = EPI_WARPS / 4;
   static constexpr int CV = 32 * CS / 16;  // 16-byte vectors per 32 elements of C
   const DgluParams& p;
   long long total_tiles;
@@ -142,13 +145,13 @@ struct DgluPolicy {
   }
 
   // Writes 32 values of this lane's row into the staging box: 16-bit D uses one box of 64
-  // columns (block `blk` = chunks 4*blk .. 4*blk+3), fp32 D one box of 32 columns per block.
+  // columns (block `blk` = chunks 4*blk .. 4*blk+3), fp32 D one box of 32 columns.
   __device__ __forceinline__ void stage_block(uint32_t stg, int lane, int blk, const float (&v)[32]) const {
     if constexpr (DS == 4) {
-      const uint32_t base = stg + blk * 4096;
+      (void)blk;
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        st_shared_v4(base + swz128(lane, i), __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+        st_shared_v4(stg + swz128(lane, i), __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
                      __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
     } else {
       const int dt = p.d_dtype;
@@ -160,7 +163,22 @@ struct DgluPolicy {
     }
   }
 
-  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, int q, int lane, bool,
+  // The staging box must no longer be read by an earlier bulk store before it is rewritten.
+  __device__ __forceinline__ void staging_free(int lane) const {
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+  }
+
+  __device__ __forceinline__ void staging_flush(uint32_t stg, int lane, int x, int y) const {
+    fence_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&p.tmap_d, stg, x, y);
+      bulk_commit_group();
+    }
+  }
+
+  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, int q, int half, int lane, bool,
                            uint8_t* stg_ptr, AccRelease rel) const {
     const int g = w.expert;
     const float alpha_g = __ldg(p.alpha + g);
@@ -176,17 +194,21 @@ struct DgluPolicy {
     const int ncols = p.N - w.n0 < BN ? p.N - w.n0 : BN;
     const int nchunks = ncols / 32;
     float dprob_acc = 0.f;
+    bool released = false;
 
     uint4 cg[CV], ci[CV];
-    load_c(row_off, w.n0, cg, ci);
+    if (half < nchunks) load_c(row_off, w.n0 + 32 * half, cg, ci);
 #pragma unroll 1
-    for (int c = 0; c < nchunks; ++c) {
+    for (int c = half; c < nchunks; c += kEpiHalves) {
       const int j0 = w.n0 + c * 32;
       uint32_t r[32];
       tmem_load_32cols(taddr + c * 32, r);
-      if (c == nchunks - 1) rel(lane);  // the MMA warp may reuse this accumulator now
+      if (c + kEpiHalves >= nchunks) {  // this warp's last read: the MMA warp may reuse the accumulator
+        rel(lane);
+        released = true;
+      }
       uint4 ng[CV], ni[CV];
-      if (c + 1 < nchunks) load_c(row_off, j0 + 32, ng, ni);
+      if (c + kEpiHalves < nchunks) load_c(row_off, j0 + 32 * kEpiHalves, ng, ni);
       float gv[32], iv[32];
       unpack_c(cg, gv);
       unpack_c(ci, iv);
@@ -219,17 +241,19 @@ struct DgluPolicy {
         gv[k] = dg;
         iv[k] = di;
       }
-      // the previous chunk's bulk store must have read the staging box before it is rewritten
-      if (lane == 0) bulk_wait_read_all();
-      __syncwarp();
-      stage_block(stg, lane, p.gate_first ? 0 : 1, gv);
-      stage_block(stg, lane, p.gate_first ? 1 : 0, iv);
-      fence_async_shared();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(&p.tmap_d, stg, 2 * j0, row0);
-        if constexpr (DS == 4) tma_store_2d(&p.tmap_d, stg + 4096, 2 * j0 + 32, row0);
-        bulk_commit_group();
+      if constexpr (DS == 2) {  // both 32-column blocks in one 64-column box
+        staging_free(lane);
+        stage_block(stg, lane, p.gate_first ? 0 : 1, gv);
+        stage_block(stg, lane, p.gate_first ? 1 : 0, iv);
+        staging_flush(stg, lane, 2 * j0, row0);
+      } else {  // fp32: one box per block, through the same buffer
+        const int first = 2 * j0, second = 2 * j0 + 32;
+        staging_free(lane);
+        stage_block(stg, lane, 0, gv);
+        staging_flush(stg, lane, p.gate_first ? first : second, row0);
+        staging_free(lane);
+        stage_block(stg, lane, 0, iv);
+        staging_flush(stg, lane, p.gate_first ? second : first, row0);
       }
       if (p.dbias_ws != nullptr) {
         const int first = 2 * j0, second = 2 * j0 + 32;
@@ -247,8 +271,9 @@ struct DgluPolicy {
         ci[i] = ni[i];
       }
     }
-    atomicAdd(p.dprob + row, dprob_acc);
-    if (p.tile_log != nullptr && q == 0 && lane == 0 && t < p.tile_log_cap) {
+    if (!released) rel(lane);
+    if (half < nchunks) atomicAdd(p.dprob + row, dprob_acc);
+    if (p.tile_log != nullptr && q == 0 && half == 0 && lane == 0 && t < p.tile_log_cap) {
       int32_t* e = p.tile_log + 4 * t;
       e[0] = g;
       e[1] = w.m0;
@@ -259,7 +284,7 @@ struct DgluPolicy {
 };
 
 template <int BN, int STAGES, int CS, int DS>
-__global__ void __launch_bounds__(kThreads, 1) dglu_bwd_kernel(const __grid_constant__ DgluParams prm) {
+__global__ void __launch_bounds__(cta_threads(kDgluEpiWarps), 1) dglu_bwd_kernel(const __grid_constant__ DgluParams prm) {
   const DgluPolicy<BN, CS, DS> pol(prm);
   persistent_gemm<BN, STAGES>(pol);
 }
@@ -308,7 +333,7 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
   const mgg_dglu_bwd_args& a = *Lc.args;
   constexpr int BN = kDgluTileN;
   constexpr int STAGES = kDgluStages;
-  using S = SmemLayout<BN, STAGES>;
+  using S = SmemLayout<BN, STAGES, kDgluEpiWarps>;
   static_assert(S::DYN_BYTES <= 232448, "shared memory");
 
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -367,7 +392,7 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);
     if (err != cudaSuccess) return err;
     const int grid = (int)(total < Lc.num_sms ? total : Lc.num_sms);
-    kern<<<grid, kThreads, S::DYN_BYTES, stream>>>(prm);
+    kern<<<grid, cta_threads(kDgluEpiWarps), S::DYN_BYTES, stream>>>(prm);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }

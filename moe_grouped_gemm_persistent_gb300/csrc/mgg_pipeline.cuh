@@ -14,10 +14,12 @@
 //   total_tiles, status, a_mn, b_mn
 //   TileWork tile(long long t)                      same answer for every role
 //   issue_loads(w, kb, sa, sb, bar)                 producer thread
-//   epilogue(w, t, taddr, q, lane, have_acc, stg, rel)  one epilogue warp; `stg` is this warp's
-//        1024-byte aligned staging buffer (kStageBytes) for bulk tensor stores, `rel` frees the
-//        TMEM accumulator and must be called once, after the warp's last tcgen05.ld of the tile
-//        (only when have_acc).
+//   EPI_WARPS                                       epilogue warps (multiple of 4)
+//   epilogue(w, t, taddr, q, half, lane, have_acc, stg, rel)  one epilogue warp; EPI_WARPS/4 warps
+//        share TMEM sub-partition q and split the tile's 32-column chunks (chunk c belongs to
+//        half c % (EPI_WARPS/4)); `stg` is this warp's 1024-byte aligned staging buffer
+//        (kStageBytes) for bulk tensor stores; `rel` frees the TMEM accumulator and must be
+//        called exactly once per tile when have_acc, after the warp's last tcgen05.ld of it.
 #pragma once
 
 #include "mgg_ptx.cuh"
@@ -27,9 +29,10 @@ namespace mgg {
 constexpr int BM = 128;     // tile rows = UMMA M (cta_group::1)
 constexpr int BK = 64;      // K elements per ring slot: one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;  // K of one kind::f16 MMA
-constexpr int kThreads = 192;
-constexpr int kEpiWarps = 4;
-constexpr int kStageBytes = 8192;  // per epilogue warp: output staging for bulk tensor stores
+constexpr int kStageBytes = 4096;  // per epilogue warp: one 32-row x 128-byte staging box
+
+// Threads of a CTA with `epi_warps` epilogue warps (a multiple of 4) after the producer and MMA warps.
+__host__ __device__ constexpr int cta_threads(int epi_warps) { return 64 + 32 * epi_warps; }
 
 struct TileWork {
   int active;   // 0: the tile is skipped by every role
@@ -39,13 +42,13 @@ struct TileWork {
   int num_kb;   // number of BK slices; 0 = no MMA (the epilogue writes without TMEM)
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EPI_WARPS>
 struct SmemLayout {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFF = EPI_OFF + kEpiWarps * kStageBytes;
+  static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * kStageBytes;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int BYTES = MISC_OFF + 16;
@@ -85,7 +88,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, WaitGu
 
 template <int BN, int STAGES, class P>
 __device__ __forceinline__ void persistent_gemm(const P& p) {
-  using S = SmemLayout<BN, STAGES>;
+  constexpr int kEpiWarps = P::EPI_WARPS;
+  static_assert(kEpiWarps % 4 == 0, "whole TMEM sub-partitions");
+  using S = SmemLayout<BN, STAGES, kEpiWarps>;
   constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N");
 
@@ -112,7 +117,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], 4);  // one arrival per epilogue warp
+      mbar_init(&tempty_bar[a], kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -206,20 +211,21 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     }
   } else {
     // ---------------------------------------------------------------- epilogue warps
-    const int q = warp & 3;  // TMEM sub-partition this warp may access
+    const int q = warp & 3;             // TMEM sub-partition this warp may access
+    const int half = (warp - 2) >> 2;   // which of the sub-partition's warps
     uint8_t* stg = smem + S::EPI_OFF + (warp - 2) * kStageBytes;
     uint32_t local = 0;
     for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
       const TileWork w = p.tile(t);
       if (!w.active) continue;
       if (w.num_kb == 0) {
-        p.epilogue(w, t, 0u, q, lane, false, stg, AccRelease{nullptr});
+        p.epilogue(w, t, 0u, q, half, lane, false, stg, AccRelease{nullptr});
         continue;
       }
       const uint32_t acc = local & 1u, use = local >> 1;
       if (!warp_wait(&tfull_bar[acc], use & 1u, wg, 4)) break;
       tc_fence_after();
-      p.epilogue(w, t, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, q, lane, true, stg,
+      p.epilogue(w, t, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, q, half, lane, true, stg,
                  AccRelease{&tempty_bar[acc]});
       ++local;
     }

@@ -37,11 +37,15 @@ struct WgradParams {
   int a_mn, b_mn, out_dtype, accumulate;
 };
 
+constexpr int kWgradEpiWarps = 4;
+
 __device__ __forceinline__ uint32_t swz128w(int r, int c16) { return (uint32_t)(r * 128 + ((c16 ^ (r & 7)) << 4)); }
 
 // OS: output element size in bytes (2 = bf16/fp16, 4 = fp32).
 template <int BN, int OS>
 struct WgradPolicy {
+  static constexpr int EPI_WARPS = kWgradEpiWarps;
+  static constexpr int kEpiHalves = EPI_WARPS / 4;
   static constexpr int CW = 128 / OS;  // output columns per staged chunk (one 128-byte row)
   const WgradParams& p;
   long long total_tiles;
@@ -91,8 +95,8 @@ struct WgradPolicy {
     }
   }
 
-  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, int q, int lane, bool have_acc,
-                           uint8_t* stg_ptr, AccRelease rel) const {
+  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, int q, int half, int lane,
+                           bool have_acc, uint8_t* stg_ptr, AccRelease rel) const {
     const int e = w.expert;
     const int row0 = w.m0 + q * 32;
     const int row = row0 + lane;
@@ -106,8 +110,9 @@ struct WgradPolicy {
     // fp32 accumulation is a bulk reduce-add at the memory side; 16-bit accumulation reads the old values
     const bool reduce = p.accumulate && OS == 4;
     const bool add_old = p.accumulate && OS == 2;
+    bool released = false;
 #pragma unroll 1
-    for (int c = 0; c < nchunks; ++c) {
+    for (int c = half; c < nchunks; c += kEpiHalves) {
       const int col0 = w.n0 + c * CW;
       float v[CW];
       if (have_acc) {
@@ -120,7 +125,10 @@ struct WgradPolicy {
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[32 + k] = __uint_as_float(r[k]);
         }
-        if (c == nchunks - 1) rel(lane);
+        if (c + kEpiHalves >= nchunks) {
+          rel(lane);
+          released = true;
+        }
       } else {
 #pragma unroll
         for (int k = 0; k < CW; ++k) v[k] = 0.f;
@@ -165,7 +173,8 @@ struct WgradPolicy {
         bulk_commit_group();
       }
     }
-    if (p.tile_log != nullptr && q == 0 && lane == 0 && t < p.tile_log_cap) {
+    if (have_acc && !released) rel(lane);
+    if (p.tile_log != nullptr && q == 0 && half == 0 && lane == 0 && t < p.tile_log_cap) {
       int32_t* l = p.tile_log + 4 * t;
       l[0] = e;
       l[1] = w.m0;
@@ -176,7 +185,7 @@ struct WgradPolicy {
 };
 
 template <int BN, int STAGES, int OS>
-__global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constant__ WgradParams prm) {
+__global__ void __launch_bounds__(cta_threads(kWgradEpiWarps), 1) wgrad_kernel(const __grid_constant__ WgradParams prm) {
   const WgradPolicy<BN, OS> pol(prm);
   persistent_gemm<BN, STAGES>(pol);
 }
@@ -258,13 +267,13 @@ int wgrad_tile_n(int64_t inter) { return (inter % 256 == 0 || inter > 2048) ? 25
 
 template <int BN, int STAGES, int OS>
 static cudaError_t launch_wgrad_bn(const WgradLaunch& Lc, WgradParams& prm, cudaStream_t stream) {
-  using S = SmemLayout<BN, STAGES>;
+  using S = SmemLayout<BN, STAGES, kWgradEpiWarps>;
   static_assert(S::DYN_BYTES <= 232448, "shared memory");
   auto kern = wgrad_kernel<BN, STAGES, OS>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);
   if (err != cudaSuccess) return err;
   const int grid = (int)(prm.total_tiles < Lc.num_sms ? prm.total_tiles : Lc.num_sms);
-  kern<<<grid, kThreads, S::DYN_BYTES, stream>>>(prm);
+  kern<<<grid, cta_threads(kWgradEpiWarps), S::DYN_BYTES, stream>>>(prm);
   return cudaGetLastError();
 }
 
