@@ -101,7 +101,7 @@ def dglu_bwd(*, a: torch.Tensor, c: torch.Tensor, padded_offsets: torch.Tensor, 
              beta: torch.Tensor, prob: torch.Tensor, dprob: torch.Tensor, d_row: torch.Tensor,
              b: Optional[torch.Tensor] = None, b_ptrs: Optional[torch.Tensor] = None, N: Optional[int] = None,
              dbias: Optional[torch.Tensor] = None, act: str = "dswiglu", geglu_filter: str = "value",
-             gate_first: bool = True, b_major: str = "k", sched: str = "static",
+             gate_first: bool = True, b_major: str = "k", sched: str = "dynamic",
              workspace: Optional[torch.Tensor] = None, tile_log: Optional[torch.Tensor] = None, stream=None):
     """Grouped GEMM + dGLU backward (see include/mgg.h, mgg_dglu_bwd).
 
@@ -148,7 +148,7 @@ def make_wgrad_args(*, a, b, offsets, hidden, inter, out=None, out_ptrs=None, ou
 def wgrad(*, a: torch.Tensor, b: torch.Tensor, offsets: torch.Tensor, hidden: int, inter: int,
           out: Optional[torch.Tensor] = None, out_ptrs: Optional[torch.Tensor] = None,
           out_dtype: Optional[str] = None, a_major: str = "k", b_major: str = "n", input_order: str = "tensor2d",
-          accumulate: bool = False, sched: str = "static", workspace: Optional[torch.Tensor] = None,
+          accumulate: bool = False, sched: str = "dynamic", workspace: Optional[torch.Tensor] = None,
           tile_log: Optional[torch.Tensor] = None, stream=None):
     """Grouped wgrad (see include/mgg.h, mgg_wgrad).  ``a``/``b`` are the flat bf16 storage
     of A (hidden, T) and B (T, inter) in the declared majors / input order."""

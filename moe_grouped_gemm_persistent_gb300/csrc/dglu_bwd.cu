@@ -35,6 +35,7 @@ struct DgluParams {
   int32_t* tile_log;
   long long tile_log_cap;
   long long total_tiles;
+  int dynamic;                  // 1: tiles claimed from the workspace counter
   int M, K, N, L;
   int num_n, num_kb;
   int a_mn, b_mn;
@@ -56,9 +57,10 @@ struct DgluPolicy {
   long long total_tiles;
   int* status;
   int a_mn, b_mn;
+  int dynamic;
 
   __device__ DgluPolicy(const DgluParams& prm)
-      : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(0), b_mn(prm.b_mn) {}
+      : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(0), b_mn(prm.b_mn), dynamic(prm.dynamic) {}
 
   // Tile order: expert-major; inside an expert, column panels of BN, and inside a panel
   // the expert's 128-row blocks, so concurrently running CTAs share one B panel and the
@@ -372,6 +374,7 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     prm.tile_log = a.tile_log;
     prm.tile_log_cap = a.tile_log != nullptr ? a.tile_log_capacity : 0;
     prm.total_tiles = total;
+    prm.dynamic = a.sched == MGG_SCHED_DYNAMIC;
     prm.M = (int)a.M;
     prm.K = (int)a.K;
     prm.N = (int)a.N;

@@ -115,7 +115,6 @@ mgg_status validate_dglu(const mgg_dglu_bwd_args& a) {
     return fail(MGG_ERR_VALUE, "geglu_filter must be VALUE or INDICATOR");
   if (a.gate_first != 0 && a.gate_first != 1) return fail(MGG_ERR_VALUE, "gate_first must be 0 or 1");
   if (a.sched != MGG_SCHED_STATIC && a.sched != MGG_SCHED_DYNAMIC) return fail(MGG_ERR_VALUE, "sched out of range");
-  if (a.sched == MGG_SCHED_DYNAMIC) return fail(MGG_ERR_UNSUPPORTED, "dynamic scheduling is not available yet");
   if (a.reserved != 0) return fail(MGG_ERR_VALUE, "reserved field must be 0");
   const void* req[] = {a.a, a.c, a.padded_offsets, a.alpha, a.beta, a.prob, a.dprob, a.d_row, a.workspace};
   const char* names[] = {"a", "c", "padded_offsets", "alpha", "beta", "prob", "dprob", "d_row", "workspace"};
@@ -158,7 +157,6 @@ mgg_status validate_wgrad(const mgg_wgrad_args& a) {
   if (!valid_dtype(a.out_dtype)) return fail(MGG_ERR_VALUE, "out_dtype out of range");
   if (a.accumulate != 0 && a.accumulate != 1) return fail(MGG_ERR_VALUE, "accumulate must be 0 or 1");
   if (a.sched != MGG_SCHED_STATIC && a.sched != MGG_SCHED_DYNAMIC) return fail(MGG_ERR_VALUE, "sched out of range");
-  if (a.sched == MGG_SCHED_DYNAMIC) return fail(MGG_ERR_UNSUPPORTED, "dynamic scheduling is not available yet");
   if (a.reserved0 != 0 || a.reserved1 != 0) return fail(MGG_ERR_VALUE, "reserved fields must be 0");
   const void* req[] = {a.a, a.b, a.offsets, a.workspace};
   const char* names[] = {"a", "b", "offsets", "workspace"};

@@ -11,7 +11,8 @@
 //               accumulates the next tile into the other TMEM buffer.
 //
 // The operation supplies a policy object P with
-//   total_tiles, status, a_mn, b_mn
+//   total_tiles, status, a_mn, b_mn, dynamic        status[3] is the dynamic scheduler's tile
+//                                                   counter (zeroed by the preparation kernel)
 //   TileWork tile(long long t)                      same answer for every role
 //   issue_loads(w, kb, sa, sb, bar)                 producer thread
 //   EPI_WARPS                                       epilogue warps (multiple of 4)
@@ -30,6 +31,7 @@ constexpr int BM = 128;     // tile rows = UMMA M (cta_group::1)
 constexpr int BK = 64;      // K elements per ring slot: one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;  // K of one kind::f16 MMA
 constexpr int kStageBytes = 4096;  // per epilogue warp: one 32-row x 128-byte staging box
+constexpr int kSchedRing = 8;      // tile indices in flight from the producer to the other roles
 
 // Threads of a CTA with `epi_warps` epilogue warps (a multiple of 4) after the producer and MMA warps.
 __host__ __device__ constexpr int cta_threads(int epi_warps) { return 64 + 32 * epi_warps; }
@@ -49,8 +51,9 @@ struct SmemLayout {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * kStageBytes;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
-  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * kSchedRing;
+  static constexpr int SCHED_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int MISC_OFF = SCHED_OFF + kSchedRing * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int DYN_BYTES = BYTES + 1024;  // slack to align the ring to 1024 B
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "ring slots must stay 1024-byte aligned");
@@ -101,6 +104,9 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   uint64_t* tfull_bar = empty_bar + STAGES;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* done_bar = tempty_bar + 2;
+  uint64_t* sfull_bar = done_bar + 1;           // [kSchedRing] a tile index was published
+  uint64_t* sempty_bar = sfull_bar + kSchedRing;  // [kSchedRing] every role has read it
+  volatile long long* sched_ring = reinterpret_cast<volatile long long*>(smem + S::SCHED_OFF);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
 
@@ -120,6 +126,10 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       mbar_init(&tempty_bar[a], kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(done_bar, 1);
+    for (int r = 0; r < kSchedRing; ++r) {
+      mbar_init(&sfull_bar[r], 1);
+      mbar_init(&sempty_bar[r], 1 + kEpiWarps);  // the MMA thread and every epilogue warp
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -132,6 +142,23 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const WaitGuard wg{abort_flag, p.status};
+  const bool dynamic = p.dynamic != 0;
+  const long long kEnd = 0x7fffffffffffffffLL;
+
+  // Static schedule: CTA b takes tiles b, b + grid, ...  Dynamic schedule: the producer thread
+  // claims the next tile from the global counter and publishes it to the MMA thread and the
+  // epilogue warps through sched_ring; every role sees the same tile sequence.
+  auto static_tile = [&](long long n) -> long long { return (long long)blockIdx.x + n * (long long)gridDim.x; };
+  auto consume_tile = [&](long long n, bool is_warp) -> long long {
+    const int r = (int)(n % kSchedRing);
+    const uint32_t ph = (uint32_t)((n / kSchedRing) & 1);
+    const bool ok = is_warp ? warp_wait(&sfull_bar[r], ph, wg, 6) : mbar_wait(&sfull_bar[r], ph, wg, 6);
+    if (!ok) return kEnd;
+    const long long t = sched_ring[r];
+    if (is_warp) __syncwarp();
+    if (!is_warp || lane == 0) mbar_arrive(&sempty_bar[r]);
+    return t;
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -140,7 +167,18 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+      int* counter = p.status + 3;
+      auto produce_tile = [&](long long n) -> long long {
+        if (!dynamic) return static_tile(n);
+        const int r = (int)(n % kSchedRing);
+        if (!mbar_wait(&sempty_bar[r], (uint32_t)(((n / kSchedRing) & 1) ^ 1), wg, 5)) return kEnd;
+        const long long t = atomicAdd(counter, 1);
+        sched_ring[r] = t;
+        mbar_arrive(&sfull_bar[r]);
+        return t;
+      };
+      long long n_tile = 0;
+      for (long long t = produce_tile(n_tile++); t < p.total_tiles && ok; t = produce_tile(n_tile++)) {
         const TileWork w = p.tile(t);
         if (!w.active) continue;
         for (int kb = 0; kb < w.num_kb; ++kb) {
@@ -175,7 +213,9 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       int stage = 0;
       uint32_t phase = 0, local = 0;
       bool ok = true;
-      for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+      long long n_tile = 0;
+      auto next_tile = [&]() { const long long n = n_tile++; return dynamic ? consume_tile(n, false) : static_tile(n); };
+      for (long long t = next_tile(); t < p.total_tiles && ok; t = next_tile()) {
         const TileWork w = p.tile(t);
         if (!w.active || w.num_kb == 0) continue;
         const uint32_t acc = local & 1u, use = local >> 1;
@@ -215,7 +255,9 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     const int half = (warp - 2) >> 2;   // which of the sub-partition's warps
     uint8_t* stg = smem + S::EPI_OFF + (warp - 2) * kStageBytes;
     uint32_t local = 0;
-    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    long long n_tile = 0;
+    auto next_tile = [&]() { const long long n = n_tile++; return dynamic ? consume_tile(n, true) : static_tile(n); };
+    for (long long t = next_tile(); t < p.total_tiles; t = next_tile()) {
       const TileWork w = p.tile(t);
       if (!w.active) continue;
       if (w.num_kb == 0) {

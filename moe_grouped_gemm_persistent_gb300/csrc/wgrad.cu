@@ -32,6 +32,7 @@ struct WgradParams {
   int32_t* tile_log;
   long long tile_log_cap;
   long long total_tiles;
+  int dynamic;                  // 1: tiles claimed from the workspace counter
   int hidden, inter, L;
   int tiles_n, tiles_per_expert;
   int a_mn, b_mn, out_dtype, accumulate;
@@ -51,9 +52,11 @@ struct WgradPolicy {
   long long total_tiles;
   int* status;
   int a_mn, b_mn;
+  int dynamic;
 
   __device__ WgradPolicy(const WgradParams& prm)
-      : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(prm.a_mn), b_mn(prm.b_mn) {}
+      : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(prm.a_mn), b_mn(prm.b_mn),
+        dynamic(prm.dynamic) {}
 
   __device__ TileWork tile(long long t) const {
     const int slot = (int)(t / p.tiles_per_expert);
@@ -316,6 +319,7 @@ cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {
   prm.tile_log = a.tile_log;
   prm.tile_log_cap = a.tile_log != nullptr ? a.tile_log_capacity : 0;
   prm.total_tiles = total;
+  prm.dynamic = a.sched == MGG_SCHED_DYNAMIC;
   prm.hidden = (int)a.hidden;
   prm.inter = (int)a.inter;
   prm.L = (int)a.L;

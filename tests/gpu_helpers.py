@@ -48,7 +48,7 @@ def dglu_b_getter(spec, b):
 
 
 def run_dglu_gpu(spec, x, dev, gate_first=True, geglu_filter="value", dprob0=None, dbias0=None, tile_log=False,
-                 dbias=None):
+                 dbias=None, sched="static"):
     """Runs mgg_dglu_bwd on inputs x (CPU tensors from synth) and returns the outputs on CPU."""
     M, N, L = spec.M, spec.N, spec.L
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
@@ -69,7 +69,7 @@ def run_dglu_gpu(spec, x, dev, gate_first=True, geglu_filter="value", dprob0=Non
         log = torch.empty(4 * api.dglu_bwd_num_tiles(M, N), dtype=torch.int32, device=dev)
     ws = api.dglu_bwd(a=g["a"], c=g["c"], padded_offsets=g["padded_offsets"], alpha=g["alpha"], beta=g["beta"],
                       prob=g["prob"], dprob=dprob, d_row=d_row, dbias=db, act=spec.act, geglu_filter=geglu_filter,
-                      gate_first=gate_first, tile_log=log, **b_kw)
+                      gate_first=gate_first, tile_log=log, sched=sched, **b_kw)
     status = api.read_device_status(ws)
     torch.cuda.synchronize()
     out = dict(status=status, d_row=d_row.cpu(), dprob=dprob.cpu(), dbias=None if db is None else db.cpu(),
@@ -93,7 +93,7 @@ def wgrad_pack(spec, x):
     return x["a"], x["b"]
 
 
-def run_wgrad_gpu(spec, x, dev, tile_log=False):
+def run_wgrad_gpu(spec, x, dev, tile_log=False, sched="static"):
     L, h, i = spec.L, spec.hidden, spec.inter
     a = x["a"].to(dev)
     b = x["b"].to(dev)
@@ -114,7 +114,7 @@ def run_wgrad_gpu(spec, x, dev, tile_log=False):
     if tile_log:
         log = torch.empty(4 * api.wgrad_num_tiles(L, h, i), dtype=torch.int32, device=dev)
     ws = api.wgrad(a=a, b=b, offsets=offs, hidden=h, inter=i, a_major=spec.a_major, b_major=spec.b_major,
-                   input_order=spec.input_order, accumulate=spec.accumulate, tile_log=log, **kw)
+                   input_order=spec.input_order, accumulate=spec.accumulate, tile_log=log, sched=sched, **kw)
     status = api.read_device_status(ws)
     torch.cuda.synchronize()
     res = out.cpu() if outs is None else torch.stack([o.cpu() for o in outs])

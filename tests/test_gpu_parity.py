@@ -71,13 +71,18 @@ DGLU_CASES = {
 }
 
 
-@pytest.mark.parametrize("case", list(DGLU_CASES))
-def test_dglu_bwd_parity(dev, case):
+DGLU_SCHED = [(c, "static") for c in DGLU_CASES] + [("swiglu_dense", "dynamic"), ("discrete_n_geglu", "dynamic"),
+                                                      ("many_experts", "dynamic")]
+DGLU_CASES["many_experts"] = dict(K=128, N=64, counts=(256, 0, 0, 512, 256, 0, 768, 256, 256, 0, 512))
+
+
+@pytest.mark.parametrize("case,sched", DGLU_SCHED)
+def test_dglu_bwd_parity(dev, case, sched):
     kw = dict(DGLU_CASES[case])
     counts = kw.pop("counts", (256, 0, 512))
     spec = synth.small_dglu_spec(case, L=len(counts), counts=counts, **kw)
     x = synth.make_dglu_inputs(spec)
-    gpu = run_dglu_gpu(spec, x, dev, tile_log=True)
+    gpu = run_dglu_gpu(spec, x, dev, tile_log=True, sched=sched)
     assert gpu["status"] == 0
     ref = run_dglu_oracle(spec, x)
     rows = [(lo, hi) for lo, hi in _ranges(spec)]
@@ -149,13 +154,18 @@ WGRAD_CASES = {
 }
 
 
-@pytest.mark.parametrize("case", list(WGRAD_CASES))
-def test_wgrad_parity(dev, case):
+WGRAD_SCHED = [(c, "static") for c in WGRAD_CASES] + [("k_n_fp32", "dynamic"), ("k_n_fp32_acc", "dynamic"),
+                                                        ("ragged_k_n_discrete", "dynamic"), ("many_experts", "dynamic")]
+WGRAD_CASES["many_experts"] = dict(hidden=256, inter=128, counts=(256, 0, 2048, 0, 512, 256, 0, 768, 256, 1024))
+
+
+@pytest.mark.parametrize("case,sched", WGRAD_SCHED)
+def test_wgrad_parity(dev, case, sched):
     kw = dict(WGRAD_CASES[case])
     counts = kw.pop("counts", (512, 0, 256, 768))
     spec = synth.small_wgrad_spec(case, L=len(counts), counts=counts, **kw)
     x = synth.make_wgrad_inputs(spec)
-    gpu = run_wgrad_gpu(spec, x, dev, tile_log=True)
+    gpu = run_wgrad_gpu(spec, x, dev, tile_log=True, sched=sched)
     assert gpu["status"] == 0
     ref = run_wgrad_oracle(spec, x)
     tol = TOL[spec.out_dtype]
