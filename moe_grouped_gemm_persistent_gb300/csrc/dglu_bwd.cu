@@ -16,7 +16,8 @@
 
 namespace mgg {
 
-constexpr int kDgluStages = 4;
+constexpr int kDgluStages = 4;     // 16-bit D_row
+constexpr int kDgluStagesF32 = 3;  // fp32 D_row: one ring slot traded for 8 KB staging per warp
 constexpr int kDgluEpiWarps = 8;  // two warps per TMEM sub-partition: the dGLU epilogue is latency-bound
 
 struct DgluParams {
@@ -51,6 +52,7 @@ __device__ __forceinline__ uint32_t swz128(int r, int c16) { return (uint32_t)(r
 template <int BN, int CS, int DS>
 struct DgluPolicy {
   static constexpr int EPI_WARPS = kDgluEpiWarps;
+  static constexpr int STG_BYTES = DS == 4 ? 8192 : 4096;  // fp32 D: the gate and the input box
   static constexpr int kEpiHalves = EPI_WARPS / 4;
   static constexpr int CV = 32 * CS / 16;  // 16-byte vectors per 32 elements of C
   const DgluParams& p;
@@ -248,14 +250,18 @@ struct DgluPolicy {
         stage_block(stg, lane, p.gate_first ? 0 : 1, gv);
         stage_block(stg, lane, p.gate_first ? 1 : 0, iv);
         staging_flush(stg, lane, 2 * j0, row0);
-      } else {  // fp32: one box per block, through the same buffer
+      } else {  // fp32: one 32-column box per block
         const int first = 2 * j0, second = 2 * j0 + 32;
         staging_free(lane);
         stage_block(stg, lane, 0, gv);
-        staging_flush(stg, lane, p.gate_first ? first : second, row0);
-        staging_free(lane);
-        stage_block(stg, lane, 0, iv);
-        staging_flush(stg, lane, p.gate_first ? second : first, row0);
+        stage_block(stg + 4096, lane, 0, iv);
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&p.tmap_d, stg, p.gate_first ? first : second, row0);
+          tma_store_2d(&p.tmap_d, stg + 4096, p.gate_first ? second : first, row0);
+          bulk_commit_group();
+        }
       }
       if (p.dbias_ws != nullptr) {
         const int first = 2 * j0, second = 2 * j0 + 32;
@@ -285,10 +291,15 @@ struct DgluPolicy {
   }
 };
 
-template <int BN, int STAGES, int CS, int DS>
+template <int BN, int CS, int DS>
 __global__ void __launch_bounds__(cta_threads(kDgluEpiWarps), 1) dglu_bwd_kernel(const __grid_constant__ DgluParams prm) {
   const DgluPolicy<BN, CS, DS> pol(prm);
-  persistent_gemm<BN, STAGES>(pol);
+  persistent_gemm<BN, DS == 4 ? kDgluStagesF32 : kDgluStages>(pol);
+}
+
+template <int BN, int DS>
+constexpr int dglu_smem_bytes() {
+  return SmemLayout<BN, DS == 4 ? kDgluStagesF32 : kDgluStages, kDgluEpiWarps, DS == 4 ? 8192 : 4096>::DYN_BYTES;
 }
 
 // Checks the device-resident arguments and builds the per-expert weight maps.
@@ -334,9 +345,6 @@ __global__ void dbias_finalize_kernel(const float* ws, __nv_bfloat16* dbias, lon
 cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
   const mgg_dglu_bwd_args& a = *Lc.args;
   constexpr int BN = kDgluTileN;
-  constexpr int STAGES = kDgluStages;
-  using S = SmemLayout<BN, STAGES, kDgluEpiWarps>;
-  static_assert(S::DYN_BYTES <= 232448, "shared memory");
 
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   int* status = reinterpret_cast<int*>(ws);
@@ -390,12 +398,13 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     prm.gate_first = a.gate_first != 0;
 
     const int cs = a.c_dtype == MGG_FP32 ? 4 : 2, ds = a.d_dtype == MGG_FP32 ? 4 : 2;
-    void (*kern)(DgluParams) = cs == 2 ? (ds == 2 ? dglu_bwd_kernel<BN, STAGES, 2, 2> : dglu_bwd_kernel<BN, STAGES, 2, 4>)
-                                       : (ds == 2 ? dglu_bwd_kernel<BN, STAGES, 4, 2> : dglu_bwd_kernel<BN, STAGES, 4, 4>);
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);
+    void (*kern)(DgluParams) = cs == 2 ? (ds == 2 ? dglu_bwd_kernel<BN, 2, 2> : dglu_bwd_kernel<BN, 2, 4>)
+                                       : (ds == 2 ? dglu_bwd_kernel<BN, 4, 2> : dglu_bwd_kernel<BN, 4, 4>);
+    const int smem = ds == 2 ? dglu_smem_bytes<BN, 2>() : dglu_smem_bytes<BN, 4>();
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     const int grid = (int)(total < Lc.num_sms ? total : Lc.num_sms);
-    kern<<<grid, cta_threads(kDgluEpiWarps), S::DYN_BYTES, stream>>>(prm);
+    kern<<<grid, cta_threads(kDgluEpiWarps), smem, stream>>>(prm);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }

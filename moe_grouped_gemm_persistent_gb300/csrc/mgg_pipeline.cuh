@@ -19,7 +19,7 @@
 //   epilogue(w, t, taddr, q, half, lane, have_acc, stg, rel)  one epilogue warp; EPI_WARPS/4 warps
 //        share TMEM sub-partition q and split the tile's 32-column chunks (chunk c belongs to
 //        half c % (EPI_WARPS/4)); `stg` is this warp's 1024-byte aligned staging buffer
-//        (kStageBytes) for bulk tensor stores; `rel` frees the TMEM accumulator and must be
+//        (P::STG_BYTES) for bulk tensor stores; `rel` frees the TMEM accumulator and must be
 //        called exactly once per tile when have_acc, after the warp's last tcgen05.ld of it.
 #pragma once
 
@@ -30,7 +30,6 @@ namespace mgg {
 constexpr int BM = 128;     // tile rows = UMMA M (cta_group::1)
 constexpr int BK = 64;      // K elements per ring slot: one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;  // K of one kind::f16 MMA
-constexpr int kStageBytes = 4096;  // per epilogue warp: one 32-row x 128-byte staging box
 constexpr int kSchedRing = 8;      // tile indices in flight from the producer to the other roles
 
 // Threads of a CTA with `epi_warps` epilogue warps (a multiple of 4) after the producer and MMA warps.
@@ -44,13 +43,14 @@ struct TileWork {
   int num_kb;   // number of BK slices; 0 = no MMA (the epilogue writes without TMEM)
 };
 
-template <int BN, int STAGES, int EPI_WARPS>
+// STG: bytes of output staging per epilogue warp (a multiple of 4 KB: 32 rows x 128 bytes per box).
+template <int BN, int STAGES, int EPI_WARPS, int STG>
 struct SmemLayout {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * kStageBytes;
+  static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * STG;
   static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * kSchedRing;
   static constexpr int SCHED_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int MISC_OFF = SCHED_OFF + kSchedRing * 8;
@@ -93,7 +93,7 @@ template <int BN, int STAGES, class P>
 __device__ __forceinline__ void persistent_gemm(const P& p) {
   constexpr int kEpiWarps = P::EPI_WARPS;
   static_assert(kEpiWarps % 4 == 0, "whole TMEM sub-partitions");
-  using S = SmemLayout<BN, STAGES, kEpiWarps>;
+  using S = SmemLayout<BN, STAGES, kEpiWarps, P::STG_BYTES>;
   constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N");
 
@@ -253,7 +253,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     // ---------------------------------------------------------------- epilogue warps
     const int q = warp & 3;             // TMEM sub-partition this warp may access
     const int half = (warp - 2) >> 2;   // which of the sub-partition's warps
-    uint8_t* stg = smem + S::EPI_OFF + (warp - 2) * kStageBytes;
+    uint8_t* stg = smem + S::EPI_OFF + (warp - 2) * P::STG_BYTES;
     uint32_t local = 0;
     long long n_tile = 0;
     auto next_tile = [&]() { const long long n = n_tile++; return dynamic ? consume_tile(n, true) : static_tile(n); };

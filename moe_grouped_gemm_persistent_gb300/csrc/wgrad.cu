@@ -46,6 +46,7 @@ __device__ __forceinline__ uint32_t swz128w(int r, int c16) { return (uint32_t)(
 template <int BN, int OS>
 struct WgradPolicy {
   static constexpr int EPI_WARPS = kWgradEpiWarps;
+  static constexpr int STG_BYTES = 4096;
   static constexpr int kEpiHalves = EPI_WARPS / 4;
   static constexpr int CW = 128 / OS;  // output columns per staged chunk (one 128-byte row)
   const WgradParams& p;
@@ -266,11 +267,13 @@ __global__ void wgrad_prep_kernel(const int32_t* offsets, int L, long long T, co
   tmap_release();
 }
 
-int wgrad_tile_n(int64_t inter) { return (inter % 256 == 0 || inter > 2048) ? 256 : 128; }
+// 128 x 256 tiles keep the tensor pipe fed (128 x 128 tiles are shared-memory-bandwidth bound);
+// narrow outputs fall back to 128 columns.
+int wgrad_tile_n(int64_t inter) { return inter > 128 ? 256 : 128; }
 
 template <int BN, int STAGES, int OS>
 static cudaError_t launch_wgrad_bn(const WgradLaunch& Lc, WgradParams& prm, cudaStream_t stream) {
-  using S = SmemLayout<BN, STAGES, kWgradEpiWarps>;
+  using S = SmemLayout<BN, STAGES, kWgradEpiWarps, 4096>;
   static_assert(S::DYN_BYTES <= 232448, "shared memory");
   auto kern = wgrad_kernel<BN, STAGES, OS>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);

@@ -50,7 +50,8 @@ def test_sizes_and_tile_counts(lib):
     assert lib.mgg_wgrad_workspace_size(64) >= 256 + 3 * 64 * 128 + 64 * 4
     assert lib.mgg_dglu_bwd_num_tiles(1024, 128) == 8
     assert lib.mgg_dglu_bwd_num_tiles(33536, 14336) == 262 * 56
-    assert lib.mgg_wgrad_num_tiles(64, 2048, 1408) == 64 * 16 * 11
+    assert lib.mgg_wgrad_num_tiles(64, 2048, 1408) == 64 * 16 * 6
+    assert lib.mgg_wgrad_num_tiles(4, 256, 128) == 4 * 2 * 1
     assert lib.mgg_wgrad_num_tiles(256, 7168, 2048) == 256 * 56 * 8
     for s in range(8):
         assert lib.mgg_status_string(s).decode().startswith("MGG_")
