@@ -16,14 +16,30 @@
 
 namespace mgg {
 
-constexpr int kDgluStages = 4;     // 16-bit D_row
-constexpr int kDgluStagesF32 = 3;  // fp32 D_row: one ring slot traded for 8 KB staging per warp
-constexpr int kDgluEpiWarps = 8;  // two warps per TMEM sub-partition: the dGLU epilogue is latency-bound
+// Per-variant configuration (CS / DS = element bytes of C / D_row).
+//  16-bit C: C reaches shared memory by TMA (a 3-deep ring of 32 x 64 boxes per epilogue warp,
+//            loaded ahead of the math), 4 epilogue warps, 3 operand-ring stages.
+//  fp32 C:   C is read per row into registers one chunk ahead; 8 epilogue warps (two per TMEM
+//            sub-partition) hide the load latency.
+//  The TMA path trades one operand-ring stage for the C ring, which pays when the epilogue
+//  dominates (small K); for K >= kTmaCMaxK the launcher takes the register path.
+constexpr int64_t kTmaCMaxK = 4095;
+
+template <int CS, int DS, bool TMAC>
+struct DgluCfg {
+  static constexpr bool kTmaC = TMAC && CS == 2;
+  static constexpr int kEpiWarps = kTmaC ? 4 : 8;
+  static constexpr int kCRing = 3;  // C boxes in flight per warp (TMA path)
+  // TMA path: C ring (16-bit D is written back in place) + fp32 D staging; register path: D staging
+  static constexpr int kStgBytes = kTmaC ? (kCRing * 4096 + (DS == 4 ? 8192 : 0)) : (DS == 4 ? 8192 : 4096);
+  static constexpr int kStages = (kTmaC || DS == 4) ? 3 : 4;
+};
 
 struct DgluParams {
   CUtensorMap tmap_a;           // A (M, K): dims {K, M}, box {64, 128}, 128B swizzle
   CUtensorMap tmap_b;           // dense B (N, K, L): dims {K, N, L}, box {64, BN, 1}
   CUtensorMap tmap_d;           // D_row (M, 2N): dims {2N, M}, box {128 B of columns, 32}, 128B swizzle
+  CUtensorMap tmap_c;           // 16-bit C (M, 2N): dims {2N, M}, box {64, 32}, 128B swizzle
   const CUtensorMap* b_maps;    // discrete B: one map per expert in the workspace, else null
   const int32_t* offsets;
   const float* alpha;
@@ -49,17 +65,20 @@ __device__ __forceinline__ float fast_sigmoid(float x) { return rcp_approx(1.0f 
 __device__ __forceinline__ uint32_t swz128(int r, int c16) { return (uint32_t)(r * 128 + ((c16 ^ (r & 7)) << 4)); }
 
 // CS / DS: element size in bytes of C and D_row (2 = bf16/fp16, 4 = fp32).
-template <int BN, int CS, int DS>
+template <int BN, int CS, int DS, bool TMAC>
 struct DgluPolicy {
-  static constexpr int EPI_WARPS = kDgluEpiWarps;
-  static constexpr int STG_BYTES = DS == 4 ? 8192 : 4096;  // fp32 D: the gate and the input box
+  using Cfg = DgluCfg<CS, DS, TMAC>;
+  static constexpr int EPI_WARPS = Cfg::kEpiWarps;
+  static constexpr int STG_BYTES = Cfg::kStgBytes;
   static constexpr int kEpiHalves = EPI_WARPS / 4;
+  static constexpr int kCRing = Cfg::kCRing;
   static constexpr int CV = 32 * CS / 16;  // 16-byte vectors per 32 elements of C
   const DgluParams& p;
   long long total_tiles;
   int* status;
   int a_mn, b_mn;
   int dynamic;
+  mutable uint32_t c_uses = 0;  // TMA path: C boxes this warp has consumed (ring position)
 
   __device__ DgluPolicy(const DgluParams& prm)
       : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(0), b_mn(prm.b_mn), dynamic(prm.dynamic) {}
@@ -182,21 +201,198 @@ struct DgluPolicy {
     }
   }
 
-  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, int q, int half, int lane, bool,
-                           uint8_t* stg_ptr, AccRelease rel) const {
+  // dGLU math on 32 columns of one row.  On entry gv / iv hold the C values of the gate and the
+  // input block, on exit dgate / dinput; returns this row's partial of sum_j R * act.
+  __device__ __forceinline__ float dglu_math(const uint32_t (&r)[32], float (&gv)[32], float (&iv)[32], float alpha2,
+                                             float beta_g, float pr) const {
+    const bool geglu = p.act == MGG_ACT_DGEGLU;
+    float dprob_acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const float R = __fmul_rn(alpha2, __uint_as_float(r[k]));
+      const float x_g = __fmul_rn(beta_g, gv[k]);  // one fp32 product, never contracted
+      const float x_i = __fmul_rn(beta_g, iv[k]);
+      const float Rp = R * pr;
+      float dg, di, act;
+      if (!geglu) {
+        const float s = fast_sigmoid(x_g);
+        di = Rp * (x_g * s);
+        dg = Rp * x_i * s * (1.0f + x_g * (1.0f - s));
+        act = x_g * s * x_i;
+      } else {
+        const float cgt = fminf(x_g, 7.0f);
+        const float cit = fminf(fmaxf(x_i, -7.0f), 7.0f);
+        const bool g_in = x_g <= 7.0f;
+        const bool i_in = (x_i >= -7.0f) && (x_i <= 7.0f);
+        const float gf = g_in ? (p.indicator ? 1.0f : x_g) : 0.0f;
+        const float inf_ = i_in ? (p.indicator ? 1.0f : x_i) : 0.0f;
+        const float s = fast_sigmoid(1.702f * cgt);
+        const float ci1 = cit + 1.0f;
+        dg = Rp * ci1 * s * (1.0f + 1.702f * cgt * (1.0f - s)) * gf;
+        di = Rp * cgt * s * inf_;
+        act = cgt * s * ci1;
+      }
+      dprob_acc += R * act;
+      gv[k] = dg;
+      iv[k] = di;
+    }
+    return dprob_acc;
+  }
+
+  __device__ __forceinline__ void dbias_partials(const TileWork& w, int j0, int lane, float (&gv)[32],
+                                                 float (&iv)[32]) const {
+    const int first = 2 * j0, second = 2 * j0 + 32;
+    const int gcol = p.gate_first ? first : second;
+    const int icol = p.gate_first ? second : first;
+    float* ws = p.dbias_ws + (size_t)w.expert * 2 * (size_t)p.N;
+    const float sg = warp_column_sums(gv, lane);
+    const float si = warp_column_sums(iv, lane);
+    atomicAdd(ws + gcol + lane, sg);
+    atomicAdd(ws + icol + lane, si);
+  }
+
+  __device__ __forceinline__ void log_tile(const TileWork& w, long long t) const {
+    if (p.tile_log != nullptr && t < p.tile_log_cap) {
+      int32_t* e = p.tile_log + 4 * t;
+      e[0] = w.expert;
+      e[1] = w.m0;
+      e[2] = w.n0;
+      e[3] = (int32_t)blockIdx.x;
+    }
+  }
+
+  __device__ __forceinline__ int num_chunks(const TileWork& w) const {
+    return (p.N - w.n0 < BN ? p.N - w.n0 : BN) / 32;
+  }
+
+  // ---------------------------------------------------------------- TMA path for 16-bit C
+  // Ring of kCRing 4 KB boxes per warp: box u % kCRing holds rows [row0, row0+32) x C columns
+  // [2*j0, 2*j0+64) (the gate and the input block of compact chunk j0).  Use u's box is loaded
+  // two uses ahead; with 16-bit D the results overwrite it in place and leave by a bulk store, so
+  // the box may be reloaded only once that store has read it.
+  __device__ __forceinline__ void c_issue(const EpiCtx& ctx, uint32_t use, int j0, int row0) const {
+    const uint32_t b = use % kCRing;
+    mbar_arrive_expect_tx(&ctx.bars[b], 4096);
+    tma_load_2d(smem_u32(ctx.stg) + b * 4096, &p.tmap_c, smem_u32(&ctx.bars[b]), 2 * j0, row0);
+  }
+
+  __device__ __forceinline__ void read_c_block(uint32_t box, int lane, int blk, float (&v)[32]) const {
+    const bool bf = p.c_dtype == MGG_BF16;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 x = ld_shared_v4(box + swz128(lane, 4 * blk + i));
+      const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (bf) {
+          v[8 * i + 2 * j + 0] = bf16_bits_to_float(wv[j] & 0xffffu);
+          v[8 * i + 2 * j + 1] = bf16_bits_to_float(wv[j] >> 16);
+        } else {
+          v[8 * i + 2 * j + 0] = __half2float(__ushort_as_half((unsigned short)(wv[j] & 0xffffu)));
+          v[8 * i + 2 * j + 1] = __half2float(__ushort_as_half((unsigned short)(wv[j] >> 16)));
+        }
+      }
+    }
+  }
+
+  __device__ void prologue(const TileWork& w, long long, const EpiCtx& ctx) const {
+    if constexpr (Cfg::kTmaC) {
+      const int nchunks = num_chunks(w);
+      const int row0 = w.m0 + 32 * ctx.q;
+      fence_async_shared();  // earlier generic reads of the ring before the async overwrite
+      __syncwarp();
+      if (ctx.lane == 0) {
+        if constexpr (DS == 2) bulk_wait_read<2>();  // the box of use c_uses was stored 3 uses ago
+        c_issue(ctx, c_uses, w.n0, row0);
+        if (nchunks > 1) {
+          if constexpr (DS == 2) bulk_wait_read<1>();
+          c_issue(ctx, c_uses + 1, w.n0 + 32, row0);
+        }
+      }
+      __syncwarp();
+    }
+  }
+
+  __device__ void epilogue_tmac(const TileWork& w, long long t, uint32_t taddr, const EpiCtx& ctx,
+                                AccRelease rel) const {
+    static_assert(kEpiHalves == 1, "one warp per TMEM sub-partition on the TMA path");
+    const int lane = ctx.lane;
     const int g = w.expert;
     const float alpha_g = __ldg(p.alpha + g);
     const float alpha2 = alpha_g * alpha_g;
     const float beta_g = __ldg(p.beta + g);
-    const int row0 = w.m0 + q * 32;
+    const int row0 = w.m0 + ctx.q * 32;
     const int row = row0 + lane;
     const float pr = __ldg(p.prob + row);
-    const size_t two_n = 2 * (size_t)p.N;
-    const size_t row_off = (size_t)row * two_n;
-    const bool geglu = p.act == MGG_ACT_DGEGLU;
-    const uint32_t stg = smem_u32(stg_ptr);
-    const int ncols = p.N - w.n0 < BN ? p.N - w.n0 : BN;
-    const int nchunks = ncols / 32;
+    const int nchunks = num_chunks(w);
+    const uint32_t ring = smem_u32(ctx.stg);
+    const uint32_t dstg = ring + kCRing * 4096;  // fp32 D staging
+    const int gblk = p.gate_first ? 0 : 1;
+    float dprob_acc = 0.f;
+    bool released = false;
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      const uint32_t u = c_uses + c;
+      const uint32_t box = ring + (u % kCRing) * 4096;
+      const int j0 = w.n0 + c * 32;
+      uint32_t r[32];
+      tmem_load_32cols(taddr + c * 32, r);
+      if (c == nchunks - 1) {
+        rel(lane);
+        released = true;
+      }
+      if (!warp_wait(&ctx.bars[u % kCRing], (u / kCRing) & 1u, ctx.wg, 7)) break;
+      float gv[32], iv[32];
+      read_c_block(box, lane, gblk, gv);
+      read_c_block(box, lane, 1 - gblk, iv);
+      dprob_acc += dglu_math(r, gv, iv, alpha2, beta_g, pr);
+      if constexpr (DS == 2) {  // D_row written back over this lane's own row of the C box
+        stage_block(box, lane, gblk, gv);
+        stage_block(box, lane, 1 - gblk, iv);
+        staging_flush(box, lane, 2 * j0, row0);
+      } else {
+        const int first = 2 * j0, second = 2 * j0 + 32;
+        staging_free(lane);
+        stage_block(dstg, lane, 0, gv);
+        stage_block(dstg + 4096, lane, 0, iv);
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&p.tmap_d, dstg, p.gate_first ? first : second, row0);
+          tma_store_2d(&p.tmap_d, dstg + 4096, p.gate_first ? second : first, row0);
+          bulk_commit_group();
+        }
+      }
+      if (p.dbias_ws != nullptr) dbias_partials(w, j0, lane, gv, iv);
+      if (c + 2 < nchunks) {  // refill the box of use u - 1 with chunk c + 2
+        if constexpr (DS == 4) fence_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (DS == 2) bulk_wait_read<1>();
+          c_issue(ctx, u + 2, j0 + 64, row0);
+        }
+      }
+    }
+    if (!released) rel(lane);
+    c_uses += (uint32_t)nchunks;
+    atomicAdd(p.dprob + row, dprob_acc);
+    if (ctx.q == 0 && lane == 0) log_tile(w, t);
+  }
+
+  // ---------------------------------------------------------------- register path for fp32 C
+  __device__ void epilogue_regc(const TileWork& w, long long t, uint32_t taddr, const EpiCtx& ctx,
+                                AccRelease rel) const {
+    const int lane = ctx.lane, half = ctx.half;
+    const int g = w.expert;
+    const float alpha_g = __ldg(p.alpha + g);
+    const float alpha2 = alpha_g * alpha_g;
+    const float beta_g = __ldg(p.beta + g);
+    const int row0 = w.m0 + ctx.q * 32;
+    const int row = row0 + lane;
+    const float pr = __ldg(p.prob + row);
+    const size_t row_off = (size_t)row * 2 * (size_t)p.N;
+    const uint32_t stg = smem_u32(ctx.stg);
+    const int nchunks = num_chunks(w);
     float dprob_acc = 0.f;
     bool released = false;
 
@@ -216,35 +412,7 @@ struct DgluPolicy {
       float gv[32], iv[32];
       unpack_c(cg, gv);
       unpack_c(ci, iv);
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float R = __fmul_rn(alpha2, __uint_as_float(r[k]));
-        const float x_g = __fmul_rn(beta_g, gv[k]);  // one fp32 product, never contracted
-        const float x_i = __fmul_rn(beta_g, iv[k]);
-        const float Rp = R * pr;
-        float dg, di, act;
-        if (!geglu) {
-          const float s = fast_sigmoid(x_g);
-          di = Rp * (x_g * s);
-          dg = Rp * x_i * s * (1.0f + x_g * (1.0f - s));
-          act = x_g * s * x_i;
-        } else {
-          const float cgt = fminf(x_g, 7.0f);
-          const float cit = fminf(fmaxf(x_i, -7.0f), 7.0f);
-          const bool g_in = x_g <= 7.0f;
-          const bool i_in = (x_i >= -7.0f) && (x_i <= 7.0f);
-          const float gf = g_in ? (p.indicator ? 1.0f : x_g) : 0.0f;
-          const float inf_ = i_in ? (p.indicator ? 1.0f : x_i) : 0.0f;
-          const float s = fast_sigmoid(1.702f * cgt);
-          const float ci1 = cit + 1.0f;
-          dg = Rp * ci1 * s * (1.0f + 1.702f * cgt * (1.0f - s)) * gf;
-          di = Rp * cgt * s * inf_;
-          act = cgt * s * ci1;
-        }
-        dprob_acc += R * act;
-        gv[k] = dg;
-        iv[k] = di;
-      }
+      dprob_acc += dglu_math(r, gv, iv, alpha2, beta_g, pr);
       if constexpr (DS == 2) {  // both 32-column blocks in one 64-column box
         staging_free(lane);
         stage_block(stg, lane, p.gate_first ? 0 : 1, gv);
@@ -263,16 +431,7 @@ struct DgluPolicy {
           bulk_commit_group();
         }
       }
-      if (p.dbias_ws != nullptr) {
-        const int first = 2 * j0, second = 2 * j0 + 32;
-        const int gcol = p.gate_first ? first : second;
-        const int icol = p.gate_first ? second : first;
-        float* ws = p.dbias_ws + (size_t)g * two_n;
-        const float sg = warp_column_sums(gv, lane);
-        const float si = warp_column_sums(iv, lane);
-        atomicAdd(ws + gcol + lane, sg);
-        atomicAdd(ws + icol + lane, si);
-      }
+      if (p.dbias_ws != nullptr) dbias_partials(w, j0, lane, gv, iv);
 #pragma unroll
       for (int i = 0; i < CV; ++i) {
         cg[i] = ng[i];
@@ -281,25 +440,32 @@ struct DgluPolicy {
     }
     if (!released) rel(lane);
     if (half < nchunks) atomicAdd(p.dprob + row, dprob_acc);
-    if (p.tile_log != nullptr && q == 0 && half == 0 && lane == 0 && t < p.tile_log_cap) {
-      int32_t* e = p.tile_log + 4 * t;
-      e[0] = g;
-      e[1] = w.m0;
-      e[2] = w.n0;
-      e[3] = (int32_t)blockIdx.x;
-    }
+    if (ctx.q == 0 && half == 0 && lane == 0) log_tile(w, t);
+  }
+
+  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, bool, const EpiCtx& ctx,
+                           AccRelease rel) const {
+    if constexpr (Cfg::kTmaC) epilogue_tmac(w, t, taddr, ctx, rel);
+    else epilogue_regc(w, t, taddr, ctx, rel);
   }
 };
 
-template <int BN, int CS, int DS>
-__global__ void __launch_bounds__(cta_threads(kDgluEpiWarps), 1) dglu_bwd_kernel(const __grid_constant__ DgluParams prm) {
-  const DgluPolicy<BN, CS, DS> pol(prm);
-  persistent_gemm<BN, DS == 4 ? kDgluStagesF32 : kDgluStages>(pol);
+template <int BN, int CS, int DS, bool TMAC>
+__global__ void __launch_bounds__(cta_threads(DgluCfg<CS, DS, TMAC>::kEpiWarps), 1)
+    dglu_bwd_kernel(const __grid_constant__ DgluParams prm) {
+  const DgluPolicy<BN, CS, DS, TMAC> pol(prm);
+  persistent_gemm<BN, DgluCfg<CS, DS, TMAC>::kStages>(pol);
 }
 
-template <int BN, int DS>
-constexpr int dglu_smem_bytes() {
-  return SmemLayout<BN, DS == 4 ? kDgluStagesF32 : kDgluStages, kDgluEpiWarps, DS == 4 ? 8192 : 4096>::DYN_BYTES;
+template <int BN, int CS, int DS, bool TMAC>
+static cudaError_t launch_dglu_variant(const DgluParams& prm, int grid, cudaStream_t stream) {
+  using C = DgluCfg<CS, DS, TMAC>;
+  constexpr int smem = SmemLayout<BN, C::kStages, C::kEpiWarps, C::kStgBytes>::DYN_BYTES;
+  auto kern = dglu_bwd_kernel<BN, CS, DS, TMAC>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, cta_threads(C::kEpiWarps), smem, stream>>>(prm);
+  return cudaGetLastError();
 }
 
 // Checks the device-resident arguments and builds the per-expert weight maps.
@@ -370,6 +536,7 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     prm.tmap_a = Lc.tmap_a;
     prm.tmap_b = Lc.tmap_b;
     prm.tmap_d = Lc.tmap_d;
+    prm.tmap_c = Lc.tmap_c;
     prm.b_maps = a.b_ptrs != nullptr ? maps : nullptr;
     prm.offsets = a.padded_offsets;
     prm.alpha = a.alpha;
@@ -398,14 +565,17 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     prm.gate_first = a.gate_first != 0;
 
     const int cs = a.c_dtype == MGG_FP32 ? 4 : 2, ds = a.d_dtype == MGG_FP32 ? 4 : 2;
-    void (*kern)(DgluParams) = cs == 2 ? (ds == 2 ? dglu_bwd_kernel<BN, 2, 2> : dglu_bwd_kernel<BN, 2, 4>)
-                                       : (ds == 2 ? dglu_bwd_kernel<BN, 4, 2> : dglu_bwd_kernel<BN, 4, 4>);
-    const int smem = ds == 2 ? dglu_smem_bytes<BN, 2>() : dglu_smem_bytes<BN, 4>();
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
+    const bool tmac = cs == 2 && a.K <= kTmaCMaxK;
     const int grid = (int)(total < Lc.num_sms ? total : Lc.num_sms);
-    kern<<<grid, cta_threads(kDgluEpiWarps), smem, stream>>>(prm);
-    err = cudaGetLastError();
+    if (cs == 2) {
+      if (tmac) err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true>(prm, grid, stream)
+                              : launch_dglu_variant<BN, 2, 4, true>(prm, grid, stream);
+      else err = ds == 2 ? launch_dglu_variant<BN, 2, 2, false>(prm, grid, stream)
+                         : launch_dglu_variant<BN, 2, 4, false>(prm, grid, stream);
+    } else {
+      err = ds == 2 ? launch_dglu_variant<BN, 4, 2, false>(prm, grid, stream)
+                    : launch_dglu_variant<BN, 4, 4, false>(prm, grid, stream);
+    }
     if (err != cudaSuccess) return err;
   }
   if (a.dbias != nullptr) {

@@ -285,6 +285,11 @@ mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream) {
     const uint32_t box[2] = {(uint32_t)(128 / esz), 32};
     if ((s = encode_map(&Lc.tmap_d, a.d_dtype, a.d_row, 2, dims, strides, box, "D_row")) != MGG_OK) return s;
   }
+  if (a.c_dtype != MGG_FP32) {  // C (M, 2N): 32-row boxes of 64 columns (one gate + one input block)
+    const uint64_t dims[2] = {2 * N, M}, strides[1] = {2 * N * 2};
+    const uint32_t box[2] = {64, 32};
+    if ((s = encode_map(&Lc.tmap_c, a.c_dtype, a.c, 2, dims, strides, box, "C")) != MGG_OK) return s;
+  }
   return from_cuda(launch_dglu_bwd(Lc, static_cast<cudaStream_t>(stream)), "mgg_dglu_bwd launch");
 }
 

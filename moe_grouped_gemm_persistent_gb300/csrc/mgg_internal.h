@@ -21,6 +21,7 @@ struct DgluLaunch {
   CUtensorMap tmap_a;
   CUtensorMap tmap_b;  // dense 3-D map, or the per-expert template (discrete)
   CUtensorMap tmap_d;  // D_row store map
+  CUtensorMap tmap_c;  // C load map (16-bit C only)
   const mgg_dglu_bwd_args* args;
   int num_sms;
   int tile_n;

@@ -16,10 +16,13 @@
 //   TileWork tile(long long t)                      same answer for every role
 //   issue_loads(w, kb, sa, sb, bar)                 producer thread
 //   EPI_WARPS                                       epilogue warps (multiple of 4)
-//   epilogue(w, t, taddr, q, half, lane, have_acc, stg, rel)  one epilogue warp; EPI_WARPS/4 warps
-//        share TMEM sub-partition q and split the tile's 32-column chunks (chunk c belongs to
-//        half c % (EPI_WARPS/4)); `stg` is this warp's 1024-byte aligned staging buffer
-//        (P::STG_BYTES) for bulk tensor stores; `rel` frees the TMEM accumulator and must be
+//   STG_BYTES                                       shared memory per epilogue warp
+//   prologue(w, t, ctx)                             one epilogue warp, before it waits for the
+//                                                   tile's accumulator (e.g. to start input loads)
+//   epilogue(w, t, taddr, have_acc, ctx, rel)       one epilogue warp; EPI_WARPS/4 warps share TMEM
+//        sub-partition ctx.q and split the tile's 32-column chunks (chunk c belongs to ctx.half =
+//        c % (EPI_WARPS/4)); ctx.stg is the warp's 1024-byte aligned STG_BYTES of shared memory,
+//        ctx.bars four mbarriers (count 1) it owns; `rel` frees the TMEM accumulator and must be
 //        called exactly once per tile when have_acc, after the warp's last tcgen05.ld of it.
 #pragma once
 
@@ -51,13 +54,23 @@ struct SmemLayout {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * STG;
-  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * kSchedRing;
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * kSchedRing + 4 * EPI_WARPS;
   static constexpr int SCHED_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int MISC_OFF = SCHED_OFF + kSchedRing * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int DYN_BYTES = BYTES + 1024;  // slack to align the ring to 1024 B
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "ring slots must stay 1024-byte aligned");
   static_assert(DYN_BYTES <= 232448, "shared memory per block");
+};
+
+// What one epilogue warp owns.
+struct EpiCtx {
+  int q;          // TMEM sub-partition (rows 32q .. 32q+31 of the tile)
+  int half;       // index among the warps sharing that sub-partition
+  int lane;
+  uint8_t* stg;   // STG_BYTES of shared memory, 1024-byte aligned
+  uint64_t* bars; // four mbarriers initialised with count 1
+  WaitGuard wg;
 };
 
 // Frees one TMEM accumulator for the MMA warp (called by every lane of an epilogue warp).
@@ -106,6 +119,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   uint64_t* done_bar = tempty_bar + 2;
   uint64_t* sfull_bar = done_bar + 1;           // [kSchedRing] a tile index was published
   uint64_t* sempty_bar = sfull_bar + kSchedRing;  // [kSchedRing] every role has read it
+  uint64_t* epi_bars = sempty_bar + kSchedRing;   // [4 * kEpiWarps] owned by the epilogue warps
   volatile long long* sched_ring = reinterpret_cast<volatile long long*>(smem + S::SCHED_OFF);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
@@ -130,6 +144,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       mbar_init(&sfull_bar[r], 1);
       mbar_init(&sempty_bar[r], 1 + kEpiWarps);  // the MMA thread and every epilogue warp
     }
+    for (int b = 0; b < 4 * kEpiWarps; ++b) mbar_init(&epi_bars[b], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -253,22 +268,22 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     // ---------------------------------------------------------------- epilogue warps
     const int q = warp & 3;             // TMEM sub-partition this warp may access
     const int half = (warp - 2) >> 2;   // which of the sub-partition's warps
-    uint8_t* stg = smem + S::EPI_OFF + (warp - 2) * P::STG_BYTES;
+    const EpiCtx ctx{q, half, lane, smem + S::EPI_OFF + (warp - 2) * P::STG_BYTES, epi_bars + 4 * (warp - 2), wg};
     uint32_t local = 0;
     long long n_tile = 0;
     auto next_tile = [&]() { const long long n = n_tile++; return dynamic ? consume_tile(n, true) : static_tile(n); };
     for (long long t = next_tile(); t < p.total_tiles; t = next_tile()) {
       const TileWork w = p.tile(t);
       if (!w.active) continue;
+      p.prologue(w, t, ctx);
       if (w.num_kb == 0) {
-        p.epilogue(w, t, 0u, q, half, lane, false, stg, AccRelease{nullptr});
+        p.epilogue(w, t, 0u, false, ctx, AccRelease{nullptr});
         continue;
       }
       const uint32_t acc = local & 1u, use = local >> 1;
       if (!warp_wait(&tfull_bar[acc], use & 1u, wg, 4)) break;
       tc_fence_after();
-      p.epilogue(w, t, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, q, half, lane, true, stg,
-                 AccRelease{&tempty_bar[acc]});
+      p.epilogue(w, t, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, true, ctx, AccRelease{&tempty_bar[acc]});
       ++local;
     }
     if (lane == 0) bulk_wait_all();  // bulk stores complete before the CTA exits

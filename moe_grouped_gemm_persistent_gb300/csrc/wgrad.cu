@@ -99,8 +99,12 @@ struct WgradPolicy {
     }
   }
 
-  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, int q, int half, int lane,
-                           bool have_acc, uint8_t* stg_ptr, AccRelease rel) const {
+  __device__ void prologue(const TileWork&, long long, const EpiCtx&) const {}
+
+  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, bool have_acc, const EpiCtx& ctx,
+                           AccRelease rel) const {
+    const int q = ctx.q, half = ctx.half, lane = ctx.lane;
+    uint8_t* stg_ptr = ctx.stg;
     const int e = w.expert;
     const int row0 = w.m0 + q * 32;
     const int row = row0 + lane;

@@ -68,6 +68,10 @@ DGLU_CASES = {
     "discrete_k": dict(b_mode="discrete", b_major="k"),
     "discrete_n_geglu": dict(b_mode="discrete", b_major="n", act="dgeglu", c_std=4.0, dbias=True),
     "wide_n": dict(N=544, K=192, counts=(512, 256)),
+    # K >= 4096 selects the register path for 16-bit C
+    "regpath_swiglu": dict(K=4096, N=96, counts=(256, 0, 256)),
+    "regpath_geglu_fp32d_dbias": dict(K=4160, N=64, counts=(256, 512), act="dgeglu", c_std=4.0, d_dtype="fp32",
+                                      dbias=True),
 }
 
 
