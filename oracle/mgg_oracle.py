@@ -35,6 +35,9 @@ GEGLU_ALPHA = 1.702
 GLU_CLAMP_MAX = 7.0
 GLU_CLAMP_MIN = -7.0
 LINEAR_OFFSET = 1.0
+# Grouped GEMM + dGLU (SM100), "Common Parameters": situ_beta1 / situ_beta2 defaults of dSiTU-GLU.
+SITU_BETA1 = 4.0
+SITU_BETA2 = 25.0
 # Grouped GEMM + dGLU: X splits into alternating 32-wide gate/input blocks.
 GLU_BLOCK = 32
 # Grouped GEMM + dGLU, "Shapes and Divisibility": m_aligned = 256, at most 1024 experts.
@@ -140,6 +143,29 @@ def dgeglu(R, prob, gate, inp, geglu_filter: str = "value"):
     return dgate, dinput, act
 
 
+def dsituglu(R, prob, gate, inp, beta1: float = SITU_BETA1, beta2: float = SITU_BETA2):
+    """dSiTU-GLU backward (dGLU page, block-scaled contract, "Equations").
+
+    T_g = beta1 tanh(G / beta1) sigmoid(G);  T_u = beta2 tanh(U / beta2);
+    dT_g/dG = (1 - tanh^2(G / beta1)) sigmoid(G) + beta1 tanh(G / beta1) sigmoid(G) (1 - sigmoid(G));
+    dT_u/dU = 1 - tanh^2(U / beta2);
+    dgate = R prob T_u dT_g/dG, dinput = R prob T_g dT_u/dU; the dprob activation is T_g T_u.
+    G is the gate and U the input block of X.  Returns (dgate, dinput, act).
+    """
+    R = np.asarray(R, np.float64)
+    prob = np.asarray(prob, np.float64)
+    G = np.asarray(gate, np.float64)
+    U = np.asarray(inp, np.float64)
+    tg = np.tanh(G / beta1)
+    sg = sigmoid(G)
+    tu = np.tanh(U / beta2)
+    T_g = beta1 * tg * sg
+    T_u = beta2 * tu
+    dT_g = (1.0 - tg * tg) * sg + beta1 * tg * sg * (1.0 - sg)
+    dT_u = 1.0 - tu * tu
+    return R * prob * T_u * dT_g, R * prob * T_g * dT_u, T_g * T_u
+
+
 def scale_x(beta_g, c_values) -> np.ndarray:
     """X = beta_g * C as one float32 product per element (then widened to float64)."""
     x32 = np.float32(beta_g) * np.asarray(c_values, dtype=np.float32)
@@ -162,7 +188,9 @@ def dglu_bwd(a: np.ndarray,
              geglu_filter: str = "value",
              rows: Optional[np.ndarray] = None,
              dprob_in: Optional[np.ndarray] = None,
-             dbias_in: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+             dbias_in: Optional[np.ndarray] = None,
+             situ_beta1: float = SITU_BETA1,
+             situ_beta2: float = SITU_BETA2) -> Dict[str, np.ndarray]:
     """Grouped GEMM + dGLU backward (dGLU page, BF16 contract).
 
     a: (M, K) values of A; get_b(g) -> (N, K) values of B_g (dense (N,K,L) slice or
@@ -218,6 +246,8 @@ def dglu_bwd(a: np.ndarray,
             dgate, dinput, a_unscaled = dswiglu(R, p, gate, inp)
         elif act == "dgeglu":
             dgate, dinput, a_unscaled = dgeglu(R, p, gate, inp, geglu_filter)
+        elif act == "dsituglu":
+            dgate, dinput, a_unscaled = dsituglu(R, p, gate, inp, situ_beta1, situ_beta2)
         else:
             raise ValueError(act)
         out = np.zeros((sel.size, two_n), dtype=np.float64)
@@ -383,7 +413,8 @@ def offsets_valid(offsets: Sequence[int], total: int, align: int = M_ALIGNED) ->
 
 __all__ = [
     "GEGLU_ALPHA", "GLU_CLAMP_MAX", "GLU_CLAMP_MIN", "LINEAR_OFFSET", "GLU_BLOCK", "M_ALIGNED", "MAX_EXPERTS",
-    "expert_ranges", "sigmoid", "glu_columns", "dswiglu", "dgeglu", "scale_x", "dglu_bwd",
+    "SITU_BETA1", "SITU_BETA2",
+    "expert_ranges", "sigmoid", "glu_columns", "dswiglu", "dgeglu", "dsituglu", "scale_x", "dglu_bwd",
     "wgrad_a_block", "wgrad_b_block", "wgrad", "wgrad_elements", "dgrad_tiles", "wgrad_tiles",
     "offsets_valid",
 ]

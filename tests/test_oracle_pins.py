@@ -39,6 +39,11 @@ def fwd_geglu_clamped(gate, inp):
     return (x + 1.0) * g * _sig(1.702 * g)
 
 
+def fwd_situglu(gate, inp, b1=4.0, b2=25.0):
+    """Forward SiTU-GLU unit: (b1 tanh(g/b1) sigmoid(g)) * (b2 tanh(u/b2))."""
+    return (b1 * math.tanh(gate / b1) * _sig(gate)) * (b2 * math.tanh(inp / b2))
+
+
 def fd(f, x, h=1e-6):
     return (f(x + h) - f(x - h)) / (2.0 * h)
 
@@ -52,7 +57,7 @@ def brute_dglu(a, bs, c, offsets, alpha, beta, prob, act, gate_first, filt):
     D = np.zeros((M, two_n))
     dprob = np.zeros(M)
     dbias = np.zeros((L, two_n))
-    fwd = fwd_swiglu if act == "dswiglu" else fwd_geglu_clamped
+    fwd = {"dswiglu": fwd_swiglu, "dgeglu": fwd_geglu_clamped, "dsituglu": fwd_situglu}[act]
     for m in range(M):
         g = next(e for e in range(L) if m < offsets[e])
         for j in range(N):
@@ -116,6 +121,7 @@ def test_constants_match_pages_fixture():
     assert O.GLU_BLOCK == vals["glu_block"]
     assert O.M_ALIGNED == vals["m_aligned"] == vals["token_multiple"]
     assert O.MAX_EXPERTS == vals["max_experts"]
+    assert O.SITU_BETA1 == vals["situ_beta1"] and O.SITU_BETA2 == vals["situ_beta2"]
 
 
 def test_expert_ranges_cumulative_ends():
@@ -173,6 +179,32 @@ def test_dgeglu_indicator_matches_fd(gate, inp):
     assert act == pytest.approx(fwd_geglu_clamped(gate, inp), rel=1e-12)
 
 
+@pytest.mark.parametrize("gate,inp", [(0.3, -1.2), (-2.5, 0.7), (6.0, 30.0), (-15.0, -40.0), (12.0, 3.0)])
+@pytest.mark.parametrize("b1,b2", [(4.0, 25.0), (2.0, 5.0)])
+def test_dsituglu_matches_fd(gate, inp, b1, b2):
+    R, p = 1.1, 0.45
+    dg, di, act = O.dsituglu(R, p, gate, inp, b1, b2)
+    # central differences of an O(10) forward carry ~1e-9 absolute rounding noise
+    assert dg == pytest.approx(R * p * fd(lambda x: fwd_situglu(x, inp, b1, b2), gate), rel=1e-7, abs=1e-8)
+    assert di == pytest.approx(R * p * fd(lambda x: fwd_situglu(gate, x, b1, b2), inp), rel=1e-7, abs=1e-8)
+    assert act == pytest.approx(fwd_situglu(gate, inp, b1, b2), rel=1e-12)
+
+
+def test_dsituglu_closed_forms():
+    # G = 0: tanh(0) = 0 and sigmoid(0) = 1/2, so T_g = 0 and dT_g/dG = 1/2
+    dg, di, act = O.dsituglu(2.0, 0.5, 0.0, 10.0)
+    assert di == 0.0 and act == 0.0
+    assert dg == pytest.approx(2.0 * 0.5 * 25.0 * math.tanh(10.0 / 25.0) * 0.5)
+    # U = 0: T_u = 0 and dT_u/dU = 1
+    dg, di, act = O.dsituglu(2.0, 0.5, 1.5, 0.0)
+    assert dg == 0.0 and act == 0.0
+    assert di == pytest.approx(2.0 * 0.5 * 4.0 * math.tanh(1.5 / 4.0) / (1 + math.exp(-1.5)))
+    # saturation: |U| >> beta2 gives dT_u/dU -> 0, T_u -> +-beta2
+    dg, di, act = O.dsituglu(1.0, 1.0, 1.0, 1e4)
+    assert abs(di) < 1e-12 and dg == pytest.approx(25.0 * ((1 - math.tanh(0.25) ** 2) / (1 + math.exp(-1.0))
+                                                           + 4 * math.tanh(0.25) * _sig(1.0) * (1 - _sig(1.0))))
+
+
 @pytest.mark.parametrize("gate,inp", [(0.3, -1.2), (6.5, 6.9), (8.0, 2.0), (3.0, -8.5), (7.0, -7.0)])
 def test_dgeglu_value_filter_is_indicator_times_raw(gate, inp):
     R, p = 1.3, 0.9
@@ -226,7 +258,7 @@ def test_scale_x_is_single_float32_product():
 # --------------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("act,filt,gate_first", [
-    ("dswiglu", "value", True), ("dswiglu", "value", False),
+    ("dswiglu", "value", True), ("dswiglu", "value", False), ("dsituglu", "value", True), ("dsituglu", "value", False),
     ("dgeglu", "indicator", True), ("dgeglu", "value", True), ("dgeglu", "value", False)])
 def test_dglu_bwd_bruteforce(act, filt, gate_first):
     a, bs, c, offsets, alpha, beta, prob = tiny_case(
