@@ -37,6 +37,7 @@ WORKLOAD_TEXT = {
              "C~N(0,4), FP32 D_row, dbias",
     "wgrad64": "grouped wgrad: L=64, hidden=2048, inter=1408, T=65536 Zipf(1.2), FP32 dense accumulate",
     "tiny": "tiny: L=4, counts [256,0,512,256], K=hidden=256, N=128",
+    "mixtral_situ": "Mixtral-like shape with the dSiTU-GLU backward (beta1=4, beta2=25), C~N(0,4), BF16 D_row",
     "mixtral_s": "profiling copy of mixtral with L=2 experts, 8192 tokens",
     "geglu_s": "profiling copy of geglu with 12288 tokens",
     "deepseek_s": "profiling copy of deepseek with L=32 experts, 16384 tokens",

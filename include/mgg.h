@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MGG_ABI_VERSION 1
+#define MGG_ABI_VERSION 2
 
 typedef enum mgg_status {
   MGG_OK = 0,
@@ -59,8 +59,10 @@ typedef enum mgg_status {
 
 typedef enum mgg_dtype { MGG_BF16 = 0, MGG_FP16 = 1, MGG_FP32 = 2 } mgg_dtype;
 
-/* dGLU page, "Common Parameters": act_func "dswiglu" (default) or "dgeglu". */
-typedef enum mgg_act { MGG_ACT_DSWIGLU = 0, MGG_ACT_DGEGLU = 1 } mgg_act;
+/* dGLU page, "Common Parameters": act_func "dswiglu" (default), "dgeglu", or "dsituglu" (whose
+ * equations the page gives under "Block-scaled contract", "Equations": T_g = beta1 tanh(G/beta1)
+ * sigmoid(G), T_u = beta2 tanh(U/beta2); here it runs in the BF16 path). */
+typedef enum mgg_act { MGG_ACT_DSWIGLU = 0, MGG_ACT_DGEGLU = 1, MGG_ACT_DSITUGLU = 2 } mgg_act;
 
 /* dGeGLU filters.  VALUE: as printed on the dGLU page (gate_filter = raw_gate when
  * raw_gate <= 7 else 0; input_filter = raw_input when -7 <= raw_input <= 7 else 0).
@@ -129,6 +131,8 @@ typedef struct mgg_dglu_bwd_args {
   int32_t gate_first;     /* 1: the gate block precedes the input block in every 64 columns */
   int32_t sched;          /* mgg_sched */
   int32_t reserved;       /* must be 0 */
+  float situ_beta1;       /* dSiTU-GLU gate tanh scale, positive finite; 0 = the default 4.0 */
+  float situ_beta2;       /* dSiTU-GLU input tanh scale, positive finite; 0 = the default 25.0 */
 } mgg_dglu_bwd_args;
 
 /*

@@ -18,7 +18,7 @@ MGG_ERR_DEVICE_POINTER = 6
 MGG_ERR_DEVICE_TIMEOUT = 7
 
 DTYPES = {"bf16": 0, "fp16": 1, "fp32": 2}
-ACTS = {"dswiglu": 0, "dgeglu": 1}
+ACTS = {"dswiglu": 0, "dgeglu": 1, "dsituglu": 2}
 FILTERS = {"value": 0, "indicator": 1}
 MAJORS = {"k": 0, "mn": 1, "m": 1, "n": 1}
 SCHEDS = {"static": 0, "dynamic": 1}
@@ -35,6 +35,7 @@ class DgluBwdArgs(ctypes.Structure):
         ("workspace_bytes", c_int64), ("tile_log_capacity", c_int64),
         ("b_major", c_int32), ("c_dtype", c_int32), ("d_dtype", c_int32), ("act", c_int32),
         ("geglu_filter", c_int32), ("gate_first", c_int32), ("sched", c_int32), ("reserved", c_int32),
+        ("situ_beta1", ctypes.c_float), ("situ_beta2", ctypes.c_float),
     ]
 
 

@@ -68,7 +68,7 @@ def new_workspace(nbytes: int, device) -> torch.Tensor:
 
 def make_dglu_args(*, a, c, padded_offsets, alpha, beta, prob, dprob, d_row, b=None, b_ptrs=None, N=None,
                    dbias=None, act="dswiglu", geglu_filter="value", gate_first=True, b_major="k",
-                   sched="static", workspace=None, tile_log=None) -> DgluBwdArgs:
+                   sched="static", workspace=None, tile_log=None, situ_beta1=4.0, situ_beta2=25.0) -> DgluBwdArgs:
     M, K = a.shape
     L = padded_offsets.numel()
     if N is None:
@@ -94,6 +94,8 @@ def make_dglu_args(*, a, c, padded_offsets, alpha, beta, prob, dprob, d_row, b=N
     args.gate_first = 1 if gate_first else 0
     args.sched = SCHEDS[sched]
     args.reserved = 0
+    args.situ_beta1 = situ_beta1
+    args.situ_beta2 = situ_beta2
     return args
 
 
@@ -102,7 +104,8 @@ def dglu_bwd(*, a: torch.Tensor, c: torch.Tensor, padded_offsets: torch.Tensor, 
              b: Optional[torch.Tensor] = None, b_ptrs: Optional[torch.Tensor] = None, N: Optional[int] = None,
              dbias: Optional[torch.Tensor] = None, act: str = "dswiglu", geglu_filter: str = "value",
              gate_first: bool = True, b_major: str = "k", sched: str = "dynamic",
-             workspace: Optional[torch.Tensor] = None, tile_log: Optional[torch.Tensor] = None, stream=None):
+             workspace: Optional[torch.Tensor] = None, tile_log: Optional[torch.Tensor] = None, stream=None,
+             situ_beta1: float = 4.0, situ_beta2: float = 25.0):
     """Grouped GEMM + dGLU backward (see include/mgg.h, mgg_dglu_bwd).
 
     d_row is written; dprob and dbias (when given) are accumulated into.  Returns the
@@ -115,7 +118,7 @@ def dglu_bwd(*, a: torch.Tensor, c: torch.Tensor, padded_offsets: torch.Tensor, 
     args = make_dglu_args(a=a, c=c, padded_offsets=padded_offsets, alpha=alpha, beta=beta, prob=prob, dprob=dprob,
                           d_row=d_row, b=b, b_ptrs=b_ptrs, N=n, dbias=dbias, act=act, geglu_filter=geglu_filter,
                           gate_first=gate_first, b_major=b_major, sched=sched, workspace=workspace,
-                          tile_log=tile_log)
+                          tile_log=tile_log, situ_beta1=situ_beta1, situ_beta2=situ_beta2)
     check(load().mgg_dglu_bwd(args, _stream(stream)))
     return workspace
 

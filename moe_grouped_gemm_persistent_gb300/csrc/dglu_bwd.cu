@@ -57,6 +57,7 @@ struct DgluParams {
   int num_n, num_kb;
   int a_mn, b_mn;
   int c_dtype, d_dtype, act, indicator, gate_first;
+  float situ_b1, situ_b2, situ_inv_b1, situ_inv_b2;  // dSiTU-GLU scales and their reciprocals
 };
 
 __device__ __forceinline__ float fast_sigmoid(float x) { return rcp_approx(1.0f + __expf(-x)); }
@@ -205,7 +206,7 @@ struct DgluPolicy {
   // input block, on exit dgate / dinput; returns this row's partial of sum_j R * act.
   __device__ __forceinline__ float dglu_math(const uint32_t (&r)[32], float (&gv)[32], float (&iv)[32], float alpha2,
                                              float beta_g, float pr) const {
-    const bool geglu = p.act == MGG_ACT_DGEGLU;
+    const int act_kind = p.act;
     float dprob_acc = 0.f;
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
@@ -214,11 +215,22 @@ struct DgluPolicy {
       const float x_i = __fmul_rn(beta_g, iv[k]);
       const float Rp = R * pr;
       float dg, di, act;
-      if (!geglu) {
+      if (act_kind == MGG_ACT_DSWIGLU) {
         const float s = fast_sigmoid(x_g);
         di = Rp * (x_g * s);
         dg = Rp * x_i * s * (1.0f + x_g * (1.0f - s));
         act = x_g * s * x_i;
+      } else if (act_kind == MGG_ACT_DSITUGLU) {
+        const float s = fast_sigmoid(x_g);
+        const float tg = tanhf(x_g * p.situ_inv_b1);
+        const float tu = tanhf(x_i * p.situ_inv_b2);
+        const float Tg = p.situ_b1 * tg * s;
+        const float Tu = p.situ_b2 * tu;
+        const float dTg = (1.0f - tg * tg) * s + p.situ_b1 * tg * s * (1.0f - s);
+        const float dTu = 1.0f - tu * tu;
+        dg = Rp * Tu * dTg;
+        di = Rp * Tg * dTu;
+        act = Tg * Tu;
       } else {
         const float cgt = fminf(x_g, 7.0f);
         const float cit = fminf(fmaxf(x_i, -7.0f), 7.0f);
@@ -563,6 +575,10 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     prm.act = a.act;
     prm.indicator = a.geglu_filter == MGG_FILTER_INDICATOR;
     prm.gate_first = a.gate_first != 0;
+    prm.situ_b1 = a.situ_beta1 != 0.0f ? a.situ_beta1 : 4.0f;
+    prm.situ_b2 = a.situ_beta2 != 0.0f ? a.situ_beta2 : 25.0f;
+    prm.situ_inv_b1 = 1.0f / prm.situ_b1;
+    prm.situ_inv_b2 = 1.0f / prm.situ_b2;
 
     const int cs = a.c_dtype == MGG_FP32 ? 4 : 2, ds = a.d_dtype == MGG_FP32 ? 4 : 2;
     const bool tmac = cs == 2 && a.K <= kTmaCMaxK;

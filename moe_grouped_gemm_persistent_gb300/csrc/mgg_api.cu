@@ -110,7 +110,14 @@ mgg_status validate_dglu(const mgg_dglu_bwd_args& a) {
   if (a.b_major != MGG_MAJOR_K && a.b_major != MGG_MAJOR_MN) return fail(MGG_ERR_VALUE, "b_major must be K or MN");
   if (a.b != nullptr && a.b_major != MGG_MAJOR_K) return fail(MGG_ERR_VALUE, "dense weights (N, K, L) are K-major");
   if (!valid_dtype(a.c_dtype) || !valid_dtype(a.d_dtype)) return fail(MGG_ERR_VALUE, "c_dtype/d_dtype out of range");
-  if (a.act != MGG_ACT_DSWIGLU && a.act != MGG_ACT_DGEGLU) return fail(MGG_ERR_VALUE, "act must be DSWIGLU or DGEGLU");
+  if (a.act != MGG_ACT_DSWIGLU && a.act != MGG_ACT_DGEGLU && a.act != MGG_ACT_DSITUGLU)
+    return fail(MGG_ERR_VALUE, "act must be DSWIGLU, DGEGLU or DSITUGLU");
+  if (a.act == MGG_ACT_DSITUGLU) {
+    const float b[2] = {a.situ_beta1, a.situ_beta2};
+    for (float v : b)
+      if (v != 0.0f && !(v > 0.0f && v < 3.0e38f))
+        return fail(MGG_ERR_VALUE, "situ_beta1 / situ_beta2 must be positive finite (0 = default)");
+  }
   if (a.geglu_filter != MGG_FILTER_VALUE && a.geglu_filter != MGG_FILTER_INDICATOR)
     return fail(MGG_ERR_VALUE, "geglu_filter must be VALUE or INDICATOR");
   if (a.gate_first != 0 && a.gate_first != 1) return fail(MGG_ERR_VALUE, "gate_first must be 0 or 1");

@@ -158,6 +158,11 @@ def workload_specs(name: str):
         w = WgradSpec("deepseek", L=256, hidden=7168, inter=2048, counts=counts.copy(),
                       a_major="k", b_major="n", input_order="tensor_ragged", out_mode="discrete")
         return d, w
+    # the Mixtral-like layer with the dSiTU-GLU backward (beta1 = 4, beta2 = 25)
+    if name == "mixtral_situ":
+        counts = dgrad_counts(0, 8, 32768, None)
+        return DgluSpec("mixtral_situ", L=8, K=4096, N=14336, counts=counts, b_std=0.02, act="dsituglu",
+                        c_std=4.0), None
     # reduced copies of the layers above, sized for profiler captures (a few GB on the device)
     if name == "mixtral_s":
         counts = dgrad_counts(0, 2, 8192, None)

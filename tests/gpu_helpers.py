@@ -48,7 +48,7 @@ def dglu_b_getter(spec, b):
 
 
 def run_dglu_gpu(spec, x, dev, gate_first=True, geglu_filter="value", dprob0=None, dbias0=None, tile_log=False,
-                 dbias=None, sched="static"):
+                 dbias=None, sched="static", situ=(4.0, 25.0)):
     """Runs mgg_dglu_bwd on inputs x (CPU tensors from synth) and returns the outputs on CPU."""
     M, N, L = spec.M, spec.N, spec.L
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
@@ -69,7 +69,8 @@ def run_dglu_gpu(spec, x, dev, gate_first=True, geglu_filter="value", dprob0=Non
         log = torch.empty(4 * api.dglu_bwd_num_tiles(M, N), dtype=torch.int32, device=dev)
     ws = api.dglu_bwd(a=g["a"], c=g["c"], padded_offsets=g["padded_offsets"], alpha=g["alpha"], beta=g["beta"],
                       prob=g["prob"], dprob=dprob, d_row=d_row, dbias=db, act=spec.act, geglu_filter=geglu_filter,
-                      gate_first=gate_first, tile_log=log, sched=sched, **b_kw)
+                      gate_first=gate_first, tile_log=log, sched=sched, situ_beta1=situ[0], situ_beta2=situ[1],
+                      **b_kw)
     status = api.read_device_status(ws)
     torch.cuda.synchronize()
     out = dict(status=status, d_row=d_row.cpu(), dprob=dprob.cpu(), dbias=None if db is None else db.cpu(),
@@ -78,14 +79,16 @@ def run_dglu_gpu(spec, x, dev, gate_first=True, geglu_filter="value", dprob0=Non
     return out
 
 
-def run_dglu_oracle(spec, x, gate_first=True, geglu_filter="value", dprob0=None, dbias0=None, rows=None):
+def run_dglu_oracle(spec, x, gate_first=True, geglu_filter="value", dprob0=None, dbias0=None, rows=None,
+                    situ=(4.0, 25.0)):
     b_get = dglu_b_getter(spec, x["b"])
     offs = x["padded_offsets"].numpy().astype(np.int64)
     c = to_np(x["c"]) if rows is None else to_np(x["c"][torch.as_tensor(rows)])
     return oracle.dglu_bwd(to_np(x["a"]), b_get, c, offs, x["alpha"].numpy(), x["beta"].numpy(), x["prob"].numpy(),
                            act=spec.act, gate_first=gate_first, geglu_filter=geglu_filter, rows=rows,
                            dprob_in=None if dprob0 is None else to_np(dprob0),
-                           dbias_in=None if dbias0 is None else to_np(dbias0))
+                           dbias_in=None if dbias0 is None else to_np(dbias0), situ_beta1=situ[0],
+                           situ_beta2=situ[1])
 
 
 def wgrad_pack(spec, x):

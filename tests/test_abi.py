@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_struct_layouts_match_library(lib):
-    assert lib.mgg_abi_version() == 1
+    assert lib.mgg_abi_version() == 2
     assert lib.mgg_sizeof_dglu_bwd_args() == ctypes.sizeof(_lib.DgluBwdArgs)
     assert lib.mgg_sizeof_wgrad_args() == ctypes.sizeof(_lib.WgradArgs)
 
@@ -88,7 +88,7 @@ def wgrad_args(**over):
 @pytest.mark.parametrize("over,expect", [
     (dict(L=0), 1), (dict(L=1025), 1), (dict(M=1000), 1), (dict(K=100), 1), (dict(N=48), 1),
     (dict(b_ptrs=FAKE), 1), (dict(b=None), 1), (dict(b_major=1), 1), (dict(c_dtype=3), 1),
-    (dict(d_dtype=-1), 1), (dict(act=2), 1), (dict(geglu_filter=5), 1), (dict(gate_first=2), 1),
+    (dict(d_dtype=-1), 1), (dict(act=3), 1), (dict(act=2, situ_beta1=-1.0), 1), (dict(act=2, situ_beta2=float("inf")), 1), (dict(geglu_filter=5), 1), (dict(gate_first=2), 1),
     (dict(a=FAKE + 8), 1), (dict(c=None), 1), (dict(dprob=FAKE + 4), 1), (dict(workspace=FAKE + 16), 1),
     (dict(workspace_bytes=100), 1), (dict(reserved=1), 1), (dict(dbias=FAKE + 2), 1),
     (dict(sched=7), 1), (dict(sched=-1), 1),

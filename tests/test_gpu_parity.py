@@ -72,6 +72,9 @@ DGLU_CASES = {
     "regpath_swiglu": dict(K=4096, N=96, counts=(256, 0, 256)),
     "regpath_geglu_fp32d_dbias": dict(K=4160, N=64, counts=(256, 512), act="dgeglu", c_std=4.0, d_dtype="fp32",
                                       dbias=True),
+    "situglu": dict(act="dsituglu", c_std=4.0),
+    "situglu_fp32d_dbias": dict(act="dsituglu", c_std=8.0, d_dtype="fp32", dbias=True),
+    "regpath_situglu": dict(K=4096, N=64, counts=(256, 0, 256), act="dsituglu", c_std=4.0),
 }
 
 
@@ -108,6 +111,16 @@ def test_dglu_block_order_and_filter_modes(dev, gate_first, filt):
     x = synth.make_dglu_inputs(spec)
     gpu = run_dglu_gpu(spec, x, dev, gate_first=gate_first, geglu_filter=filt)
     ref = run_dglu_oracle(spec, x, gate_first=gate_first, geglu_filter=filt)
+    check_close("d_row", to_np(gpu["d_row"]), ref["d_row"], TOL["bf16"])
+    check_close("dprob", to_np(gpu["dprob"]), ref["dprob"], TOL_DPROB)
+
+
+@pytest.mark.parametrize("betas", [(2.0, 5.0), (0.5, 40.0)])
+def test_dsituglu_custom_betas(dev, betas):
+    spec = synth.small_dglu_spec("situ_b", act="dsituglu", c_std=6.0)
+    x = synth.make_dglu_inputs(spec)
+    gpu = run_dglu_gpu(spec, x, dev, situ=betas)
+    ref = run_dglu_oracle(spec, x, situ=betas)
     check_close("d_row", to_np(gpu["d_row"]), ref["d_row"], TOL["bf16"])
     check_close("dprob", to_np(gpu["dprob"]), ref["dprob"], TOL_DPROB)
 
