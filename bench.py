@@ -149,13 +149,14 @@ def recorded_traffic(kernel: str, workload: str):
 class Problem:
     """Device-resident inputs/outputs of one workload and the two ABI calls of a step."""
 
-    def __init__(self, workload: str, dev, sched: str = "dynamic"):
+    def __init__(self, workload: str, dev, sched: str = "dynamic", cta: str = "auto"):
         import torch
         from moe_grouped_gemm_persistent_gb300 import api, synth
         self.api = api
         self.torch = torch
         self.dev = dev
         self.sched = sched
+        self.cta = cta
         self.dspec, self.wspec = synth.workload_specs(workload)
         self.d = self.w = None
         if self.dspec is not None:
@@ -203,13 +204,13 @@ class Problem:
             self.dbias.zero_()
         self.api.dglu_bwd(a=x["a"], c=x["c"], padded_offsets=x["padded_offsets"], alpha=x["alpha"], beta=x["beta"],
                           prob=x["prob"], dprob=self.dprob, d_row=self.d_row, dbias=self.dbias, act=s.act,
-                          workspace=self.d_ws, sched=self.sched, **self.b_kw)
+                          workspace=self.d_ws, sched=self.sched, cta=self.cta, **self.b_kw)
 
     def wgrad(self):
         s, y = self.wspec, self.w
         self.api.wgrad(a=y["a"], b=y["b"], offsets=y["offsets"], hidden=s.hidden, inter=s.inter,
                        a_major=s.a_major, b_major=s.b_major, input_order=s.input_order, accumulate=s.accumulate,
-                       workspace=self.w_ws, sched=self.sched, **self.w_kw)
+                       workspace=self.w_ws, sched=self.sched, cta=self.cta, **self.w_kw)
 
     def flops(self):
         f = {}
@@ -414,6 +415,8 @@ def main():
     ap.add_argument("--workload", default="deepseek", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--sched", default="dynamic", choices=["static", "dynamic"])
+    ap.add_argument("--cta", default="auto", choices=["auto", "single", "pair"],
+                    help="tile-to-SM mapping: one CTA per 128-row tile, or a CTA pair per 256-row tile")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -440,7 +443,7 @@ def main():
         torch.distributed.barrier()
     build()
 
-    prob = Problem(args.workload, dev, args.sched)
+    prob = Problem(args.workload, dev, args.sched, args.cta)
     total_ms, per, clocks = time_steps(prob, args.steps, args.warmup, world)
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -492,7 +495,7 @@ def main():
             "config": {"workload": args.workload, "description": WORKLOAD_TEXT[args.workload],
                        "flops_per_step": step_flops, "l2": "inputs larger than L2 (no flush)"
                        if args.workload not in ("tiny",) else "inputs fit in L2 (tiny)",
-                       "parallelism": f"replicas x{world}", "sched": args.sched},
+                       "parallelism": f"replicas x{world}", "sched": args.sched, "cta": args.cta},
             "parts": parts, "roofline": roofline, "frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
             "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": prob.launches_per_step * args.steps,

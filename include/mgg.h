@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MGG_ABI_VERSION 2
+#define MGG_ABI_VERSION 3
 
 typedef enum mgg_status {
   MGG_OK = 0,
@@ -76,6 +76,13 @@ typedef enum mgg_major { MGG_MAJOR_K = 0, MGG_MAJOR_MN = 1 } mgg_major;
 /* Persistent tile scheduling (dGLU page, class API: use_dynamic_sched; wgrad page,
  * "Scheduling, cache, and errors": dynamic persistent scheduling). */
 typedef enum mgg_sched { MGG_SCHED_STATIC = 0, MGG_SCHED_DYNAMIC = 1 } mgg_sched;
+
+/* How output tiles map to SMs.  SINGLE: one CTA per SM computes 128-row tiles (cta_group::1).
+ * PAIR: a cluster of two CTAs on two SMs computes 256-row tiles with cta_group::2 MMAs, each CTA
+ * loading its own 128 rows of A and half of the tile's B columns (half the B traffic per SM);
+ * wgrad accepts PAIR only when hidden is a multiple of 256.  AUTO: the library picks per call.
+ * The result and the tile log (one entry per 128-row CTA tile) do not depend on the mode. */
+typedef enum mgg_cta_mode { MGG_CTA_AUTO = 0, MGG_CTA_SINGLE = 1, MGG_CTA_PAIR = 2 } mgg_cta_mode;
 
 /* wgrad page, "BF16 contract": input_order "tensor2d" (declared strides) or
  * "tensor_ragged" (per-expert K-contiguous blocks concatenated in memory). */
@@ -130,7 +137,7 @@ typedef struct mgg_dglu_bwd_args {
   int32_t geglu_filter;   /* mgg_geglu_filter */
   int32_t gate_first;     /* 1: the gate block precedes the input block in every 64 columns */
   int32_t sched;          /* mgg_sched */
-  int32_t reserved;       /* must be 0 */
+  int32_t cta_mode;       /* mgg_cta_mode */
   float situ_beta1;       /* dSiTU-GLU gate tanh scale, positive finite; 0 = the default 4.0 */
   float situ_beta2;       /* dSiTU-GLU input tanh scale, positive finite; 0 = the default 25.0 */
 } mgg_dglu_bwd_args;
@@ -173,7 +180,7 @@ typedef struct mgg_wgrad_args {
   int32_t out_dtype;      /* mgg_dtype */
   int32_t accumulate;     /* accumulate_on_output */
   int32_t sched;          /* mgg_sched */
-  int32_t reserved0;      /* must be 0 */
+  int32_t cta_mode;       /* mgg_cta_mode */
   int32_t reserved1;      /* must be 0 */
 } mgg_wgrad_args;
 

@@ -22,6 +22,7 @@ ACTS = {"dswiglu": 0, "dgeglu": 1, "dsituglu": 2}
 FILTERS = {"value": 0, "indicator": 1}
 MAJORS = {"k": 0, "mn": 1, "m": 1, "n": 1}
 SCHEDS = {"static": 0, "dynamic": 1}
+CTA_MODES = {"auto": 0, "single": 1, "pair": 2}
 ORDERS = {"tensor2d": 0, "tensor_ragged": 1}
 
 
@@ -34,7 +35,7 @@ class DgluBwdArgs(ctypes.Structure):
         ("tile_log", c_void_p),
         ("workspace_bytes", c_int64), ("tile_log_capacity", c_int64),
         ("b_major", c_int32), ("c_dtype", c_int32), ("d_dtype", c_int32), ("act", c_int32),
-        ("geglu_filter", c_int32), ("gate_first", c_int32), ("sched", c_int32), ("reserved", c_int32),
+        ("geglu_filter", c_int32), ("gate_first", c_int32), ("sched", c_int32), ("cta_mode", c_int32),
         ("situ_beta1", ctypes.c_float), ("situ_beta2", ctypes.c_float),
     ]
 
@@ -46,7 +47,7 @@ class WgradArgs(ctypes.Structure):
         ("workspace", c_void_p), ("tile_log", c_void_p),
         ("workspace_bytes", c_int64), ("tile_log_capacity", c_int64),
         ("a_major", c_int32), ("b_major", c_int32), ("input_order", c_int32), ("out_dtype", c_int32),
-        ("accumulate", c_int32), ("sched", c_int32), ("reserved0", c_int32), ("reserved1", c_int32),
+        ("accumulate", c_int32), ("sched", c_int32), ("cta_mode", c_int32), ("reserved1", c_int32),
     ]
 
 

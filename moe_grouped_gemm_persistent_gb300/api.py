@@ -10,7 +10,7 @@ from typing import Optional, Sequence
 import torch
 
 from . import _lib
-from ._lib import ACTS, DTYPES, FILTERS, MAJORS, ORDERS, SCHEDS, DgluBwdArgs, WgradArgs, check, load
+from ._lib import ACTS, CTA_MODES, DTYPES, FILTERS, MAJORS, ORDERS, SCHEDS, DgluBwdArgs, WgradArgs, check, load
 
 _TORCH_TO_DT = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}
 
@@ -68,7 +68,8 @@ def new_workspace(nbytes: int, device) -> torch.Tensor:
 
 def make_dglu_args(*, a, c, padded_offsets, alpha, beta, prob, dprob, d_row, b=None, b_ptrs=None, N=None,
                    dbias=None, act="dswiglu", geglu_filter="value", gate_first=True, b_major="k",
-                   sched="static", workspace=None, tile_log=None, situ_beta1=4.0, situ_beta2=25.0) -> DgluBwdArgs:
+                   sched="static", workspace=None, tile_log=None, situ_beta1=4.0, situ_beta2=25.0,
+                   cta="auto") -> DgluBwdArgs:
     M, K = a.shape
     L = padded_offsets.numel()
     if N is None:
@@ -93,7 +94,7 @@ def make_dglu_args(*, a, c, padded_offsets, alpha, beta, prob, dprob, d_row, b=N
     args.geglu_filter = FILTERS[geglu_filter]
     args.gate_first = 1 if gate_first else 0
     args.sched = SCHEDS[sched]
-    args.reserved = 0
+    args.cta_mode = CTA_MODES[cta]
     args.situ_beta1 = situ_beta1
     args.situ_beta2 = situ_beta2
     return args
@@ -105,8 +106,10 @@ def dglu_bwd(*, a: torch.Tensor, c: torch.Tensor, padded_offsets: torch.Tensor, 
              dbias: Optional[torch.Tensor] = None, act: str = "dswiglu", geglu_filter: str = "value",
              gate_first: bool = True, b_major: str = "k", sched: str = "dynamic",
              workspace: Optional[torch.Tensor] = None, tile_log: Optional[torch.Tensor] = None, stream=None,
-             situ_beta1: float = 4.0, situ_beta2: float = 25.0):
+             situ_beta1: float = 4.0, situ_beta2: float = 25.0, cta: str = "auto"):
     """Grouped GEMM + dGLU backward (see include/mgg.h, mgg_dglu_bwd).
+
+    ``cta`` is "auto", "single" (128-row tiles per CTA) or "pair" (256-row tiles per CTA pair).
 
     d_row is written; dprob and dbias (when given) are accumulated into.  Returns the
     workspace used (allocated here when not given).
@@ -118,14 +121,14 @@ def dglu_bwd(*, a: torch.Tensor, c: torch.Tensor, padded_offsets: torch.Tensor, 
     args = make_dglu_args(a=a, c=c, padded_offsets=padded_offsets, alpha=alpha, beta=beta, prob=prob, dprob=dprob,
                           d_row=d_row, b=b, b_ptrs=b_ptrs, N=n, dbias=dbias, act=act, geglu_filter=geglu_filter,
                           gate_first=gate_first, b_major=b_major, sched=sched, workspace=workspace,
-                          tile_log=tile_log, situ_beta1=situ_beta1, situ_beta2=situ_beta2)
+                          tile_log=tile_log, situ_beta1=situ_beta1, situ_beta2=situ_beta2, cta=cta)
     check(load().mgg_dglu_bwd(args, _stream(stream)))
     return workspace
 
 
 def make_wgrad_args(*, a, b, offsets, hidden, inter, out=None, out_ptrs=None, out_dtype=None, a_major="k",
                     b_major="n", input_order="tensor2d", accumulate=False, sched="static", workspace=None,
-                    tile_log=None, tokens_sum=None) -> WgradArgs:
+                    tile_log=None, tokens_sum=None, cta="auto") -> WgradArgs:
     L = offsets.numel()
     args = WgradArgs()
     args.hidden, args.inter, args.L = hidden, inter, L
@@ -144,7 +147,8 @@ def make_wgrad_args(*, a, b, offsets, hidden, inter, out=None, out_ptrs=None, ou
     args.out_dtype = DTYPES[out_dtype]
     args.accumulate = 1 if accumulate else 0
     args.sched = SCHEDS[sched]
-    args.reserved0 = args.reserved1 = 0
+    args.cta_mode = CTA_MODES[cta]
+    args.reserved1 = 0
     return args
 
 
@@ -152,15 +156,16 @@ def wgrad(*, a: torch.Tensor, b: torch.Tensor, offsets: torch.Tensor, hidden: in
           out: Optional[torch.Tensor] = None, out_ptrs: Optional[torch.Tensor] = None,
           out_dtype: Optional[str] = None, a_major: str = "k", b_major: str = "n", input_order: str = "tensor2d",
           accumulate: bool = False, sched: str = "dynamic", workspace: Optional[torch.Tensor] = None,
-          tile_log: Optional[torch.Tensor] = None, stream=None):
+          tile_log: Optional[torch.Tensor] = None, stream=None, cta: str = "auto"):
     """Grouped wgrad (see include/mgg.h, mgg_wgrad).  ``a``/``b`` are the flat bf16 storage
-    of A (hidden, T) and B (T, inter) in the declared majors / input order."""
+    of A (hidden, T) and B (T, inter) in the declared majors / input order; ``cta`` as in
+    dglu_bwd ("pair" needs hidden % 256 == 0)."""
     L = offsets.numel()
     if workspace is None:
         workspace = new_workspace(wgrad_workspace_size(L), a.device)
     args = make_wgrad_args(a=a, b=b, offsets=offsets, hidden=hidden, inter=inter, out=out, out_ptrs=out_ptrs,
                            out_dtype=out_dtype, a_major=a_major, b_major=b_major, input_order=input_order,
-                           accumulate=accumulate, sched=sched, workspace=workspace, tile_log=tile_log)
+                           accumulate=accumulate, sched=sched, workspace=workspace, tile_log=tile_log, cta=cta)
     check(load().mgg_wgrad(args, _stream(stream)))
     return workspace
 

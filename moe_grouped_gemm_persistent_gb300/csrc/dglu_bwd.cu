@@ -16,23 +16,27 @@
 
 namespace mgg {
 
-// Per-variant configuration (CS / DS = element bytes of C / D_row).
-//  16-bit C: C reaches shared memory by TMA (a 3-deep ring of 32 x 64 boxes per epilogue warp,
-//            loaded ahead of the math), 4 epilogue warps, 3 operand-ring stages.
-//  fp32 C:   C is read per row into registers one chunk ahead; 8 epilogue warps (two per TMEM
+// Per-variant configuration (CS / DS = element bytes of C / D_row; PAIR = CTA-pair tiles).
+//  TMA-C (16-bit C): C reaches shared memory by TMA (a 3-deep ring of 32 x 64 boxes per epilogue
+//            warp, loaded ahead of the math).
+//  register-C: C is read per row into registers one chunk ahead; 8 epilogue warps (two per TMEM
 //            sub-partition) hide the load latency.
-//  The TMA path trades one operand-ring stage for the C ring, which pays when the epilogue
-//  dominates (small K); for K >= kTmaCMaxK the launcher takes the register path.
-constexpr int64_t kTmaCMaxK = 4095;
+//  The ring stages take whatever shared memory the epilogue leaves (at most 6).  A single CTA
+//  loads 48 KB per stage, a CTA of a pair 32 KB (half of B), so pairs afford the TMA-C ring with
+//  eight warps and four stages; a single CTA only affords it with four warps and three stages,
+//  which pays when the epilogue dominates (K <= kTmaCMaxK).
 
-template <int CS, int DS, bool TMAC>
+template <int CS, int DS, bool TMAC, bool PAIR>
 struct DgluCfg {
   static constexpr bool kTmaC = TMAC && CS == 2;
-  static constexpr int kEpiWarps = kTmaC ? 4 : 8;
+  static constexpr int kEpiWarps = kTmaC ? ((PAIR && DS == 2) ? 8 : 4) : 8;
   static constexpr int kCRing = 3;  // C boxes in flight per warp (TMA path)
   // TMA path: C ring (16-bit D is written back in place) + fp32 D staging; register path: D staging
   static constexpr int kStgBytes = kTmaC ? (kCRing * 4096 + (DS == 4 ? 8192 : 0)) : (DS == 4 ? 8192 : 4096);
-  static constexpr int kStages = (kTmaC || DS == 4) ? 3 : 4;
+  static constexpr int kSlotBytes = 128 * 128 + (PAIR ? 128 : 256) * 128;
+  static constexpr int kFit = (232448 - 2048 - kEpiWarps * kStgBytes) / kSlotBytes;
+  static constexpr int kStages = kFit < 6 ? kFit : 6;
+  static_assert(kStages >= 3, "operand ring too shallow");
 };
 
 struct DgluParams {
@@ -70,9 +74,11 @@ __device__ __forceinline__ float fast_tanh(float x) { return 1.0f - 2.0f * rcp_a
 __device__ __forceinline__ uint32_t swz128(int r, int c16) { return (uint32_t)(r * 128 + ((c16 ^ (r & 7)) << 4)); }
 
 // CS / DS: element size in bytes of C and D_row (2 = bf16/fp16, 4 = fp32).
-template <int BN, int CS, int DS, bool TMAC>
+template <int BN, int CS, int DS, bool TMAC, bool PAIR>
 struct DgluPolicy {
-  using Cfg = DgluCfg<CS, DS, TMAC>;
+  using Cfg = DgluCfg<CS, DS, TMAC, PAIR>;
+  static constexpr int kTileM = PAIR ? 2 * BM : BM;   // rows of a tile (a pair's tile spans both CTAs)
+  static constexpr int kBLoad = PAIR ? BN / 2 : BN;   // B rows this CTA loads
   static constexpr int EPI_WARPS = Cfg::kEpiWarps;
   static constexpr int STG_BYTES = Cfg::kStgBytes;
   static constexpr int kEpiHalves = EPI_WARPS / 4;
@@ -89,11 +95,11 @@ struct DgluPolicy {
       : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(0), b_mn(prm.b_mn), dynamic(prm.dynamic) {}
 
   // Tile order: expert-major; inside an expert, column panels of BN, and inside a panel
-  // the expert's 128-row blocks, so concurrently running CTAs share one B panel and the
-  // expert's A rows in L2.  Tile t belongs to the expert containing row
-  // floor(t / num_n) * 128 (its tiles occupy [begin/128 * num_n, end/128 * num_n)).
+  // the expert's row blocks (kTileM rows; experts are 256-row aligned), so concurrently running
+  // CTAs share one B panel and the expert's A rows in L2.  Tile t belongs to the expert containing
+  // row floor(t / num_n) * kTileM (its tiles occupy [begin/kTileM * num_n, end/kTileM * num_n)).
   __device__ TileWork tile(long long t) const {
-    const int row = (int)(t / p.num_n) * BM;
+    const int row = (int)(t / p.num_n) * kTileM;
     int lo = 0, hi = p.L - 1;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
@@ -102,30 +108,39 @@ struct DgluPolicy {
     }
     const int g = lo;
     const int begin = g ? __ldg(p.offsets + g - 1) : 0;
-    const int mblocks = (__ldg(p.offsets + g) - begin) / BM;
-    const long long u = t - (long long)(begin / BM) * p.num_n;
+    const int mblocks = (__ldg(p.offsets + g) - begin) / kTileM;
+    const long long u = t - (long long)(begin / kTileM) * p.num_n;
     TileWork w;
     w.active = 1;
     w.expert = g;
     w.n0 = (int)(u / mblocks) * BN;
-    w.m0 = begin + (int)(u % mblocks) * BM;
+    w.m0 = begin + (int)(u % mblocks) * kTileM;
     w.k0 = 0;
     w.num_kb = p.num_kb;
     return w;
   }
 
-  __device__ void issue_loads(const TileWork& w, int kb, uint32_t sa, uint32_t sb, uint32_t bar) const {
-    tma_load_2d(sa, &p.tmap_a, bar, kb * BK, w.m0);
+  static __device__ __forceinline__ void load2(uint32_t dst, const void* map, uint32_t bar, int x, int y) {
+    if constexpr (PAIR) tma_load_2d_pair(dst, map, bar, x, y);
+    else tma_load_2d(dst, map, bar, x, y);
+  }
+
+  // This CTA's rows of A (m0 + 128 * rank) and its kBLoad columns of B (n0 + kBLoad * rank).
+  __device__ void issue_loads(const TileWork& w, int kb, uint32_t sa, uint32_t sb, uint32_t bar, int rank) const {
+    const int mrow = w.m0 + rank * BM;
+    const int ncol = w.n0 + rank * kBLoad;
+    load2(sa, &p.tmap_a, bar, kb * BK, mrow);
     if (p.b_maps == nullptr) {
-      tma_load_3d(sb, &p.tmap_b, bar, kb * BK, w.n0, w.expert);
+      if constexpr (PAIR) tma_load_3d_pair(sb, &p.tmap_b, bar, kb * BK, ncol, w.expert);
+      else tma_load_3d(sb, &p.tmap_b, bar, kb * BK, ncol, w.expert);
     } else {
       const CUtensorMap* m = p.b_maps + w.expert;
       if (kb == 0) tmap_acquire(m);
       if (!p.b_mn) {
-        tma_load_2d(sb, m, bar, kb * BK, w.n0);
+        load2(sb, m, bar, kb * BK, ncol);
       } else {
 #pragma unroll
-        for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, m, bar, w.n0 + 64 * j, kb * BK);
+        for (int j = 0; j < kBLoad / 64; ++j) load2(sb + j * 8192, m, bar, ncol + 64 * j, kb * BK);
       }
     }
   }
@@ -267,11 +282,13 @@ struct DgluPolicy {
     atomicAdd(ws + icol + lane, si);
   }
 
-  __device__ __forceinline__ void log_tile(const TileWork& w, long long t) const {
-    if (p.tile_log != nullptr && t < p.tile_log_cap) {
-      int32_t* e = p.tile_log + 4 * t;
+  // One entry per CTA tile of 128 rows (a pair's tile logs two).
+  __device__ __forceinline__ void log_tile(const TileWork& w, long long t, int rank) const {
+    const long long idx = PAIR ? 2 * t + rank : t;
+    if (p.tile_log != nullptr && idx < p.tile_log_cap) {
+      int32_t* e = p.tile_log + 4 * idx;
       e[0] = w.expert;
-      e[1] = w.m0;
+      e[1] = w.m0 + rank * BM;
       e[2] = w.n0;
       e[3] = (int32_t)blockIdx.x;
     }
@@ -279,6 +296,11 @@ struct DgluPolicy {
 
   __device__ __forceinline__ int num_chunks(const TileWork& w) const {
     return (p.N - w.n0 < BN ? p.N - w.n0 : BN) / 32;
+  }
+
+  // Chunks of this warp: half, half + kEpiHalves, ...
+  __device__ __forceinline__ int own_chunks(int nchunks, int half) const {
+    return nchunks > half ? (nchunks - half + kEpiHalves - 1) / kEpiHalves : 0;
   }
 
   // ---------------------------------------------------------------- TMA path for 16-bit C
@@ -313,16 +335,16 @@ struct DgluPolicy {
 
   __device__ void prologue(const TileWork& w, long long, const EpiCtx& ctx) const {
     if constexpr (Cfg::kTmaC) {
-      const int nchunks = num_chunks(w);
-      const int row0 = w.m0 + 32 * ctx.q;
+      const int nown = own_chunks(num_chunks(w), ctx.half);
+      const int row0 = w.m0 + ctx.rank * BM + 32 * ctx.q;
       fence_async_shared();  // earlier generic reads of the ring before the async overwrite
       __syncwarp();
-      if (ctx.lane == 0) {
+      if (ctx.lane == 0 && nown > 0) {
         if constexpr (DS == 2) bulk_wait_read<2>();  // the box of use c_uses was stored 3 uses ago
-        c_issue(ctx, c_uses, w.n0, row0);
-        if (nchunks > 1) {
+        c_issue(ctx, c_uses, w.n0 + 32 * ctx.half, row0);
+        if (nown > 1) {
           if constexpr (DS == 2) bulk_wait_read<1>();
-          c_issue(ctx, c_uses + 1, w.n0 + 32, row0);
+          c_issue(ctx, c_uses + 1, w.n0 + 32 * (ctx.half + kEpiHalves), row0);
         }
       }
       __syncwarp();
@@ -331,29 +353,29 @@ struct DgluPolicy {
 
   __device__ void epilogue_tmac(const TileWork& w, long long t, uint32_t taddr, const EpiCtx& ctx,
                                 AccRelease rel) const {
-    static_assert(kEpiHalves == 1, "one warp per TMEM sub-partition on the TMA path");
-    const int lane = ctx.lane;
+    const int lane = ctx.lane, half = ctx.half;
     const int g = w.expert;
     const float alpha_g = __ldg(p.alpha + g);
     const float alpha2 = alpha_g * alpha_g;
     const float beta_g = __ldg(p.beta + g);
-    const int row0 = w.m0 + ctx.q * 32;
+    const int row0 = w.m0 + ctx.rank * BM + ctx.q * 32;
     const int row = row0 + lane;
     const float pr = __ldg(p.prob + row);
-    const int nchunks = num_chunks(w);
+    const int nown = own_chunks(num_chunks(w), half);
     const uint32_t ring = smem_u32(ctx.stg);
     const uint32_t dstg = ring + kCRing * 4096;  // fp32 D staging
     const int gblk = p.gate_first ? 0 : 1;
     float dprob_acc = 0.f;
     bool released = false;
 #pragma unroll 1
-    for (int c = 0; c < nchunks; ++c) {
-      const uint32_t u = c_uses + c;
+    for (int i = 0; i < nown; ++i) {
+      const int c = half + i * kEpiHalves;
+      const uint32_t u = c_uses + i;
       const uint32_t box = ring + (u % kCRing) * 4096;
       const int j0 = w.n0 + c * 32;
       uint32_t r[32];
       tmem_load_32cols(taddr + c * 32, r);
-      if (c == nchunks - 1) {
+      if (i == nown - 1) {
         rel(lane);
         released = true;
       }
@@ -380,19 +402,19 @@ struct DgluPolicy {
         }
       }
       if (p.dbias_ws != nullptr) dbias_partials(w, j0, lane, gv, iv);
-      if (c + 2 < nchunks) {  // refill the box of use u - 1 with chunk c + 2
+      if (i + 2 < nown) {  // refill the box of use u - 1 with this warp's chunk i + 2
         if constexpr (DS == 4) fence_async_shared();
         __syncwarp();
         if (lane == 0) {
           if constexpr (DS == 2) bulk_wait_read<1>();
-          c_issue(ctx, u + 2, j0 + 64, row0);
+          c_issue(ctx, u + 2, j0 + 64 * kEpiHalves, row0);
         }
       }
     }
     if (!released) rel(lane);
-    c_uses += (uint32_t)nchunks;
-    atomicAdd(p.dprob + row, dprob_acc);
-    if (ctx.q == 0 && lane == 0) log_tile(w, t);
+    c_uses += (uint32_t)nown;
+    if (nown > 0) atomicAdd(p.dprob + row, dprob_acc);
+    if (ctx.q == 0 && half == 0 && lane == 0) log_tile(w, t, ctx.rank);
   }
 
   // ---------------------------------------------------------------- register path for fp32 C
@@ -403,7 +425,7 @@ struct DgluPolicy {
     const float alpha_g = __ldg(p.alpha + g);
     const float alpha2 = alpha_g * alpha_g;
     const float beta_g = __ldg(p.beta + g);
-    const int row0 = w.m0 + ctx.q * 32;
+    const int row0 = w.m0 + ctx.rank * BM + ctx.q * 32;
     const int row = row0 + lane;
     const float pr = __ldg(p.prob + row);
     const size_t row_off = (size_t)row * 2 * (size_t)p.N;
@@ -456,7 +478,7 @@ struct DgluPolicy {
     }
     if (!released) rel(lane);
     if (half < nchunks) atomicAdd(p.dprob + row, dprob_acc);
-    if (ctx.q == 0 && half == 0 && lane == 0) log_tile(w, t);
+    if (ctx.q == 0 && half == 0 && lane == 0) log_tile(w, t, ctx.rank);
   }
 
   __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, bool, const EpiCtx& ctx,
@@ -466,22 +488,23 @@ struct DgluPolicy {
   }
 };
 
-template <int BN, int CS, int DS, bool TMAC>
-__global__ void __launch_bounds__(cta_threads(DgluCfg<CS, DS, TMAC>::kEpiWarps), 1)
+template <int BN, int CS, int DS, bool TMAC, bool PAIR>
+__global__ void __launch_bounds__(cta_threads(DgluCfg<CS, DS, TMAC, PAIR>::kEpiWarps), 1)
     dglu_bwd_kernel(const __grid_constant__ DgluParams prm) {
-  const DgluPolicy<BN, CS, DS, TMAC> pol(prm);
-  persistent_gemm<BN, DgluCfg<CS, DS, TMAC>::kStages>(pol);
+  const DgluPolicy<BN, CS, DS, TMAC, PAIR> pol(prm);
+  persistent_gemm<BN, DgluCfg<CS, DS, TMAC, PAIR>::kStages, PAIR>(pol);
 }
 
-template <int BN, int CS, int DS, bool TMAC>
-static cudaError_t launch_dglu_variant(const DgluParams& prm, int grid, cudaStream_t stream) {
-  using C = DgluCfg<CS, DS, TMAC>;
-  constexpr int smem = SmemLayout<BN, C::kStages, C::kEpiWarps, C::kStgBytes>::DYN_BYTES;
-  auto kern = dglu_bwd_kernel<BN, CS, DS, TMAC>;
+template <int BN, int CS, int DS, bool TMAC, bool PAIR>
+static cudaError_t launch_dglu_variant(const DgluParams& prm, int num_sms, cudaStream_t stream) {
+  using C = DgluCfg<CS, DS, TMAC, PAIR>;
+  constexpr int smem = SmemLayout<PAIR ? BN / 2 : BN, C::kStages, C::kEpiWarps, C::kStgBytes>::DYN_BYTES;
+  auto kern = dglu_bwd_kernel<BN, CS, DS, TMAC, PAIR>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  kern<<<grid, cta_threads(C::kEpiWarps), smem, stream>>>(prm);
-  return cudaGetLastError();
+  static int max_units = 0;  // co-resident CTAs (pairs) of this variant, asked once
+  return launch_persistent(kern, prm, prm.total_tiles, num_sms, PAIR, cta_threads(C::kEpiWarps), smem, &max_units,
+                           stream);
 }
 
 // Checks the device-resident arguments and builds the per-expert weight maps.
@@ -542,7 +565,7 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
   }
   const long long num_n = (a.N + BN - 1) / BN;
-  const long long total = (a.M / BM) * num_n;
+  const long long total = (a.M / (Lc.pair ? 2 * BM : BM)) * num_n;  // M is a multiple of 256
   if (a.tile_log != nullptr && a.tile_log_capacity > 0) {
     err = cudaMemsetAsync(a.tile_log, 0xff, sizeof(int32_t) * 4 * (size_t)a.tile_log_capacity, stream);
     if (err != cudaSuccess) return err;
@@ -585,16 +608,21 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     prm.situ_inv_b2 = 1.0f / prm.situ_b2;
 
     const int cs = a.c_dtype == MGG_FP32 ? 4 : 2, ds = a.d_dtype == MGG_FP32 ? 4 : 2;
-    const bool tmac = cs == 2 && a.K <= kTmaCMaxK;
-    const int grid = (int)(total < Lc.num_sms ? total : Lc.num_sms);
-    if (cs == 2) {
-      if (tmac) err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true>(prm, grid, stream)
-                              : launch_dglu_variant<BN, 2, 4, true>(prm, grid, stream);
-      else err = ds == 2 ? launch_dglu_variant<BN, 2, 2, false>(prm, grid, stream)
-                         : launch_dglu_variant<BN, 2, 4, false>(prm, grid, stream);
+    const int n = Lc.num_sms;
+    if (Lc.pair) {  // pairs take the C ring whenever C is 16-bit
+      if (cs == 2) err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, true>(prm, n, stream)
+                                 : launch_dglu_variant<BN, 2, 4, true, true>(prm, n, stream);
+      else err = ds == 2 ? launch_dglu_variant<BN, 4, 2, false, true>(prm, n, stream)
+                         : launch_dglu_variant<BN, 4, 4, false, true>(prm, n, stream);
+    } else if (cs == 2 && a.K <= kTmaCMaxK) {
+      err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, false>(prm, n, stream)
+                    : launch_dglu_variant<BN, 2, 4, true, false>(prm, n, stream);
+    } else if (cs == 2) {
+      err = ds == 2 ? launch_dglu_variant<BN, 2, 2, false, false>(prm, n, stream)
+                    : launch_dglu_variant<BN, 2, 4, false, false>(prm, n, stream);
     } else {
-      err = ds == 2 ? launch_dglu_variant<BN, 4, 2, false>(prm, grid, stream)
-                    : launch_dglu_variant<BN, 4, 4, false>(prm, grid, stream);
+      err = ds == 2 ? launch_dglu_variant<BN, 4, 2, false, false>(prm, n, stream)
+                    : launch_dglu_variant<BN, 4, 4, false, false>(prm, n, stream);
     }
     if (err != cudaSuccess) return err;
   }

@@ -122,7 +122,8 @@ mgg_status validate_dglu(const mgg_dglu_bwd_args& a) {
     return fail(MGG_ERR_VALUE, "geglu_filter must be VALUE or INDICATOR");
   if (a.gate_first != 0 && a.gate_first != 1) return fail(MGG_ERR_VALUE, "gate_first must be 0 or 1");
   if (a.sched != MGG_SCHED_STATIC && a.sched != MGG_SCHED_DYNAMIC) return fail(MGG_ERR_VALUE, "sched out of range");
-  if (a.reserved != 0) return fail(MGG_ERR_VALUE, "reserved field must be 0");
+  if (a.cta_mode != MGG_CTA_AUTO && a.cta_mode != MGG_CTA_SINGLE && a.cta_mode != MGG_CTA_PAIR)
+    return fail(MGG_ERR_VALUE, "cta_mode out of range");
   const void* req[] = {a.a, a.c, a.padded_offsets, a.alpha, a.beta, a.prob, a.dprob, a.d_row, a.workspace};
   const char* names[] = {"a", "c", "padded_offsets", "alpha", "beta", "prob", "dprob", "d_row", "workspace"};
   for (int i = 0; i < 9; ++i) {
@@ -164,7 +165,11 @@ mgg_status validate_wgrad(const mgg_wgrad_args& a) {
   if (!valid_dtype(a.out_dtype)) return fail(MGG_ERR_VALUE, "out_dtype out of range");
   if (a.accumulate != 0 && a.accumulate != 1) return fail(MGG_ERR_VALUE, "accumulate must be 0 or 1");
   if (a.sched != MGG_SCHED_STATIC && a.sched != MGG_SCHED_DYNAMIC) return fail(MGG_ERR_VALUE, "sched out of range");
-  if (a.reserved0 != 0 || a.reserved1 != 0) return fail(MGG_ERR_VALUE, "reserved fields must be 0");
+  if (a.cta_mode != MGG_CTA_AUTO && a.cta_mode != MGG_CTA_SINGLE && a.cta_mode != MGG_CTA_PAIR)
+    return fail(MGG_ERR_VALUE, "cta_mode out of range");
+  if (a.cta_mode == MGG_CTA_PAIR && a.hidden % 256 != 0)
+    return fail(MGG_ERR_VALUE, "cta_mode PAIR needs hidden to be a multiple of 256");
+  if (a.reserved1 != 0) return fail(MGG_ERR_VALUE, "reserved field must be 0");
   const void* req[] = {a.a, a.b, a.offsets, a.workspace};
   const char* names[] = {"a", "b", "offsets", "workspace"};
   for (int i = 0; i < 4; ++i) {
@@ -184,6 +189,17 @@ mgg_status validate_wgrad(const mgg_wgrad_args& a) {
   }
   return MGG_OK;
 }
+
+// AUTO picks CTA pairs where they measured faster on GB300: for the dgrad whenever a single CTA
+// would read C through registers (fp32 C, or K >= 4096 where the single CTA's C ring would cost an
+// operand stage), since a pair's halved B slot leaves room for the C ring, eight epilogue warps
+// and four stages (Mixtral-shaped K = 4096: +12%; K = 2048 dGeGLU: -3%, so those stay single).
+bool dglu_pair(const mgg_dglu_bwd_args& a) {
+  if (a.cta_mode != MGG_CTA_AUTO) return a.cta_mode == MGG_CTA_PAIR;
+  return a.c_dtype == MGG_FP32 || a.K > kTmaCMaxK;
+}
+
+bool wgrad_pair(const mgg_wgrad_args& a) { return a.cta_mode == MGG_CTA_PAIR && a.hidden % 256 == 0; }
 
 mgg_status from_cuda(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return MGG_OK;
@@ -267,6 +283,8 @@ mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream) {
   Lc.args = args;
   Lc.num_sms = dev.num_sms;
   Lc.tile_n = kDgluTileN;
+  Lc.pair = dglu_pair(a);
+  const uint32_t b_rows = (uint32_t)(Lc.pair ? kDgluTileN / 2 : kDgluTileN);  // B rows one CTA loads
   const uint64_t M = (uint64_t)(a.M > 0 ? a.M : 256), K = (uint64_t)a.K, N = (uint64_t)a.N, L = (uint64_t)a.L;
   {
     const uint64_t dims[2] = {K, M}, strides[1] = {K * 2};
@@ -275,11 +293,11 @@ mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream) {
   }
   if (a.b != nullptr) {
     const uint64_t dims[3] = {K, N, L}, strides[2] = {K * 2, N * K * 2};
-    const uint32_t box[3] = {64, (uint32_t)kDgluTileN, 1};
+    const uint32_t box[3] = {64, b_rows, 1};
     if ((s = encode_bf16(&Lc.tmap_b, a.b, 3, dims, strides, box, "dense B")) != MGG_OK) return s;
   } else if (a.b_major == MGG_MAJOR_K) {
     const uint64_t dims[2] = {K, N}, strides[1] = {K * 2};
-    const uint32_t box[2] = {64, (uint32_t)kDgluTileN};
+    const uint32_t box[2] = {64, b_rows};
     if ((s = encode_bf16(&Lc.tmap_b, a.a, 2, dims, strides, box, "discrete K-major B")) != MGG_OK) return s;
   } else {
     const uint64_t dims[2] = {N, K}, strides[1] = {N * 2};
@@ -314,6 +332,7 @@ mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {
   Lc.args = args;
   Lc.num_sms = dev.num_sms;
   Lc.tile_n = wgrad_tile_n(a.inter);
+  Lc.pair = wgrad_pair(a);
   const bool ragged = a.input_order == MGG_ORDER_TENSOR_RAGGED;
   Lc.a_ragged = ragged && a.a_major == MGG_MAJOR_K;
   Lc.b_ragged = ragged && a.b_major == MGG_MAJOR_K;
@@ -333,7 +352,7 @@ mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {
     if ((s = encode_bf16(&Lc.tmap_b, a.b, 2, dims, strides, box, "B (N-major)")) != MGG_OK) return s;
   } else {  // (T, inter) with T contiguous: rows of T
     const uint64_t dims[2] = {T, I}, strides[1] = {T * 2};
-    const uint32_t box[2] = {64, (uint32_t)Lc.tile_n};
+    const uint32_t box[2] = {64, (uint32_t)(Lc.pair ? Lc.tile_n / 2 : Lc.tile_n)};  // B rows one CTA loads
     if ((s = encode_bf16(&Lc.tmap_b, a.b, 2, dims, strides, box, "B (K-major)")) != MGG_OK) return s;
   }
   {  // outputs: 32-row boxes of one 128-byte row of columns

@@ -25,6 +25,7 @@ struct DgluLaunch {
   const mgg_dglu_bwd_args* args;
   int num_sms;
   int tile_n;
+  bool pair;  // 256-row tiles on CTA pairs (B maps load half a tile's columns)
 };
 
 struct WgradLaunch {
@@ -36,6 +37,7 @@ struct WgradLaunch {
   int tile_n;
   bool a_ragged;  // per-expert A maps built on the device
   bool b_ragged;
+  bool pair;      // 256-row tiles on CTA pairs (B maps load half a tile's columns)
 };
 
 // Launchers (queue the prep kernel, the persistent kernel and finalisers on `stream`).
@@ -51,6 +53,8 @@ cudaError_t launch_tmap_replace_probe(const CUtensorMap& tmpl, void* out, const 
 void set_last_error(const std::string& msg);
 
 constexpr int kDgluTileN = 256;
+// Largest K for which a single CTA stages 16-bit C through a TMA ring (one operand stage less).
+constexpr int64_t kTmaCMaxK = 4095;
 int wgrad_tile_n(int64_t inter);
 
 }  // namespace mgg

@@ -1,27 +1,35 @@
-// Persistent, warp-specialised grouped GEMM pipeline for sm_103a (one CTA per SM).
+// Persistent, warp-specialised grouped GEMM pipeline for sm_103a.
 //
-//   warp 0      TMA producer: one elected thread streams BK-wide slices of the A and
-//               B tiles into a STAGES-deep shared-memory ring (full/empty mbarriers).
-//   warp 1      MMA issuer: allocates TMEM, one thread issues tcgen05.mma (128 x BN x 16,
-//               bf16 in, fp32 accumulate) into one of two TMEM accumulators and commits
-//               the ring slots and the finished accumulator to mbarriers.
-//   warps 2..5  epilogue: each warp owns one 32-lane TMEM sub-partition (rows
-//               32*(warp%4) .. +31 of the tile), reads the accumulator with tcgen05.ld
-//               and hands it to the operation's epilogue while the MMA warp already
-//               accumulates the next tile into the other TMEM buffer.
+//   warp 0      TMA producer: one elected thread streams BK-wide slices of the A and B tiles
+//               into a STAGES-deep shared-memory ring (full/empty mbarriers).
+//   warp 1      TMEM allocator and MMA issuer: one thread issues tcgen05.mma (bf16 in, fp32
+//               accumulate) into one of two TMEM accumulators and commits the ring slots and the
+//               finished accumulator to mbarriers.
+//   warps 2..   epilogue: each warp owns one 32-lane TMEM sub-partition (rows 32*(warp%4) ..
+//               +31 of its CTA's rows), reads the accumulator with tcgen05.ld and hands it to the
+//               operation's epilogue while the MMA already accumulates the next tile.
+//
+// Single CTA (PAIR = false): one CTA per SM computes 128 x BN tiles with cta_group::1.
+// CTA pair (PAIR = true): a cluster of two CTAs on two SMs computes 256 x BN tiles with
+// cta_group::2 MMAs issued by the even CTA; each CTA loads its own 128 rows of A and half of the
+// BN columns of B, so per SM the B traffic and the ring slot shrink by half, and each CTA's TMEM
+// holds the accumulator rows it then writes out.  The even CTA's full barrier counts the bytes of
+// both CTAs' loads; its MMA commits arrive on both CTAs' barriers (multicast); both CTAs' epilogue
+// warps free the accumulator on the even CTA's barrier.
 //
 // The operation supplies a policy object P with
 //   total_tiles, status, a_mn, b_mn, dynamic        status[3] is the dynamic scheduler's tile
 //                                                   counter (zeroed by the preparation kernel)
-//   TileWork tile(long long t)                      same answer for every role
-//   issue_loads(w, kb, sa, sb, bar)                 producer thread
-//   EPI_WARPS                                       epilogue warps (multiple of 4)
-//   STG_BYTES                                       shared memory per epilogue warp
+//   TileWork tile(long long t)                      same answer for every role and both CTAs
+//   issue_loads(w, kb, sa, sb, bar, rank)           producer thread; `bar` is the address the
+//                                                   loads complete on (the even CTA's in a pair)
+//   EPI_WARPS, STG_BYTES                            epilogue warps (multiple of 4), bytes per warp
 //   prologue(w, t, ctx)                             one epilogue warp, before it waits for the
 //                                                   tile's accumulator (e.g. to start input loads)
 //   epilogue(w, t, taddr, have_acc, ctx, rel)       one epilogue warp; EPI_WARPS/4 warps share TMEM
 //        sub-partition ctx.q and split the tile's 32-column chunks (chunk c belongs to ctx.half =
-//        c % (EPI_WARPS/4)); ctx.stg is the warp's 1024-byte aligned STG_BYTES of shared memory,
+//        c % (EPI_WARPS/4)); ctx.rank is the CTA's rank in the pair (its rows start at
+//        m0 + 128*rank); ctx.stg is the warp's 1024-byte aligned STG_BYTES of shared memory,
 //        ctx.bars four mbarriers (count 1) it owns; `rel` frees the TMEM accumulator and must be
 //        called exactly once per tile when have_acc, after the warp's last tcgen05.ld of it.
 #pragma once
@@ -30,10 +38,10 @@
 
 namespace mgg {
 
-constexpr int BM = 128;     // tile rows = UMMA M (cta_group::1)
-constexpr int BK = 64;      // K elements per ring slot: one 128-byte swizzle row of bf16
-constexpr int UMMA_K = 16;  // K of one kind::f16 MMA
-constexpr int kSchedRing = 8;      // tile indices in flight from the producer to the other roles
+constexpr int BM = 128;        // accumulator rows per CTA (UMMA M per CTA)
+constexpr int BK = 64;         // K elements per ring slot: one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;     // K of one kind::f16 MMA
+constexpr int kSchedRing = 8;  // tile indices in flight from the producer to the other roles
 
 // Threads of a CTA with `epi_warps` epilogue warps (a multiple of 4) after the producer and MMA warps.
 __host__ __device__ constexpr int cta_threads(int epi_warps) { return 64 + 32 * epi_warps; }
@@ -46,18 +54,19 @@ struct TileWork {
   int num_kb;   // number of BK slices; 0 = no MMA (the epilogue writes without TMEM)
 };
 
+// BN_LOAD: B rows (N) this CTA loads per slot (BN, or BN/2 in a pair).
 // STG: bytes of output staging per epilogue warp (a multiple of 4 KB: 32 rows x 128 bytes per box).
-template <int BN, int STAGES, int EPI_WARPS, int STG>
+template <int BN_LOAD, int STAGES, int EPI_WARPS, int STG>
 struct SmemLayout {
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = BN_LOAD * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * STG;
   static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * kSchedRing + 4 * EPI_WARPS;
   static constexpr int SCHED_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int MISC_OFF = SCHED_OFF + kSchedRing * 8;
-  static constexpr int BYTES = MISC_OFF + 16;
+  static constexpr int BYTES = MISC_OFF + 16;  // TMEM address, abort flag, skip flag
   static constexpr int DYN_BYTES = BYTES + 1024;  // slack to align the ring to 1024 B
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "ring slots must stay 1024-byte aligned");
   static_assert(DYN_BYTES <= 232448, "shared memory per block");
@@ -65,21 +74,27 @@ struct SmemLayout {
 
 // What one epilogue warp owns.
 struct EpiCtx {
-  int q;          // TMEM sub-partition (rows 32q .. 32q+31 of the tile)
+  int q;          // TMEM sub-partition (rows 32q .. 32q+31 of this CTA's rows)
   int half;       // index among the warps sharing that sub-partition
   int lane;
+  int rank;       // rank of the CTA in its pair (0 for a single CTA)
   uint8_t* stg;   // STG_BYTES of shared memory, 1024-byte aligned
   uint64_t* bars; // four mbarriers initialised with count 1
   WaitGuard wg;
 };
 
-// Frees one TMEM accumulator for the MMA warp (called by every lane of an epilogue warp).
+// Frees one TMEM accumulator for the MMA thread (called by every lane of an epilogue warp):
+// arrives on the accumulator's "empty" barrier, which lives in the even CTA of a pair.
 struct AccRelease {
-  uint64_t* bar;
+  uint32_t bar;    // shared::cta address (single CTA) or shared::cluster address (pair)
+  bool remote;
   __device__ __forceinline__ void operator()(int lane) const {
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar);
+    if (lane == 0) {
+      if (remote) mbar_arrive_remote(bar);
+      else asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+    }
   }
 };
 
@@ -97,18 +112,21 @@ static __device__ __noinline__ void mbar_wait_drain(uint64_t* bar, uint32_t pari
 }
 
 // Every lane of the warp waits; the warp proceeds only if all lanes saw the phase.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, WaitGuard g, int where) {
-  const bool ok = mbar_wait(bar, parity, g, where);
+  const bool ok = CLUSTER ? mbar_wait_cluster(bar, parity, g, where) : mbar_wait(bar, parity, g, where);
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int BN, int STAGES, class P>
+template <int BN, int STAGES, bool PAIR, class P>
 __device__ __forceinline__ void persistent_gemm(const P& p) {
   constexpr int kEpiWarps = P::EPI_WARPS;
   static_assert(kEpiWarps % 4 == 0, "whole TMEM sub-partitions");
-  using S = SmemLayout<BN, STAGES, kEpiWarps, P::STG_BYTES>;
+  constexpr int kBLoad = PAIR ? BN / 2 : BN;
+  using S = SmemLayout<kBLoad, STAGES, kEpiWarps, P::STG_BYTES>;
   constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N");
+  static_assert(!PAIR || BN % 128 == 0, "a pair splits B in 64-column multiples");
 
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -117,18 +135,29 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   uint64_t* tfull_bar = empty_bar + STAGES;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* done_bar = tempty_bar + 2;
-  uint64_t* sfull_bar = done_bar + 1;           // [kSchedRing] a tile index was published
-  uint64_t* sempty_bar = sfull_bar + kSchedRing;  // [kSchedRing] every role has read it
+  uint64_t* sfull_bar = done_bar + 1;             // [kSchedRing] a tile index was published
+  uint64_t* sempty_bar = sfull_bar + kSchedRing;  // [kSchedRing] every consumer has read it
   uint64_t* epi_bars = sempty_bar + kSchedRing;   // [4 * kEpiWarps] owned by the epilogue warps
   volatile long long* sched_ring = reinterpret_cast<volatile long long*>(smem + S::SCHED_OFF);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
 
-  // The preparation kernel of this call found invalid device-side arguments.
-  if (*reinterpret_cast<volatile int*>(p.status) != 0) return;
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  // The preparation kernel of this call found invalid device-side arguments: nothing to do.  A
+  // single CTA leaves at once; the CTAs of a pair must agree, so the even CTA's reading decides
+  // for both (another pair's timeout may set the word between the two readings).
+  volatile int* skip_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 8);
+  if constexpr (!PAIR) {
+    if (*reinterpret_cast<volatile int*>(p.status) != 0) return;
+  } else if (leader && threadIdx.x == 0) {
+    *skip_flag = *reinterpret_cast<volatile int*>(p.status);
+  }
+  // consumers of one published tile index: the MMA thread and the epilogue warps of this CTA, plus
+  // in a pair the peer's producer thread and epilogue warps (the peer's MMA warp is idle)
+  constexpr uint32_t kSchedConsumers = PAIR ? 2u * (1u + kEpiWarps) : 1u + kEpiWarps;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -137,46 +166,68 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], kEpiWarps);  // one arrival per epilogue warp
+      mbar_init(&tempty_bar[a], (PAIR ? 2 : 1) * kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(done_bar, 1);
     for (int r = 0; r < kSchedRing; ++r) {
       mbar_init(&sfull_bar[r], 1);
-      mbar_init(&sempty_bar[r], 1 + kEpiWarps);  // the MMA thread and every epilogue warp
+      mbar_init(&sempty_bar[r], kSchedConsumers);
     }
     for (int b = 0; b < 4 * kEpiWarps; ++b) mbar_init(&epi_bars[b], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // barriers of both CTAs initialised before any remote use
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if constexpr (PAIR) {
+    const int skip = leader ? *skip_flag : (int)ld_cluster_u32(mapa_shared(smem_u32((const void*)skip_flag), 0));
+    if (skip != 0) {
+      cluster_sync_all();  // no CTA leaves while its peer may still read its shared memory
+      if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+      return;
+    }
+  }
   const WaitGuard wg{abort_flag, p.status};
   const bool dynamic = p.dynamic != 0;
   const long long kEnd = 0x7fffffffffffffffLL;
 
-  // Static schedule: CTA b takes tiles b, b + grid, ...  Dynamic schedule: the producer thread
-  // claims the next tile from the global counter and publishes it to the MMA thread and the
-  // epilogue warps through sched_ring; every role sees the same tile sequence.
-  auto static_tile = [&](long long n) -> long long { return (long long)blockIdx.x + n * (long long)gridDim.x; };
+  // Static schedule: unit u (a CTA, or a pair) takes tiles u, u + units, ...  Dynamic schedule:
+  // the (even CTA's) producer thread claims the next tile from the global counter and publishes it
+  // to every consumer through sched_ring; every role sees the same tile sequence.
+  const long long unit = PAIR ? (long long)(blockIdx.x >> 1) : (long long)blockIdx.x;
+  const long long units = PAIR ? (long long)(gridDim.x >> 1) : (long long)gridDim.x;
+  auto static_tile = [&](long long n) -> long long { return unit + n * units; };
+  // `remote_sempty`: consumers in the odd CTA arrive on the even CTA's ring barrier.
   auto consume_tile = [&](long long n, bool is_warp) -> long long {
     const int r = (int)(n % kSchedRing);
     const uint32_t ph = (uint32_t)((n / kSchedRing) & 1);
-    const bool ok = is_warp ? warp_wait(&sfull_bar[r], ph, wg, 6) : mbar_wait(&sfull_bar[r], ph, wg, 6);
+    bool ok;
+    if (is_warp) ok = warp_wait<PAIR>(&sfull_bar[r], ph, wg, 6);
+    else ok = PAIR ? mbar_wait_cluster(&sfull_bar[r], ph, wg, 6) : mbar_wait(&sfull_bar[r], ph, wg, 6);
     if (!ok) return kEnd;
     const long long t = sched_ring[r];
     if (is_warp) __syncwarp();
-    if (!is_warp || lane == 0) mbar_arrive(&sempty_bar[r]);
+    if (!is_warp || lane == 0) {
+      if (PAIR && !leader) mbar_arrive_remote(mapa_shared(smem_u32(&sempty_bar[r]), 0));
+      else mbar_arrive(&sempty_bar[r]);
+    }
     return t;
   };
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------------- TMA producer (both CTAs)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -185,13 +236,22 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       int* counter = p.status + 3;
       auto produce_tile = [&](long long n) -> long long {
         if (!dynamic) return static_tile(n);
+        if (PAIR && !leader) return consume_tile(n, false);
         const int r = (int)(n % kSchedRing);
-        if (!mbar_wait(&sempty_bar[r], (uint32_t)(((n / kSchedRing) & 1) ^ 1), wg, 5)) return kEnd;
+        const uint32_t eph = (uint32_t)(((n / kSchedRing) & 1) ^ 1);
+        // in a pair the odd CTA's consumers release the slot remotely: acquire at cluster scope
+        if (!(PAIR ? mbar_wait_cluster(&sempty_bar[r], eph, wg, 5) : mbar_wait(&sempty_bar[r], eph, wg, 5)))
+          return kEnd;
         const long long t = atomicAdd(counter, 1);
         sched_ring[r] = t;
+        if constexpr (PAIR) {  // the odd CTA's copy of the ring, then its "published" barrier
+          st_cluster_u64(mapa_shared(smem_u32((const void*)&sched_ring[r]), 1), (unsigned long long)t);
+          mbar_arrive_remote(mapa_shared(smem_u32(&sfull_bar[r]), 1));
+        }
         mbar_arrive(&sfull_bar[r]);
         return t;
       };
+      const uint32_t expect = PAIR ? 2u * S::STAGE_BYTES : (uint32_t)S::STAGE_BYTES;
       long long n_tile = 0;
       for (long long t = produce_tile(n_tile++); t < p.total_tiles && ok; t = produce_tile(n_tile++)) {
         const TileWork w = p.tile(t);
@@ -201,9 +261,10 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[stage], S::STAGE_BYTES);
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], expect);
           const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
-          p.issue_loads(w, kb, sa, sa + S::A_BYTES, smem_u32(&full_bar[stage]));
+          const uint32_t bar = PAIR ? mapa_shared(smem_u32(&full_bar[stage]), 0) : smem_u32(&full_bar[stage]);
+          p.issue_loads(w, kb, sa, sa + S::A_BYTES, bar, (int)rank);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -211,7 +272,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
           }
         }
       }
-      if (!ok) {  // let the copies already in flight land before the CTA exits
+      if (!ok && leader) {  // let the copies already in flight land before the CTA exits
         const long long n_flight = issued < STAGES ? issued : STAGES;
         for (long long i = 1; i <= n_flight; ++i) {
           const long long n = issued - i;
@@ -220,9 +281,9 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
+    // ---------------------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && leader) {
+      const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, p.a_mn, p.b_mn);
       const uint32_t a_lbo = p.a_mn ? 8192u : 16u, a_kstep = p.a_mn ? 2048u : 32u;
       const uint32_t b_lbo = p.b_mn ? 8192u : 16u, b_kstep = p.b_mn ? 2048u : 32u;
       int stage = 0;
@@ -249,26 +310,34 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
           for (int k = 0; k < BK / UMMA_K; ++k) {
             const uint64_t ad = smem_desc_sw128(sa + k * a_kstep, a_lbo, 1024u);
             const uint64_t bd = smem_desc_sw128(sb + k * b_kstep, b_lbo, 1024u);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            else umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit(smem_u32(&empty_bar[stage]));  // ring slot free once these MMAs finish
+          // ring slot free (in both CTAs of a pair) once these MMAs finish
+          if constexpr (PAIR) umma_commit_pair_multicast(smem_u32(&empty_bar[stage]), (uint16_t)3);
+          else umma_commit(smem_u32(&empty_bar[stage]));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(smem_u32(&tfull_bar[acc]));  // accumulator complete
+        // accumulator complete (in both CTAs' TMEM)
+        if constexpr (PAIR) umma_commit_pair_multicast(smem_u32(&tfull_bar[acc]), (uint16_t)3);
+        else umma_commit(smem_u32(&tfull_bar[acc]));
         ++local;
       }
-      umma_commit(smem_u32(done_bar));  // all MMAs of this CTA retired before TMEM is freed
+      // every MMA of this CTA (pair) retired before TMEM is freed
+      if constexpr (PAIR) umma_commit_pair_multicast(smem_u32(done_bar), (uint16_t)1);
+      else umma_commit(smem_u32(done_bar));
       mbar_wait_drain(done_bar, 0);
     }
   } else {
-    // ---------------------------------------------------------------- epilogue warps
-    const int q = warp & 3;             // TMEM sub-partition this warp may access
-    const int half = (warp - 2) >> 2;   // which of the sub-partition's warps
-    const EpiCtx ctx{q, half, lane, smem + S::EPI_OFF + (warp - 2) * P::STG_BYTES, epi_bars + 4 * (warp - 2), wg};
+    // ---------------------------------------------------------------- epilogue warps (both CTAs)
+    const int q = warp & 3;                 // TMEM sub-partition this warp may access
+    const int half = (warp - 2) >> 2;       // which of the sub-partition's warps
+    const EpiCtx ctx{q, half, lane, (int)rank, smem + S::EPI_OFF + (warp - 2) * P::STG_BYTES,
+                     epi_bars + 4 * (warp - 2), wg};
     uint32_t local = 0;
     long long n_tile = 0;
     auto next_tile = [&]() { const long long n = n_tile++; return dynamic ? consume_tile(n, true) : static_tile(n); };
@@ -277,25 +346,65 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       if (!w.active) continue;
       p.prologue(w, t, ctx);
       if (w.num_kb == 0) {
-        p.epilogue(w, t, 0u, false, ctx, AccRelease{nullptr});
+        p.epilogue(w, t, 0u, false, ctx, AccRelease{0u, false});
         continue;
       }
       const uint32_t acc = local & 1u, use = local >> 1;
       if (!warp_wait(&tfull_bar[acc], use & 1u, wg, 4)) break;
       tc_fence_after();
-      p.epilogue(w, t, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, true, ctx, AccRelease{&tempty_bar[acc]});
+      const uint32_t ebar = PAIR ? mapa_shared(smem_u32(&tempty_bar[acc]), 0) : smem_u32(&tempty_bar[acc]);
+      p.epilogue(w, t, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, true, ctx, AccRelease{ebar, PAIR});
       ++local;
     }
     if (lane == 0) bulk_wait_all();  // bulk stores complete before the CTA exits
     __syncwarp();
   }
 
+  __syncwarp();  // the role branches above split warps 0 and 1; the barriers below are warp-aligned
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // the pair's MMAs are retired and no peer still signals us
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
+}
+
+// Launches a persistent kernel: one CTA per SM (single) or one cluster of two CTAs per SM pair,
+// never more units than tiles.  `max_units` caches the number of co-resident units of this
+// kernel (0 = not yet known); a pair needs both SMs of a cluster slot, so it asks the runtime.
+template <class Prm>
+inline cudaError_t launch_persistent(void (*kern)(Prm), const Prm& prm, long long total_tiles, int num_sms,
+                                     bool pair, int threads, int smem, int* max_units, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  if (pair) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  int units = *max_units;
+  if (units <= 0) {
+    if (pair) {
+      cfg.gridDim = dim3(2, 1, 1);
+      cudaError_t err = cudaOccupancyMaxActiveClusters(&units, kern, &cfg);
+      if (err != cudaSuccess) return err;
+      if (units <= 0) return cudaErrorInvalidConfiguration;  // no SM pair can hold the kernel
+    } else {
+      units = num_sms;
+    }
+    *max_units = units;
+  }
+  if (total_tiles < units) units = (int)total_tiles;
+  cfg.gridDim = dim3((unsigned)(pair ? 2 * units : units), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
 // ------------------------------------------------------------------------------------

@@ -42,9 +42,12 @@ constexpr int kWgradEpiWarps = 4;
 
 __device__ __forceinline__ uint32_t swz128w(int r, int c16) { return (uint32_t)(r * 128 + ((c16 ^ (r & 7)) << 4)); }
 
-// OS: output element size in bytes (2 = bf16/fp16, 4 = fp32).
-template <int BN, int OS>
+// OS: output element size in bytes (2 = bf16/fp16, 4 = fp32).  PAIR: 256-row tiles computed by a
+// CTA pair (hidden is then a multiple of 256), each CTA loading half of the tile's B columns.
+template <int BN, int OS, bool PAIR>
 struct WgradPolicy {
+  static constexpr int kTileM = PAIR ? 2 * BM : BM;
+  static constexpr int kBLoad = PAIR ? BN / 2 : BN;
   static constexpr int EPI_WARPS = kWgradEpiWarps;
   static constexpr int STG_BYTES = 4096;
   static constexpr int kEpiHalves = EPI_WARPS / 4;
@@ -68,34 +71,42 @@ struct WgradPolicy {
     TileWork w;
     w.expert = e;
     w.active = (end > begin) || !p.accumulate;
-    w.m0 = (local / p.tiles_n) * BM;
+    w.m0 = (local / p.tiles_n) * kTileM;
     w.n0 = (local % p.tiles_n) * BN;
     w.k0 = begin;
     w.num_kb = (end - begin) / BK;
     return w;
   }
 
-  __device__ void issue_loads(const TileWork& w, int kb, uint32_t sa, uint32_t sb, uint32_t bar) const {
+  static __device__ __forceinline__ void load2(uint32_t dst, const void* map, uint32_t bar, int x, int y) {
+    if constexpr (PAIR) tma_load_2d_pair(dst, map, bar, x, y);
+    else tma_load_2d(dst, map, bar, x, y);
+  }
+
+  // This CTA's 128 rows of A (m0 + 128 * rank) and its kBLoad columns of B (n0 + kBLoad * rank).
+  __device__ void issue_loads(const TileWork& w, int kb, uint32_t sa, uint32_t sb, uint32_t bar, int rank) const {
     const int k = w.k0 + kb * BK;
+    const int mrow = w.m0 + rank * BM;
+    const int ncol = w.n0 + rank * kBLoad;
     if (p.a_maps != nullptr) {
       const CUtensorMap* m = p.a_maps + w.expert;
       if (kb == 0) tmap_acquire(m);
-      tma_load_2d(sa, m, bar, kb * BK, w.m0);
+      load2(sa, m, bar, kb * BK, mrow);
     } else if (!p.a_mn) {
-      tma_load_2d(sa, &p.tmap_a, bar, k, w.m0);
+      load2(sa, &p.tmap_a, bar, k, mrow);
     } else {
-      tma_load_2d(sa, &p.tmap_a, bar, w.m0, k);
-      tma_load_2d(sa + 8192, &p.tmap_a, bar, w.m0 + 64, k);
+      load2(sa, &p.tmap_a, bar, mrow, k);
+      load2(sa + 8192, &p.tmap_a, bar, mrow + 64, k);
     }
     if (p.b_maps != nullptr) {
       const CUtensorMap* m = p.b_maps + w.expert;
       if (kb == 0) tmap_acquire(m);
-      tma_load_2d(sb, m, bar, kb * BK, w.n0);
+      load2(sb, m, bar, kb * BK, ncol);
     } else if (p.b_mn) {
 #pragma unroll
-      for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, &p.tmap_b, bar, w.n0 + 64 * j, k);
+      for (int j = 0; j < kBLoad / 64; ++j) load2(sb + j * 8192, &p.tmap_b, bar, ncol + 64 * j, k);
     } else {
-      tma_load_2d(sb, &p.tmap_b, bar, k, w.n0);
+      load2(sb, &p.tmap_b, bar, k, ncol);
     }
   }
 
@@ -106,7 +117,7 @@ struct WgradPolicy {
     const int q = ctx.q, half = ctx.half, lane = ctx.lane;
     uint8_t* stg_ptr = ctx.stg;
     const int e = w.expert;
-    const int row0 = w.m0 + q * 32;
+    const int row0 = w.m0 + ctx.rank * BM + q * 32;
     const int row = row0 + lane;
     const bool rows_in = row0 < p.hidden;
     const uint32_t stg = smem_u32(stg_ptr);
@@ -182,20 +193,22 @@ struct WgradPolicy {
       }
     }
     if (have_acc && !released) rel(lane);
-    if (p.tile_log != nullptr && q == 0 && half == 0 && lane == 0 && t < p.tile_log_cap) {
-      int32_t* l = p.tile_log + 4 * t;
+    // one entry per CTA tile of 128 rows (a pair's tile logs two)
+    const long long idx = PAIR ? 2 * t + ctx.rank : t;
+    if (p.tile_log != nullptr && q == 0 && half == 0 && lane == 0 && idx < p.tile_log_cap) {
+      int32_t* l = p.tile_log + 4 * idx;
       l[0] = e;
-      l[1] = w.m0;
+      l[1] = w.m0 + ctx.rank * BM;
       l[2] = w.n0;
       l[3] = (int32_t)blockIdx.x;
     }
   }
 };
 
-template <int BN, int STAGES, int OS>
+template <int BN, int STAGES, int OS, bool PAIR>
 __global__ void __launch_bounds__(cta_threads(kWgradEpiWarps), 1) wgrad_kernel(const __grid_constant__ WgradParams prm) {
-  const WgradPolicy<BN, OS> pol(prm);
-  persistent_gemm<BN, STAGES>(pol);
+  const WgradPolicy<BN, OS, PAIR> pol(prm);
+  persistent_gemm<BN, STAGES, PAIR>(pol);
 }
 
 // Checks offsets / output pointers, orders experts by decreasing token count and builds
@@ -275,16 +288,25 @@ __global__ void wgrad_prep_kernel(const int32_t* offsets, int L, long long T, co
 // narrow outputs fall back to 128 columns.
 int wgrad_tile_n(int64_t inter) { return inter > 128 ? 256 : 128; }
 
-template <int BN, int STAGES, int OS>
+// Ring depth: as many stages as the shared memory holds, at most 6 (a single CTA loads 48 KB
+// (BN = 256) or 32 KB (BN = 128) per stage, a CTA of a pair half of the B part of that).
+template <int BN, bool PAIR>
+constexpr int wgrad_stages() {
+  constexpr int slot = (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
+  constexpr int fit = (232448 - 2048 - kWgradEpiWarps * 4096) / slot;
+  return fit < 6 ? fit : 6;
+}
+
+template <int BN, int OS, bool PAIR>
 static cudaError_t launch_wgrad_bn(const WgradLaunch& Lc, WgradParams& prm, cudaStream_t stream) {
-  using S = SmemLayout<BN, STAGES, kWgradEpiWarps, 4096>;
-  static_assert(S::DYN_BYTES <= 232448, "shared memory");
-  auto kern = wgrad_kernel<BN, STAGES, OS>;
+  constexpr int STAGES = wgrad_stages<BN, PAIR>();
+  using S = SmemLayout<PAIR ? BN / 2 : BN, STAGES, kWgradEpiWarps, 4096>;
+  auto kern = wgrad_kernel<BN, STAGES, OS, PAIR>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);
   if (err != cudaSuccess) return err;
-  const int grid = (int)(prm.total_tiles < Lc.num_sms ? prm.total_tiles : Lc.num_sms);
-  kern<<<grid, cta_threads(kWgradEpiWarps), S::DYN_BYTES, stream>>>(prm);
-  return cudaGetLastError();
+  static int max_units = 0;  // co-resident CTAs (pairs) of this variant, asked once
+  return launch_persistent(kern, prm, prm.total_tiles, Lc.num_sms, PAIR, cta_threads(kWgradEpiWarps), S::DYN_BYTES,
+                           &max_units, stream);
 }
 
 cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {
@@ -303,7 +325,7 @@ cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
 
   const int BN = Lc.tile_n;
-  const long long tiles_m = (a.hidden + BM - 1) / BM;
+  const long long tiles_m = Lc.pair ? a.hidden / (2 * BM) : (a.hidden + BM - 1) / BM;  // pair: hidden % 256 == 0
   const long long tiles_n = (a.inter + BN - 1) / BN;
   const long long total = a.L * tiles_m * tiles_n;
   if (a.tile_log != nullptr && a.tile_log_capacity > 0) {
@@ -337,8 +359,12 @@ cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {
   prm.out_dtype = a.out_dtype;
   prm.accumulate = a.accumulate != 0;
   const bool fp32 = a.out_dtype == MGG_FP32;
-  if (BN == 256) return fp32 ? launch_wgrad_bn<256, 4, 4>(Lc, prm, stream) : launch_wgrad_bn<256, 4, 2>(Lc, prm, stream);
-  return fp32 ? launch_wgrad_bn<128, 6, 4>(Lc, prm, stream) : launch_wgrad_bn<128, 6, 2>(Lc, prm, stream);
+  if (Lc.pair) {
+    if (BN == 256) return fp32 ? launch_wgrad_bn<256, 4, true>(Lc, prm, stream) : launch_wgrad_bn<256, 2, true>(Lc, prm, stream);
+    return fp32 ? launch_wgrad_bn<128, 4, true>(Lc, prm, stream) : launch_wgrad_bn<128, 2, true>(Lc, prm, stream);
+  }
+  if (BN == 256) return fp32 ? launch_wgrad_bn<256, 4, false>(Lc, prm, stream) : launch_wgrad_bn<256, 2, false>(Lc, prm, stream);
+  return fp32 ? launch_wgrad_bn<128, 4, false>(Lc, prm, stream) : launch_wgrad_bn<128, 2, false>(Lc, prm, stream);
 }
 
 }  // namespace mgg

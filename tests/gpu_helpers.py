@@ -48,7 +48,7 @@ def dglu_b_getter(spec, b):
 
 
 def run_dglu_gpu(spec, x, dev, gate_first=True, geglu_filter="value", dprob0=None, dbias0=None, tile_log=False,
-                 dbias=None, sched="static", situ=(4.0, 25.0)):
+                 dbias=None, sched="static", situ=(4.0, 25.0), cta="auto"):
     """Runs mgg_dglu_bwd on inputs x (CPU tensors from synth) and returns the outputs on CPU."""
     M, N, L = spec.M, spec.N, spec.L
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
@@ -70,7 +70,7 @@ def run_dglu_gpu(spec, x, dev, gate_first=True, geglu_filter="value", dprob0=Non
     ws = api.dglu_bwd(a=g["a"], c=g["c"], padded_offsets=g["padded_offsets"], alpha=g["alpha"], beta=g["beta"],
                       prob=g["prob"], dprob=dprob, d_row=d_row, dbias=db, act=spec.act, geglu_filter=geglu_filter,
                       gate_first=gate_first, tile_log=log, sched=sched, situ_beta1=situ[0], situ_beta2=situ[1],
-                      **b_kw)
+                      cta=cta, **b_kw)
     status = api.read_device_status(ws)
     torch.cuda.synchronize()
     out = dict(status=status, d_row=d_row.cpu(), dprob=dprob.cpu(), dbias=None if db is None else db.cpu(),
@@ -96,7 +96,7 @@ def wgrad_pack(spec, x):
     return x["a"], x["b"]
 
 
-def run_wgrad_gpu(spec, x, dev, tile_log=False, sched="static"):
+def run_wgrad_gpu(spec, x, dev, tile_log=False, sched="static", cta="auto"):
     L, h, i = spec.L, spec.hidden, spec.inter
     a = x["a"].to(dev)
     b = x["b"].to(dev)
@@ -117,7 +117,8 @@ def run_wgrad_gpu(spec, x, dev, tile_log=False, sched="static"):
     if tile_log:
         log = torch.empty(4 * api.wgrad_num_tiles(L, h, i), dtype=torch.int32, device=dev)
     ws = api.wgrad(a=a, b=b, offsets=offs, hidden=h, inter=i, a_major=spec.a_major, b_major=spec.b_major,
-                   input_order=spec.input_order, accumulate=spec.accumulate, tile_log=log, sched=sched, **kw)
+                   input_order=spec.input_order, accumulate=spec.accumulate, tile_log=log, sched=sched, cta=cta,
+                   **kw)
     status = api.read_device_status(ws)
     torch.cuda.synchronize()
     res = out.cpu() if outs is None else torch.stack([o.cpu() for o in outs])

@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_struct_layouts_match_library(lib):
-    assert lib.mgg_abi_version() == 2
+    assert lib.mgg_abi_version() == 3
     assert lib.mgg_sizeof_dglu_bwd_args() == ctypes.sizeof(_lib.DgluBwdArgs)
     assert lib.mgg_sizeof_wgrad_args() == ctypes.sizeof(_lib.WgradArgs)
 
@@ -90,7 +90,7 @@ def wgrad_args(**over):
     (dict(b_ptrs=FAKE), 1), (dict(b=None), 1), (dict(b_major=1), 1), (dict(c_dtype=3), 1),
     (dict(d_dtype=-1), 1), (dict(act=3), 1), (dict(act=2, situ_beta1=-1.0), 1), (dict(act=2, situ_beta2=float("inf")), 1), (dict(geglu_filter=5), 1), (dict(gate_first=2), 1),
     (dict(a=FAKE + 8), 1), (dict(c=None), 1), (dict(dprob=FAKE + 4), 1), (dict(workspace=FAKE + 16), 1),
-    (dict(workspace_bytes=100), 1), (dict(reserved=1), 1), (dict(dbias=FAKE + 2), 1),
+    (dict(workspace_bytes=100), 1), (dict(cta_mode=3), 1), (dict(cta_mode=-1), 1), (dict(dbias=FAKE + 2), 1),
     (dict(sched=7), 1), (dict(sched=-1), 1),
 ])
 def test_dglu_validation_rejects_before_launch(lib, over, expect):
@@ -103,7 +103,8 @@ def test_dglu_validation_rejects_before_launch(lib, over, expect):
     (dict(L=0), 1), (dict(hidden=100), 1), (dict(inter=4), 1), (dict(tokens_sum=1000), 1),
     (dict(out_ptrs=FAKE), 1), (dict(out=None), 1), (dict(a_major=3), 1), (dict(input_order=2), 1),
     (dict(out_dtype=9), 1), (dict(accumulate=2), 1), (dict(b=FAKE + 8), 1), (dict(offsets=None), 1),
-    (dict(workspace_bytes=8), 1), (dict(reserved1=1), 1), (dict(sched=2), 1),
+    (dict(workspace_bytes=8), 1), (dict(reserved1=1), 1), (dict(sched=2), 1), (dict(cta_mode=3), 1),
+    (dict(cta_mode=2, hidden=128), 1),
 ])
 def test_wgrad_validation_rejects_before_launch(lib, over, expect):
     st = lib.mgg_wgrad(wgrad_args(**over), None)

@@ -49,11 +49,11 @@ def _check(spec_d, spec_w, x, y, d_row, dprob, out):
         assert rel_fro(to_np(out[e].cpu()), wref[e]) <= TOL["fp32"], e
 
 
-@pytest.mark.parametrize("sched", ["static", "dynamic"])
-def test_graph_replay_with_new_values_and_new_offsets(dev, sched):
+@pytest.mark.parametrize("sched,cta", [("static", "single"), ("dynamic", "single"), ("dynamic", "pair")])
+def test_graph_replay_with_new_values_and_new_offsets(dev, sched, cta):
     counts = np.array([512, 0, 256, 768], dtype=np.int64)
     spec_d = synth.small_dglu_spec("g", L=4, counts=counts, K=192, N=96)
-    spec_w = synth.small_wgrad_spec("g", L=4, counts=counts, hidden=128, inter=128)
+    spec_w = synth.small_wgrad_spec("g", L=4, counts=counts, hidden=256, inter=128)
     x0 = synth.make_dglu_inputs(spec_d)
     y0 = synth.make_wgrad_inputs(spec_w)
     bufs = {"d": {k: v.to(dev) for k, v in x0.items()}, "w": {k: v.to(dev) for k, v in y0.items() if v is not None}}
@@ -69,9 +69,9 @@ def test_graph_replay_with_new_values_and_new_offsets(dev, sched):
         dprob.zero_()
         api.dglu_bwd(a=d["a"], b=d["b"], c=d["c"], padded_offsets=d["padded_offsets"], alpha=d["alpha"],
                      beta=d["beta"], prob=d["prob"], dprob=dprob, d_row=d_row, workspace=ws_d, sched=sched,
-                     stream=stream)
+                     stream=stream, cta=cta)
         api.wgrad(a=w["a"], b=w["b"], offsets=w["offsets"], hidden=spec_w.hidden, inter=spec_w.inter, out=out,
-                  workspace=ws_w, sched=sched, stream=stream)
+                  workspace=ws_w, sched=sched, stream=stream, cta=cta)
 
     s = torch.cuda.Stream(dev)
     s.wait_stream(torch.cuda.current_stream(dev))

@@ -83,13 +83,18 @@ DGLU_SCHED = [(c, "static") for c in DGLU_CASES] + [("swiglu_dense", "dynamic"),
 DGLU_CASES["many_experts"] = dict(K=128, N=64, counts=(256, 0, 0, 512, 256, 0, 768, 256, 256, 0, 512))
 
 
+# "single": 128-row tiles, one CTA per SM; "pair": 256-row tiles on CTA pairs (cta_group::2).
+CTAS = ["single", "pair"]
+
+
+@pytest.mark.parametrize("cta", CTAS)
 @pytest.mark.parametrize("case,sched", DGLU_SCHED)
-def test_dglu_bwd_parity(dev, case, sched):
+def test_dglu_bwd_parity(dev, case, sched, cta):
     kw = dict(DGLU_CASES[case])
     counts = kw.pop("counts", (256, 0, 512))
     spec = synth.small_dglu_spec(case, L=len(counts), counts=counts, **kw)
     x = synth.make_dglu_inputs(spec)
-    gpu = run_dglu_gpu(spec, x, dev, tile_log=True, sched=sched)
+    gpu = run_dglu_gpu(spec, x, dev, tile_log=True, sched=sched, cta=cta)
     assert gpu["status"] == 0
     ref = run_dglu_oracle(spec, x)
     rows = [(lo, hi) for lo, hi in _ranges(spec)]
@@ -146,11 +151,12 @@ def test_dglu_tiny_workload(dev):
     check_close("dprob", to_np(gpu["dprob"]), ref["dprob"], TOL_DPROB)
 
 
-def test_dglu_bad_offsets_report_and_leave_outputs(dev):
+@pytest.mark.parametrize("cta", CTAS)
+def test_dglu_bad_offsets_report_and_leave_outputs(dev, cta):
     spec = synth.small_dglu_spec("bad")
     x = synth.make_dglu_inputs(spec)
     x["padded_offsets"] = torch.tensor([256, 128, 768], dtype=torch.int32)  # decreasing
-    gpu = run_dglu_gpu(spec, x, dev)
+    gpu = run_dglu_gpu(spec, x, dev, cta=cta)
     assert gpu["status"] == 5
     assert torch.isnan(gpu["d_row"].float()).all()
     assert (gpu["dprob"] == 0).all()
@@ -176,13 +182,16 @@ WGRAD_SCHED = [(c, "static") for c in WGRAD_CASES] + [("k_n_fp32", "dynamic"), (
 WGRAD_CASES["many_experts"] = dict(hidden=256, inter=128, counts=(256, 0, 2048, 0, 512, 256, 0, 768, 256, 1024))
 
 
+@pytest.mark.parametrize("cta", CTAS)
 @pytest.mark.parametrize("case,sched", WGRAD_SCHED)
-def test_wgrad_parity(dev, case, sched):
+def test_wgrad_parity(dev, case, sched, cta):
     kw = dict(WGRAD_CASES[case])
     counts = kw.pop("counts", (512, 0, 256, 768))
+    if cta == "pair" and kw.get("hidden", 192) % 256 != 0:
+        kw["hidden"] = 512  # CTA pairs tile hidden in 256-row blocks
     spec = synth.small_wgrad_spec(case, L=len(counts), counts=counts, **kw)
     x = synth.make_wgrad_inputs(spec)
-    gpu = run_wgrad_gpu(spec, x, dev, tile_log=True, sched=sched)
+    gpu = run_wgrad_gpu(spec, x, dev, tile_log=True, sched=sched, cta=cta)
     assert gpu["status"] == 0
     ref = run_wgrad_oracle(spec, x)
     tol = TOL[spec.out_dtype]
@@ -215,14 +224,15 @@ def test_wgrad_sum_over_experts_equals_full_matmul(dev):
     assert rel_fro(total, A @ B) < TOL["fp32"]
 
 
-def test_wgrad_bad_pointer_reports(dev):
-    spec = synth.small_wgrad_spec("badptr", out_mode="discrete")
+@pytest.mark.parametrize("cta", CTAS)
+def test_wgrad_bad_pointer_reports(dev, cta):
+    spec = synth.small_wgrad_spec("badptr", out_mode="discrete", hidden=256)
     x = synth.make_wgrad_inputs(spec)
     L, h, i = spec.L, spec.hidden, spec.inter
     outs = [torch.zeros(h, i, device=dev) for _ in range(L)]
     ptrs = api.pointer_array(outs, dev)
     ptrs[1] += 4  # misaligned entry
     ws = api.wgrad(a=x["a"].to(dev), b=x["b"].to(dev), offsets=x["offsets"].to(dev), hidden=h, inter=i,
-                   out_ptrs=ptrs, out_dtype="fp32")
+                   out_ptrs=ptrs, out_dtype="fp32", cta=cta)
     assert api.read_device_status(ws) == 6
     assert all((o == 0).all() for o in outs)
