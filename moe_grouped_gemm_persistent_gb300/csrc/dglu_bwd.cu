@@ -126,7 +126,8 @@ struct DgluPolicy {
   }
 
   // This CTA's rows of A (m0 + 128 * rank) and its kBLoad columns of B (n0 + kBLoad * rank).
-  __device__ void issue_loads(const TileWork& w, int kb, uint32_t sa, uint32_t sb, uint32_t bar, int rank) const {
+  __device__ void issue_loads(const TileWork& w, int kb, uint32_t sa, uint32_t sb, uint32_t bar, int rank,
+                              const MapAcquired& acq) const {
     const int mrow = w.m0 + rank * BM;
     const int ncol = w.n0 + rank * kBLoad;
     load2(sa, &p.tmap_a, bar, kb * BK, mrow);
@@ -135,7 +136,7 @@ struct DgluPolicy {
       else tma_load_3d(sb, &p.tmap_b, bar, kb * BK, ncol, w.expert);
     } else {
       const CUtensorMap* m = p.b_maps + w.expert;
-      if (kb == 0) tmap_acquire(m);
+      if (kb == 0 && acq.first_use(w.expert)) tmap_acquire(m);
       if (!p.b_mn) {
         load2(sb, m, bar, kb * BK, ncol);
       } else {

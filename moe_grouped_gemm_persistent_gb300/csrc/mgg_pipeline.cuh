@@ -20,9 +20,10 @@
 // The operation supplies a policy object P with
 //   total_tiles, status, a_mn, b_mn, dynamic        status[3] is the dynamic scheduler's tile
 //                                                   counter (zeroed by the preparation kernel)
-//   TileWork tile(long long t)                      same answer for every role and both CTAs
-//   issue_loads(w, kb, sa, sb, bar, rank)           producer thread; `bar` is the address the
-//                                                   loads complete on (the even CTA's in a pair)
+//   TileWork tile(long long t)                      called once per tile, by the producer thread
+//   issue_loads(w, kb, sa, sb, bar, rank, acq)      producer thread; `bar` is the address the
+//                                                   loads complete on (the even CTA's in a pair);
+//                                                   `acq` records the maps it has acquired
 //   EPI_WARPS, STG_BYTES                            epilogue warps (multiple of 4), bytes per warp
 //   prologue(w, t, ctx)                             one epilogue warp, before it waits for the
 //                                                   tile's accumulator (e.g. to start input loads)
@@ -41,7 +42,26 @@ namespace mgg {
 constexpr int BM = 128;        // accumulator rows per CTA (UMMA M per CTA)
 constexpr int BK = 64;         // K elements per ring slot: one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;     // K of one kind::f16 MMA
-constexpr int kSchedRing = 8;  // tile indices in flight from the producer to the other roles
+constexpr int kSchedRing = 8;  // published tiles in flight from the producer to the other roles
+constexpr int kSchedEntry = 32; // bytes of one published tile: index + TileWork
+constexpr int kMaxExperts = 1024;
+constexpr int kAcqWords = kMaxExperts / 32;  // one bit per expert
+
+// Per-thread record of the per-expert tensor maps (built in global memory by the preparation
+// kernel) this thread has already acquired for the tensormap proxy.  One acquire per map and
+// thread is enough: the maps do not change while the kernel runs, and the fence orders all of
+// this thread's later TMA uses of the map after the preparation kernel's writes.
+struct MapAcquired {
+  uint32_t* bits;  // kAcqWords words of shared memory owned by one thread
+  // True the first time expert e is seen: the caller then acquires that expert's maps.
+  __device__ __forceinline__ bool first_use(int e) const {
+    const uint32_t m = 1u << (e & 31);
+    const uint32_t w = bits[e >> 5];
+    if (w & m) return false;
+    bits[e >> 5] = w | m;
+    return true;
+  }
+};
 
 // Threads of a CTA with `epi_warps` epilogue warps (a multiple of 4) after the producer and MMA warps.
 __host__ __device__ constexpr int cta_threads(int epi_warps) { return 64 + 32 * epi_warps; }
@@ -64,11 +84,13 @@ struct SmemLayout {
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * STG;
   static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * kSchedRing + 4 * EPI_WARPS;
-  static constexpr int SCHED_OFF = BAR_OFF + NUM_BARS * 8;
-  static constexpr int MISC_OFF = SCHED_OFF + kSchedRing * 8;
+  static constexpr int SCHED_OFF = (BAR_OFF + NUM_BARS * 8 + 15) / 16 * 16;
+  static constexpr int ACQ_OFF = SCHED_OFF + kSchedRing * kSchedEntry;  // producer, then each epilogue warp
+  static constexpr int MISC_OFF = ACQ_OFF + (1 + EPI_WARPS) * kAcqWords * 4;
   static constexpr int BYTES = MISC_OFF + 16;  // TMEM address, abort flag, skip flag
   static constexpr int DYN_BYTES = BYTES + 1024;  // slack to align the ring to 1024 B
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "ring slots must stay 1024-byte aligned");
+  static_assert(SCHED_OFF % 16 == 0, "16-byte aligned published tiles");
   static_assert(DYN_BYTES <= 232448, "shared memory per block");
 };
 
@@ -80,6 +102,7 @@ struct EpiCtx {
   int rank;       // rank of the CTA in its pair (0 for a single CTA)
   uint8_t* stg;   // STG_BYTES of shared memory, 1024-byte aligned
   uint64_t* bars; // four mbarriers initialised with count 1
+  MapAcquired acq;  // the tensor maps lane 0 of this warp has acquired
   WaitGuard wg;
 };
 
@@ -135,10 +158,10 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   uint64_t* tfull_bar = empty_bar + STAGES;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* done_bar = tempty_bar + 2;
-  uint64_t* sfull_bar = done_bar + 1;             // [kSchedRing] a tile index was published
+  uint64_t* sfull_bar = done_bar + 1;             // [kSchedRing] a tile was published
   uint64_t* sempty_bar = sfull_bar + kSchedRing;  // [kSchedRing] every consumer has read it
   uint64_t* epi_bars = sempty_bar + kSchedRing;   // [4 * kEpiWarps] owned by the epilogue warps
-  volatile long long* sched_ring = reinterpret_cast<volatile long long*>(smem + S::SCHED_OFF);
+  const uint32_t sched_ring = smem_u32(smem + S::SCHED_OFF);  // [kSchedRing] x {t, TileWork}
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
 
@@ -174,6 +197,8 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       mbar_init(&sempty_bar[r], kSchedConsumers);
     }
     for (int b = 0; b < 4 * kEpiWarps; ++b) mbar_init(&epi_bars[b], 1);
+    uint32_t* acq = reinterpret_cast<uint32_t*>(smem + S::ACQ_OFF);
+    for (int i = 0; i < (1 + kEpiWarps) * kAcqWords; ++i) acq[i] = 0u;
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -204,26 +229,34 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   const long long kEnd = 0x7fffffffffffffffLL;
 
   // Static schedule: unit u (a CTA, or a pair) takes tiles u, u + units, ...  Dynamic schedule:
-  // the (even CTA's) producer thread claims the next tile from the global counter and publishes it
-  // to every consumer through sched_ring; every role sees the same tile sequence.
+  // the next tile comes from the global counter.  Either way the (even CTA's) producer thread
+  // alone computes each tile's TileWork and publishes {t, TileWork} through the shared-memory
+  // ring (into both CTAs of a pair), so the other roles never touch global memory to schedule.
+  // The last entry published has t >= total_tiles and ends every role's loop.
   const long long unit = PAIR ? (long long)(blockIdx.x >> 1) : (long long)blockIdx.x;
   const long long units = PAIR ? (long long)(gridDim.x >> 1) : (long long)gridDim.x;
-  auto static_tile = [&](long long n) -> long long { return unit + n * units; };
-  // `remote_sempty`: consumers in the odd CTA arrive on the even CTA's ring barrier.
-  auto consume_tile = [&](long long n, bool is_warp) -> long long {
+  // Consumers in the odd CTA of a pair release the slot on the even CTA's barrier.
+  auto consume_tile = [&](long long n, bool is_warp, TileWork& w) -> long long {
     const int r = (int)(n % kSchedRing);
     const uint32_t ph = (uint32_t)((n / kSchedRing) & 1);
     bool ok;
     if (is_warp) ok = warp_wait<PAIR>(&sfull_bar[r], ph, wg, 6);
     else ok = PAIR ? mbar_wait_cluster(&sfull_bar[r], ph, wg, 6) : mbar_wait(&sfull_bar[r], ph, wg, 6);
     if (!ok) return kEnd;
-    const long long t = sched_ring[r];
+    const uint4 e0 = ld_shared_v4(sched_ring + r * kSchedEntry);
+    const uint4 e1 = ld_shared_v4(sched_ring + r * kSchedEntry + 16);
     if (is_warp) __syncwarp();
     if (!is_warp || lane == 0) {
       if (PAIR && !leader) mbar_arrive_remote(mapa_shared(smem_u32(&sempty_bar[r]), 0));
       else mbar_arrive(&sempty_bar[r]);
     }
-    return t;
+    w.active = (int)e0.z;
+    w.expert = (int)e0.w;
+    w.m0 = (int)e1.x;
+    w.n0 = (int)e1.y;
+    w.k0 = (int)e1.z;
+    w.num_kb = (int)e1.w;
+    return (long long)(((unsigned long long)e0.y << 32) | e0.x);
   };
 
   if (warp == 0) {
@@ -234,27 +267,39 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       long long issued = 0;
       bool ok = true;
       int* counter = p.status + 3;
-      auto produce_tile = [&](long long n) -> long long {
-        if (!dynamic) return static_tile(n);
-        if (PAIR && !leader) return consume_tile(n, false);
+      auto produce_tile = [&](long long n, TileWork& w) -> long long {
+        if (PAIR && !leader) return consume_tile(n, false, w);
         const int r = (int)(n % kSchedRing);
         const uint32_t eph = (uint32_t)(((n / kSchedRing) & 1) ^ 1);
         // in a pair the odd CTA's consumers release the slot remotely: acquire at cluster scope
         if (!(PAIR ? mbar_wait_cluster(&sempty_bar[r], eph, wg, 5) : mbar_wait(&sempty_bar[r], eph, wg, 5)))
           return kEnd;
-        const long long t = atomicAdd(counter, 1);
-        sched_ring[r] = t;
-        if constexpr (PAIR) {  // the odd CTA's copy of the ring, then its "published" barrier
-          st_cluster_u64(mapa_shared(smem_u32((const void*)&sched_ring[r]), 1), (unsigned long long)t);
+        long long t = dynamic ? (long long)atomicAdd(counter, 1) : unit + n * units;
+        if (t >= p.total_tiles) {
+          t = p.total_tiles;
+          w = TileWork{0, 0, 0, 0, 0, 0};
+        } else {
+          w = p.tile(t);
+        }
+        const uint32_t t_lo = (uint32_t)((unsigned long long)t & 0xffffffffu);
+        const uint32_t t_hi = (uint32_t)((unsigned long long)t >> 32);
+        const uint32_t slot = sched_ring + r * kSchedEntry;
+        st_shared_v4(slot, t_lo, t_hi, (uint32_t)w.active, (uint32_t)w.expert);
+        st_shared_v4(slot + 16, (uint32_t)w.m0, (uint32_t)w.n0, (uint32_t)w.k0, (uint32_t)w.num_kb);
+        if constexpr (PAIR) {  // the odd CTA's copy of the entry, then its "published" barrier
+          const uint32_t peer = mapa_shared(slot, 1);
+          st_cluster_v4(peer, t_lo, t_hi, (uint32_t)w.active, (uint32_t)w.expert);
+          st_cluster_v4(peer + 16, (uint32_t)w.m0, (uint32_t)w.n0, (uint32_t)w.k0, (uint32_t)w.num_kb);
           mbar_arrive_remote(mapa_shared(smem_u32(&sfull_bar[r]), 1));
         }
         mbar_arrive(&sfull_bar[r]);
         return t;
       };
       const uint32_t expect = PAIR ? 2u * S::STAGE_BYTES : (uint32_t)S::STAGE_BYTES;
+      const MapAcquired acq_producer{reinterpret_cast<uint32_t*>(smem + S::ACQ_OFF)};
       long long n_tile = 0;
-      for (long long t = produce_tile(n_tile++); t < p.total_tiles && ok; t = produce_tile(n_tile++)) {
-        const TileWork w = p.tile(t);
+      TileWork w;
+      for (long long t = produce_tile(n_tile++, w); t < p.total_tiles && ok; t = produce_tile(n_tile++, w)) {
         if (!w.active) continue;
         for (int kb = 0; kb < w.num_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wg, 1)) {
@@ -264,7 +309,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], expect);
           const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
           const uint32_t bar = PAIR ? mapa_shared(smem_u32(&full_bar[stage]), 0) : smem_u32(&full_bar[stage]);
-          p.issue_loads(w, kb, sa, sa + S::A_BYTES, bar, (int)rank);
+          p.issue_loads(w, kb, sa, sa + S::A_BYTES, bar, (int)rank, acq_producer);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -290,9 +335,9 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       uint32_t phase = 0, local = 0;
       bool ok = true;
       long long n_tile = 0;
-      auto next_tile = [&]() { const long long n = n_tile++; return dynamic ? consume_tile(n, false) : static_tile(n); };
-      for (long long t = next_tile(); t < p.total_tiles && ok; t = next_tile()) {
-        const TileWork w = p.tile(t);
+      TileWork w;
+      for (long long t = consume_tile(n_tile++, false, w); t < p.total_tiles && ok;
+           t = consume_tile(n_tile++, false, w)) {
         if (!w.active || w.num_kb == 0) continue;
         const uint32_t acc = local & 1u, use = local >> 1;
         if (!mbar_wait(&tempty_bar[acc], (use & 1u) ^ 1u, wg, 2)) break;
@@ -337,12 +382,12 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     const int q = warp & 3;                 // TMEM sub-partition this warp may access
     const int half = (warp - 2) >> 2;       // which of the sub-partition's warps
     const EpiCtx ctx{q, half, lane, (int)rank, smem + S::EPI_OFF + (warp - 2) * P::STG_BYTES,
-                     epi_bars + 4 * (warp - 2), wg};
+                     epi_bars + 4 * (warp - 2),
+                     MapAcquired{reinterpret_cast<uint32_t*>(smem + S::ACQ_OFF) + (warp - 1) * kAcqWords}, wg};
     uint32_t local = 0;
     long long n_tile = 0;
-    auto next_tile = [&]() { const long long n = n_tile++; return dynamic ? consume_tile(n, true) : static_tile(n); };
-    for (long long t = next_tile(); t < p.total_tiles; t = next_tile()) {
-      const TileWork w = p.tile(t);
+    TileWork w;
+    for (long long t = consume_tile(n_tile++, true, w); t < p.total_tiles; t = consume_tile(n_tile++, true, w)) {
       if (!w.active) continue;
       p.prologue(w, t, ctx);
       if (w.num_kb == 0) {

@@ -291,8 +291,9 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr) {
   return v;
 }
 
-__device__ __forceinline__ void st_cluster_u64(uint32_t cluster_addr, unsigned long long v) {
-  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(cluster_addr), "l"(v) : "memory");
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
 }
 
 // try_wait with cluster-scope acquire (the phase was completed by a peer CTA's release).

@@ -7,8 +7,8 @@
 // dense (L, hidden, inter) tensor or to per-expert output pointers.
 //
 // Scheduling: the preparation kernel orders experts by decreasing token count; the
-// persistent CTAs walk the (expert, hidden tile, inter tile) space in that order, so the
-// longest reductions start first (longest-processing-time-first).
+// persistent CTAs walk the (expert, hidden tile, inter tile) space in that order
+// (longest-processing-time-first), the dynamic schedule alternating between its two ends.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -39,6 +39,7 @@ struct WgradParams {
 };
 
 constexpr int kWgradEpiWarps = 4;
+constexpr int kWgradStgBytes = 8192;  // 4 KB staging boxes per epilogue warp (a ring of two)
 
 __device__ __forceinline__ uint32_t swz128w(int r, int c16) { return (uint32_t)(r * 128 + ((c16 ^ (r & 7)) << 4)); }
 
@@ -49,10 +50,12 @@ struct WgradPolicy {
   static constexpr int kTileM = PAIR ? 2 * BM : BM;
   static constexpr int kBLoad = PAIR ? BN / 2 : BN;
   static constexpr int EPI_WARPS = kWgradEpiWarps;
-  static constexpr int STG_BYTES = 4096;
+  static constexpr int STG_BYTES = kWgradStgBytes;
   static constexpr int kEpiHalves = EPI_WARPS / 4;
   static constexpr int CW = 128 / OS;  // output columns per staged chunk (one 128-byte row)
   const WgradParams& p;
+  static constexpr int kBoxes = STG_BYTES / 4096;
+  mutable uint32_t stg_uses = 0;  // staging boxes this warp has filled (box = stg_uses % kBoxes)
   long long total_tiles;
   int* status;
   int a_mn, b_mn;
@@ -62,9 +65,13 @@ struct WgradPolicy {
       : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(prm.a_mn), b_mn(prm.b_mn),
         dynamic(prm.dynamic) {}
 
+  // Tiles in LPT order (experts by decreasing token count).  The dynamic schedule hands them out
+  // alternately from the long end and the short end, so each SM interleaves MMA-bound long
+  // reductions with store-bound short ones; the static schedule deals them round-robin.
   __device__ TileWork tile(long long t) const {
-    const int slot = (int)(t / p.tiles_per_expert);
-    const int local = (int)(t % p.tiles_per_expert);
+    const long long idx = !p.dynamic ? t : (t & 1) ? p.total_tiles - 1 - (t >> 1) : (t >> 1);
+    const int slot = (int)(idx / p.tiles_per_expert);
+    const int local = (int)(idx % p.tiles_per_expert);
     const int e = __ldg(p.order + slot);
     const int begin = e ? __ldg(p.offsets + e - 1) : 0;
     const int end = __ldg(p.offsets + e);
@@ -84,13 +91,17 @@ struct WgradPolicy {
   }
 
   // This CTA's 128 rows of A (m0 + 128 * rank) and its kBLoad columns of B (n0 + kBLoad * rank).
-  __device__ void issue_loads(const TileWork& w, int kb, uint32_t sa, uint32_t sb, uint32_t bar, int rank) const {
+  __device__ void issue_loads(const TileWork& w, int kb, uint32_t sa, uint32_t sb, uint32_t bar, int rank,
+                              const MapAcquired& acq) const {
     const int k = w.k0 + kb * BK;
     const int mrow = w.m0 + rank * BM;
     const int ncol = w.n0 + rank * kBLoad;
+    if (kb == 0 && (p.a_maps != nullptr || p.b_maps != nullptr) && acq.first_use(w.expert)) {
+      if (p.a_maps != nullptr) tmap_acquire(p.a_maps + w.expert);
+      if (p.b_maps != nullptr) tmap_acquire(p.b_maps + w.expert);
+    }
     if (p.a_maps != nullptr) {
       const CUtensorMap* m = p.a_maps + w.expert;
-      if (kb == 0) tmap_acquire(m);
       load2(sa, m, bar, kb * BK, mrow);
     } else if (!p.a_mn) {
       load2(sa, &p.tmap_a, bar, k, mrow);
@@ -99,9 +110,7 @@ struct WgradPolicy {
       load2(sa + 8192, &p.tmap_a, bar, mrow + 64, k);
     }
     if (p.b_maps != nullptr) {
-      const CUtensorMap* m = p.b_maps + w.expert;
-      if (kb == 0) tmap_acquire(m);
-      load2(sb, m, bar, kb * BK, ncol);
+      load2(sb, p.b_maps + w.expert, bar, kb * BK, ncol);
     } else if (p.b_mn) {
 #pragma unroll
       for (int j = 0; j < kBLoad / 64; ++j) load2(sb + j * 8192, &p.tmap_b, bar, ncol + 64 * j, k);
@@ -125,7 +134,7 @@ struct WgradPolicy {
     const int nchunks = (ncols + CW - 1) / CW;
     const bool discrete = p.out_maps != nullptr;
     const CUtensorMap* map = discrete ? p.out_maps + e : &p.tmap_out;
-    if (discrete && lane == 0) tmap_acquire(map);
+    if (discrete && lane == 0 && ctx.acq.first_use(e)) tmap_acquire(map);
     // fp32 accumulation is a bulk reduce-add at the memory side; 16-bit accumulation reads the old values
     const bool reduce = p.accumulate && OS == 4;
     const bool add_old = p.accumulate && OS == 2;
@@ -165,29 +174,33 @@ struct WgradPolicy {
           for (int k = 0; k < 32; ++k) v[32 * h + k] += old[k];
         }
       }
-      if (lane == 0) bulk_wait_read_all();
+      if (!rows_in) continue;  // rows past hidden (single-CTA tiles only): nothing to write
+      // the box was last filled kBoxes stores ago: wait until at most kBoxes - 1 stores still read
+      const uint32_t box = stg + (stg_uses % kBoxes) * 4096u;
+      ++stg_uses;
+      if (lane == 0) bulk_wait_read<kBoxes - 1>();
       __syncwarp();
       if constexpr (OS == 4) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          st_shared_v4(stg + swz128w(lane, i), __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+          st_shared_v4(box + swz128w(lane, i), __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
                        __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
       } else {
         const int dt = p.out_dtype;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          st_shared_v4(stg + swz128w(lane, i), pack2(v[8 * i], v[8 * i + 1], dt), pack2(v[8 * i + 2], v[8 * i + 3], dt),
+          st_shared_v4(box + swz128w(lane, i), pack2(v[8 * i], v[8 * i + 1], dt), pack2(v[8 * i + 2], v[8 * i + 3], dt),
                        pack2(v[8 * i + 4], v[8 * i + 5], dt), pack2(v[8 * i + 6], v[8 * i + 7], dt));
       }
       fence_async_shared();
       __syncwarp();
-      if (lane == 0 && rows_in) {
+      if (lane == 0) {
         if (discrete) {
-          if (reduce) tma_reduce_add_2d(map, stg, col0, row0);
-          else tma_store_2d(map, stg, col0, row0);
+          if (reduce) tma_reduce_add_2d(map, box, col0, row0);
+          else tma_store_2d(map, box, col0, row0);
         } else {
-          if (reduce) tma_reduce_add_3d(map, stg, col0, row0, e);
-          else tma_store_3d(map, stg, col0, row0, e);
+          if (reduce) tma_reduce_add_3d(map, box, col0, row0, e);
+          else tma_store_3d(map, box, col0, row0, e);
         }
         bulk_commit_group();
       }
@@ -293,14 +306,14 @@ int wgrad_tile_n(int64_t inter) { return inter > 128 ? 256 : 128; }
 template <int BN, bool PAIR>
 constexpr int wgrad_stages() {
   constexpr int slot = (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
-  constexpr int fit = (232448 - 2048 - kWgradEpiWarps * 4096) / slot;
+  constexpr int fit = (232448 - 2048 - kWgradEpiWarps * kWgradStgBytes) / slot;
   return fit < 6 ? fit : 6;
 }
 
 template <int BN, int OS, bool PAIR>
 static cudaError_t launch_wgrad_bn(const WgradLaunch& Lc, WgradParams& prm, cudaStream_t stream) {
   constexpr int STAGES = wgrad_stages<BN, PAIR>();
-  using S = SmemLayout<PAIR ? BN / 2 : BN, STAGES, kWgradEpiWarps, 4096>;
+  using S = SmemLayout<PAIR ? BN / 2 : BN, STAGES, kWgradEpiWarps, kWgradStgBytes>;
   auto kern = wgrad_kernel<BN, STAGES, OS, PAIR>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);
   if (err != cudaSuccess) return err;
