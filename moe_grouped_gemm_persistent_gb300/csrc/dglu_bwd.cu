@@ -18,24 +18,25 @@ namespace mgg {
 
 // Per-variant configuration (CS / DS = element bytes of C / D_row; PAIR = CTA-pair tiles).
 //  TMA-C (16-bit C): C reaches shared memory by TMA (a 3-deep ring of 32 x 64 boxes per epilogue
-//            warp, loaded ahead of the math).
+//            warp, loaded ahead of the math); the results go back out of the consumed box (16-bit
+//            D, or the gate half of fp32 D, whose input half takes one more 4 KB box).
 //  register-C: C is read per row into registers one chunk ahead; 8 epilogue warps (two per TMEM
 //            sub-partition) hide the load latency.
 //  The ring stages take whatever shared memory the epilogue leaves (at most 6).  A single CTA
 //  loads 48 KB per stage, a CTA of a pair 32 KB (half of B), so pairs afford the TMA-C ring with
-//  eight warps and four stages; a single CTA only affords it with four warps and three stages,
-//  which pays when the epilogue dominates (K <= kTmaCMaxK).
+//  eight warps for 16-bit D (fp32 D keeps four warps and five stages: eight measured slower with
+//  the three stages left); a single CTA only affords it with four warps and three stages, which
+//  pays when the epilogue dominates (K <= kTmaCMaxK).
 
 template <int CS, int DS, bool TMAC, bool PAIR>
 struct DgluCfg {
   static constexpr bool kTmaC = TMAC && CS == 2;
   static constexpr int kEpiWarps = kTmaC ? ((PAIR && DS == 2) ? 8 : 4) : 8;
   static constexpr int kCRing = 3;  // C boxes in flight per warp (TMA path)
-  // TMA path: C ring (16-bit D is written back in place) + fp32 D staging; register path: D staging
-  static constexpr int kStgBytes = kTmaC ? (kCRing * 4096 + (DS == 4 ? 8192 : 0)) : (DS == 4 ? 8192 : 4096);
-  static constexpr int kSlotBytes = 128 * 128 + (PAIR ? 128 : 256) * 128;
-  static constexpr int kFit = (232448 - 2048 - kEpiWarps * kStgBytes) / kSlotBytes;
-  static constexpr int kStages = kFit < 6 ? kFit : 6;
+  // TMA path: C ring + the input half of fp32 D; register path: D staging
+  static constexpr int kStgBytes = kTmaC ? (kCRing * 4096 + (DS == 4 ? 4096 : 0)) : (DS == 4 ? 8192 : 4096);
+  static constexpr int kStages = max_stages(PAIR ? kDgluTileN / 2 : kDgluTileN, kEpiWarps, kStgBytes,
+                                            num_acc(kDgluTileN), 6);
   static_assert(kStages >= 3, "operand ring too shallow");
 };
 
@@ -224,23 +225,25 @@ struct DgluPolicy {
 
   // dGLU math on 32 columns of one row.  On entry gv / iv hold the C values of the gate and the
   // input block, on exit dgate / dinput; returns this row's partial of sum_j R * act.
-  __device__ __forceinline__ float dglu_math(const uint32_t (&r)[32], float (&gv)[32], float (&iv)[32], float alpha2,
-                                             float beta_g, float pr) const {
-    const int act_kind = p.act;
+  // One activation over a 32-column chunk; the activation is fixed per launch, so the branch is
+  // taken once per chunk and only that activation's unrolled loop runs.
+  template <int ACT, int NV>
+  __device__ __forceinline__ float dglu_math_act(const uint32_t* r, float* gv, float* iv, float alpha2, float beta_g,
+                                                 float pr) const {
     float dprob_acc = 0.f;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
+    for (int k = 0; k < NV; ++k) {
       const float R = __fmul_rn(alpha2, __uint_as_float(r[k]));
       const float x_g = __fmul_rn(beta_g, gv[k]);  // one fp32 product, never contracted
       const float x_i = __fmul_rn(beta_g, iv[k]);
       const float Rp = R * pr;
       float dg, di, act;
-      if (act_kind == MGG_ACT_DSWIGLU) {
+      if constexpr (ACT == MGG_ACT_DSWIGLU) {
         const float s = fast_sigmoid(x_g);
         di = Rp * (x_g * s);
         dg = Rp * x_i * s * (1.0f + x_g * (1.0f - s));
         act = x_g * s * x_i;
-      } else if (act_kind == MGG_ACT_DSITUGLU) {
+      } else if constexpr (ACT == MGG_ACT_DSITUGLU) {
         const float s = fast_sigmoid(x_g);
         const float tg = fast_tanh(x_g * p.situ_inv_b1);
         const float tu = fast_tanh(x_i * p.situ_inv_b2);
@@ -271,6 +274,15 @@ struct DgluPolicy {
     return dprob_acc;
   }
 
+  // NV values per call: r points at the NV accumulator words, gv / iv at NV gate / input values.
+  template <int NV>
+  __device__ __forceinline__ float dglu_math(const uint32_t* r, float* gv, float* iv, float alpha2, float beta_g,
+                                             float pr) const {
+    if (p.act == MGG_ACT_DSWIGLU) return dglu_math_act<MGG_ACT_DSWIGLU, NV>(r, gv, iv, alpha2, beta_g, pr);
+    if (p.act == MGG_ACT_DSITUGLU) return dglu_math_act<MGG_ACT_DSITUGLU, NV>(r, gv, iv, alpha2, beta_g, pr);
+    return dglu_math_act<MGG_ACT_DGEGLU, NV>(r, gv, iv, alpha2, beta_g, pr);
+  }
+
   __device__ __forceinline__ void dbias_partials(const TileWork& w, int j0, int lane, float (&gv)[32],
                                                  float (&iv)[32]) const {
     const int first = 2 * j0, second = 2 * j0 + 32;
@@ -279,8 +291,20 @@ struct DgluPolicy {
     float* ws = p.dbias_ws + (size_t)w.expert * 2 * (size_t)p.N;
     const float sg = warp_column_sums(gv, lane);
     const float si = warp_column_sums(iv, lane);
-    atomicAdd(ws + gcol + lane, sg);
-    atomicAdd(ws + icol + lane, si);
+    // lanes 4i gather columns 4i..4i+3 and add them with one 16-byte reduction (4x fewer atomics
+    // on addresses that every CTA of the same expert and column panel updates)
+    float g4[4], i4[4];
+    g4[0] = sg;
+    i4[0] = si;
+#pragma unroll
+    for (int d = 1; d < 4; ++d) {
+      g4[d] = __shfl_down_sync(0xffffffffu, sg, d);
+      i4[d] = __shfl_down_sync(0xffffffffu, si, d);
+    }
+    if ((lane & 3) == 0) {
+      red_add_v4(ws + gcol + lane, g4);
+      red_add_v4(ws + icol + lane, i4);
+    }
   }
 
   // One entry per CTA tile of 128 rows (a pair's tile logs two).
@@ -307,8 +331,9 @@ struct DgluPolicy {
   // ---------------------------------------------------------------- TMA path for 16-bit C
   // Ring of kCRing 4 KB boxes per warp: box u % kCRing holds rows [row0, row0+32) x C columns
   // [2*j0, 2*j0+64) (the gate and the input block of compact chunk j0).  Use u's box is loaded
-  // two uses ahead; with 16-bit D the results overwrite it in place and leave by a bulk store, so
-  // the box may be reloaded only once that store has read it.
+  // two uses ahead; the results overwrite it (16-bit D, or the gate half of fp32 D) and leave by
+  // a bulk store (one bulk group per use), so the box may be reloaded only once that store has
+  // read it.
   __device__ __forceinline__ void c_issue(const EpiCtx& ctx, uint32_t use, int j0, int row0) const {
     const uint32_t b = use % kCRing;
     mbar_arrive_expect_tx(&ctx.bars[b], 4096);
@@ -336,15 +361,16 @@ struct DgluPolicy {
 
   __device__ void prologue(const TileWork& w, long long, const EpiCtx& ctx) const {
     if constexpr (Cfg::kTmaC) {
+      if (*ctx.wg.abort_flag) return;  // the CTA is stopping: start no copies that nobody would wait for
       const int nown = own_chunks(num_chunks(w), ctx.half);
       const int row0 = w.m0 + ctx.rank * BM + 32 * ctx.q;
       fence_async_shared();  // earlier generic reads of the ring before the async overwrite
       __syncwarp();
       if (ctx.lane == 0 && nown > 0) {
-        if constexpr (DS == 2) bulk_wait_read<2>();  // the box of use c_uses was stored 3 uses ago
+        bulk_wait_read<2>();  // the box of use c_uses was stored out of 3 uses ago
         c_issue(ctx, c_uses, w.n0 + 32 * ctx.half, row0);
         if (nown > 1) {
-          if constexpr (DS == 2) bulk_wait_read<1>();
+          bulk_wait_read<1>();
           c_issue(ctx, c_uses + 1, w.n0 + 32 * (ctx.half + kEpiHalves), row0);
         }
       }
@@ -364,7 +390,7 @@ struct DgluPolicy {
     const float pr = __ldg(p.prob + row);
     const int nown = own_chunks(num_chunks(w), half);
     const uint32_t ring = smem_u32(ctx.stg);
-    const uint32_t dstg = ring + kCRing * 4096;  // fp32 D staging
+    const uint32_t dstg = ring + kCRing * 4096;  // the input half of fp32 D
     const int gblk = p.gate_first ? 0 : 1;
     float dprob_acc = 0.f;
     bool released = false;
@@ -380,34 +406,41 @@ struct DgluPolicy {
         rel(lane);
         released = true;
       }
-      if (!warp_wait(&ctx.bars[u % kCRing], (u / kCRing) & 1u, ctx.wg, 7)) break;
+      if (!warp_wait(&ctx.bars[u % kCRing], (u / kCRing) & 1u, ctx.wg, 7)) {
+        // stopping: let this warp's C copies still in flight (uses u and u + 1) land first
+        if (lane == 0)
+          for (uint32_t v = u; v < c_uses + (uint32_t)nown && v < u + 2; ++v)
+            mbar_wait_drain(&ctx.bars[v % kCRing], (v / kCRing) & 1u);
+        __syncwarp();
+        break;
+      }
       float gv[32], iv[32];
       read_c_block(box, lane, gblk, gv);
       read_c_block(box, lane, 1 - gblk, iv);
-      dprob_acc += dglu_math(r, gv, iv, alpha2, beta_g, pr);
+      dprob_acc += dglu_math<32>(r, gv, iv, alpha2, beta_g, pr);
       if constexpr (DS == 2) {  // D_row written back over this lane's own row of the C box
         stage_block(box, lane, gblk, gv);
         stage_block(box, lane, 1 - gblk, iv);
         staging_flush(box, lane, 2 * j0, row0);
-      } else {
+      } else {  // fp32: the gate block over the consumed C box, the input block in the extra box
         const int first = 2 * j0, second = 2 * j0 + 32;
-        staging_free(lane);
-        stage_block(dstg, lane, 0, gv);
-        stage_block(dstg + 4096, lane, 0, iv);
+        if (lane == 0) bulk_wait_read<0>();  // the extra box's previous store has read it
+        __syncwarp();
+        stage_block(box, lane, 0, gv);
+        stage_block(dstg, lane, 0, iv);
         fence_async_shared();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&p.tmap_d, dstg, p.gate_first ? first : second, row0);
-          tma_store_2d(&p.tmap_d, dstg + 4096, p.gate_first ? second : first, row0);
+          tma_store_2d(&p.tmap_d, box, p.gate_first ? first : second, row0);
+          tma_store_2d(&p.tmap_d, dstg, p.gate_first ? second : first, row0);
           bulk_commit_group();
         }
       }
       if (p.dbias_ws != nullptr) dbias_partials(w, j0, lane, gv, iv);
       if (i + 2 < nown) {  // refill the box of use u - 1 with this warp's chunk i + 2
-        if constexpr (DS == 4) fence_async_shared();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (DS == 2) bulk_wait_read<1>();
+          bulk_wait_read<1>();  // the store out of that box (one group ago) has read it
           c_issue(ctx, u + 2, j0 + 64 * kEpiHalves, row0);
         }
       }
@@ -451,7 +484,7 @@ struct DgluPolicy {
       float gv[32], iv[32];
       unpack_c(cg, gv);
       unpack_c(ci, iv);
-      dprob_acc += dglu_math(r, gv, iv, alpha2, beta_g, pr);
+      dprob_acc += dglu_math<32>(r, gv, iv, alpha2, beta_g, pr);
       if constexpr (DS == 2) {  // both 32-column blocks in one 64-column box
         staging_free(lane);
         stage_block(stg, lane, p.gate_first ? 0 : 1, gv);
@@ -499,7 +532,7 @@ __global__ void __launch_bounds__(cta_threads(DgluCfg<CS, DS, TMAC, PAIR>::kEpiW
 template <int BN, int CS, int DS, bool TMAC, bool PAIR>
 static cudaError_t launch_dglu_variant(const DgluParams& prm, int num_sms, cudaStream_t stream) {
   using C = DgluCfg<CS, DS, TMAC, PAIR>;
-  constexpr int smem = SmemLayout<PAIR ? BN / 2 : BN, C::kStages, C::kEpiWarps, C::kStgBytes>::DYN_BYTES;
+  constexpr int smem = SmemLayout<PAIR ? BN / 2 : BN, C::kStages, C::kEpiWarps, C::kStgBytes, num_acc(BN)>::DYN_BYTES;
   auto kern = dglu_bwd_kernel<BN, CS, DS, TMAC, PAIR>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;

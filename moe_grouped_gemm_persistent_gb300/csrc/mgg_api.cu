@@ -193,13 +193,20 @@ mgg_status validate_wgrad(const mgg_wgrad_args& a) {
 // AUTO picks CTA pairs where they measured faster on GB300: for the dgrad whenever a single CTA
 // would read C through registers (fp32 C, or K >= 4096 where the single CTA's C ring would cost an
 // operand stage), since a pair's halved B slot leaves room for the C ring, eight epilogue warps
-// and four stages (Mixtral-shaped K = 4096: +12%; K = 2048 dGeGLU: -3%, so those stay single).
+// and four stages (K = 7168: +4%; K = 4096: even; K = 2048 dGeGLU: even, so that one stays single).
 bool dglu_pair(const mgg_dglu_bwd_args& a) {
   if (a.cta_mode != MGG_CTA_AUTO) return a.cta_mode == MGG_CTA_PAIR;
   return a.c_dtype == MGG_FP32 || a.K > kTmaCMaxK;
 }
 
-bool wgrad_pair(const mgg_wgrad_args& a) { return a.cta_mode == MGG_CTA_PAIR && a.hidden % 256 == 0; }
+// For the wgrad AUTO takes pairs when the experts average at least 1024 tokens (dense accumulate
+// Zipf-shaped layer, ~1000 tokens per expert: +6%); with short reductions (~512 tokens per
+// expert) the pair's coupled epilogues cost more than the halved B traffic saves (-9%).
+bool wgrad_pair(const mgg_wgrad_args& a) {
+  if (a.hidden % 256 != 0) return false;
+  if (a.cta_mode != MGG_CTA_AUTO) return a.cta_mode == MGG_CTA_PAIR;
+  return a.tokens_sum >= 1024 * a.L;
+}
 
 mgg_status from_cuda(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return MGG_OK;

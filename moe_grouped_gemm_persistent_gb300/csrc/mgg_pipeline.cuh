@@ -3,8 +3,8 @@
 //   warp 0      TMA producer: one elected thread streams BK-wide slices of the A and B tiles
 //               into a STAGES-deep shared-memory ring (full/empty mbarriers).
 //   warp 1      TMEM allocator and MMA issuer: one thread issues tcgen05.mma (bf16 in, fp32
-//               accumulate) into one of two TMEM accumulators and commits the ring slots and the
-//               finished accumulator to mbarriers.
+//               accumulate) into one of the TMEM accumulators (512 / BN of them, at most 4) and
+//               commits the ring slots and the finished accumulator to mbarriers.
 //   warps 2..   epilogue: each warp owns one 32-lane TMEM sub-partition (rows 32*(warp%4) ..
 //               +31 of its CTA's rows), reads the accumulator with tcgen05.ld and hands it to the
 //               operation's epilogue while the MMA already accumulates the next tile.
@@ -74,16 +74,36 @@ struct TileWork {
   int num_kb;   // number of BK slices; 0 = no MMA (the epilogue writes without TMEM)
 };
 
+// TMEM accumulators of BN fp32 columns in the 512 columns of an SM (at most 4 in flight).
+__host__ __device__ constexpr int num_acc(int bn) { return 512 / bn < 4 ? 512 / bn : 4; }
+
 // BN_LOAD: B rows (N) this CTA loads per slot (BN, or BN/2 in a pair).
 // STG: bytes of output staging per epilogue warp (a multiple of 4 KB: 32 rows x 128 bytes per box).
-template <int BN_LOAD, int STAGES, int EPI_WARPS, int STG>
+// NACC: TMEM accumulators (num_acc(BN)).
+constexpr int kMaxSmemBytes = 232448;  // dynamic shared memory per block (227 KB)
+
+// Dynamic shared memory of one CTA (the same arithmetic as SmemLayout below).
+__host__ __device__ constexpr int smem_bytes(int bn_load, int stages, int epi_warps, int stg, int nacc) {
+  return ((stages * (BM + bn_load) * BK * 2 + epi_warps * stg +
+           (2 * stages + 2 * nacc + 1 + 2 * kSchedRing + 4 * epi_warps) * 8 + 15) / 16 * 16) +
+         kSchedRing * kSchedEntry + (1 + epi_warps) * kAcqWords * 4 + 16 + 1024;
+}
+
+// Deepest operand ring (at most `cap` slots) that fits next to the epilogue's shared memory.
+__host__ __device__ constexpr int max_stages(int bn_load, int epi_warps, int stg, int nacc, int cap) {
+  int s = cap;
+  while (s > 1 && smem_bytes(bn_load, s, epi_warps, stg, nacc) > kMaxSmemBytes) --s;
+  return s;
+}
+
+template <int BN_LOAD, int STAGES, int EPI_WARPS, int STG, int NACC>
 struct SmemLayout {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN_LOAD * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * STG;
-  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * kSchedRing + 4 * EPI_WARPS;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1 + 2 * kSchedRing + 4 * EPI_WARPS;
   static constexpr int SCHED_OFF = (BAR_OFF + NUM_BARS * 8 + 15) / 16 * 16;
   static constexpr int ACQ_OFF = SCHED_OFF + kSchedRing * kSchedEntry;  // producer, then each epilogue warp
   static constexpr int MISC_OFF = ACQ_OFF + (1 + EPI_WARPS) * kAcqWords * 4;
@@ -91,7 +111,8 @@ struct SmemLayout {
   static constexpr int DYN_BYTES = BYTES + 1024;  // slack to align the ring to 1024 B
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "ring slots must stay 1024-byte aligned");
   static_assert(SCHED_OFF % 16 == 0, "16-byte aligned published tiles");
-  static_assert(DYN_BYTES <= 232448, "shared memory per block");
+  static_assert(DYN_BYTES == smem_bytes(BN_LOAD, STAGES, EPI_WARPS, STG, NACC), "layout arithmetic");
+  static_assert(DYN_BYTES <= kMaxSmemBytes, "shared memory per block");
 };
 
 // What one epilogue warp owns.
@@ -146,8 +167,9 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   constexpr int kEpiWarps = P::EPI_WARPS;
   static_assert(kEpiWarps % 4 == 0, "whole TMEM sub-partitions");
   constexpr int kBLoad = PAIR ? BN / 2 : BN;
-  using S = SmemLayout<kBLoad, STAGES, kEpiWarps, P::STG_BYTES>;
-  constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
+  constexpr int NACC = num_acc(BN);
+  using S = SmemLayout<kBLoad, STAGES, kEpiWarps, P::STG_BYTES, NACC>;
+  constexpr uint32_t TMEM_COLS = tmem_cols_for(NACC * BN);
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N");
   static_assert(!PAIR || BN % 128 == 0, "a pair splits B in 64-column multiples");
 
@@ -156,8 +178,8 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* tfull_bar = empty_bar + STAGES;
-  uint64_t* tempty_bar = tfull_bar + 2;
-  uint64_t* done_bar = tempty_bar + 2;
+  uint64_t* tempty_bar = tfull_bar + NACC;
+  uint64_t* done_bar = tempty_bar + NACC;
   uint64_t* sfull_bar = done_bar + 1;             // [kSchedRing] a tile was published
   uint64_t* sempty_bar = sfull_bar + kSchedRing;  // [kSchedRing] every consumer has read it
   uint64_t* epi_bars = sempty_bar + kSchedRing;   // [4 * kEpiWarps] owned by the epilogue warps
@@ -187,7 +209,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NACC; ++a) {
       mbar_init(&tfull_bar[a], 1);
       mbar_init(&tempty_bar[a], (PAIR ? 2 : 1) * kEpiWarps);  // one arrival per epilogue warp
     }
@@ -339,7 +361,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       for (long long t = consume_tile(n_tile++, false, w); t < p.total_tiles && ok;
            t = consume_tile(n_tile++, false, w)) {
         if (!w.active || w.num_kb == 0) continue;
-        const uint32_t acc = local & 1u, use = local >> 1;
+        const uint32_t acc = local % NACC, use = local / NACC;
         if (!mbar_wait(&tempty_bar[acc], (use & 1u) ^ 1u, wg, 2)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -394,7 +416,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
         p.epilogue(w, t, 0u, false, ctx, AccRelease{0u, false});
         continue;
       }
-      const uint32_t acc = local & 1u, use = local >> 1;
+      const uint32_t acc = local % NACC, use = local / NACC;
       if (!warp_wait(&tfull_bar[acc], use & 1u, wg, 4)) break;
       tc_fence_after();
       const uint32_t ebar = PAIR ? mapa_shared(smem_u32(&tempty_bar[acc]), 0) : smem_u32(&tempty_bar[acc]);

@@ -166,6 +166,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// Relaxed device-scope fp32 add of 4 consecutive floats (16-byte aligned) at global memory.
+__device__ __forceinline__ void red_add_v4(float* addr, const float (&v)[4]) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3])
+               : "memory");
+}
+
 // Approximate reciprocal (one MUFU operation); rcp(+inf) = 0.
 __device__ __forceinline__ float rcp_approx(float x) {
   float y;

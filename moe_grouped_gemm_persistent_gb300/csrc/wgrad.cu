@@ -305,15 +305,13 @@ int wgrad_tile_n(int64_t inter) { return inter > 128 ? 256 : 128; }
 // (BN = 256) or 32 KB (BN = 128) per stage, a CTA of a pair half of the B part of that).
 template <int BN, bool PAIR>
 constexpr int wgrad_stages() {
-  constexpr int slot = (BM + (PAIR ? BN / 2 : BN)) * BK * 2;
-  constexpr int fit = (232448 - 2048 - kWgradEpiWarps * kWgradStgBytes) / slot;
-  return fit < 6 ? fit : 6;
+  return max_stages(PAIR ? BN / 2 : BN, kWgradEpiWarps, kWgradStgBytes, num_acc(BN), 6);
 }
 
 template <int BN, int OS, bool PAIR>
 static cudaError_t launch_wgrad_bn(const WgradLaunch& Lc, WgradParams& prm, cudaStream_t stream) {
   constexpr int STAGES = wgrad_stages<BN, PAIR>();
-  using S = SmemLayout<PAIR ? BN / 2 : BN, STAGES, kWgradEpiWarps, kWgradStgBytes>;
+  using S = SmemLayout<PAIR ? BN / 2 : BN, STAGES, kWgradEpiWarps, kWgradStgBytes, num_acc(BN)>;
   auto kern = wgrad_kernel<BN, STAGES, OS, PAIR>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);
   if (err != cudaSuccess) return err;
