@@ -406,6 +406,14 @@ def oracle_sample(prob_or_specs, dev, budget_s: float, seed: int = 0, max_expert
 
 
 # ----------------------------------------------------------------------------------------
+def max_over_ranks(value: float, dev) -> float:
+    """The largest of every rank's value (the slowest rank's time decides a step)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -446,9 +454,7 @@ def main():
     prob = Problem(args.workload, dev, args.sched, args.cta)
     total_ms, per, clocks = time_steps(prob, args.steps, args.warmup, world)
     if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
     ms_step = total_ms / args.steps
     flops = prob.flops()
     step_flops = sum(flops.values())
@@ -474,9 +480,7 @@ def main():
     if not args.no_e2e:
         ms_e2e, bi, bo = time_e2e(prob, args.e2e_steps, 1)
         if world > 1:
-            t = torch.tensor([ms_e2e], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms_e2e = float(t.item())
+            ms_e2e = max_over_ranks(ms_e2e, dev)
         e2e = {"value": round(step_flops * world / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "ms_per_step": round(ms_e2e, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "steps": args.e2e_steps}
