@@ -17,24 +17,25 @@
 namespace mgg {
 
 // Per-variant configuration (CS / DS = element bytes of C / D_row; PAIR = CTA-pair tiles).
-//  TMA-C (16-bit C): C reaches shared memory by TMA (a 3-deep ring of 32 x 64 boxes per epilogue
-//            warp, loaded ahead of the math); the results go back out of the consumed box (16-bit
-//            D, or the gate half of fp32 D, whose input half takes one more 4 KB box).
-//  register-C: C is read per row into registers one chunk ahead; 8 epilogue warps (two per TMEM
-//            sub-partition) hide the load latency.
-//  The ring stages take whatever shared memory the epilogue leaves (at most 6).  A single CTA
-//  loads 48 KB per stage, a CTA of a pair 32 KB (half of B), so pairs afford the TMA-C ring with
-//  eight warps for 16-bit D (fp32 D keeps four warps and five stages: eight measured slower with
-//  the three stages left); a single CTA only affords it with four warps and three stages, which
-//  pays when the epilogue dominates (K <= kTmaCMaxK).
+//  TMA-C (16-bit C): C reaches shared memory by TMA (a 2-box ring of 32 x 64 boxes per epilogue
+//            warp, each loaded a chunk ahead of its math); the results go back out of the
+//            consumed box (16-bit D in one store; fp32 D as the gate half, then the input half).
+//  register-C: C is read per row into registers one chunk ahead.
+//  Both use 8 epilogue warps (two per TMEM sub-partition), so each scheduler interleaves two
+//  warps' math.  The ring stages take whatever shared memory the epilogue leaves (at most 6): a
+//  single CTA loads 48 KB per stage (3 stages next to the TMA-C ring), a CTA of a pair 32 KB
+//  (5 stages); a single CTA takes the TMA-C path when K <= kTmaCMaxK.
 
 template <int CS, int DS, bool TMAC, bool PAIR>
 struct DgluCfg {
   static constexpr bool kTmaC = TMAC && CS == 2;
-  static constexpr int kEpiWarps = kTmaC ? ((PAIR && DS == 2) ? 8 : 4) : 8;
-  static constexpr int kCRing = 3;  // C boxes in flight per warp (TMA path)
-  // TMA path: C ring + the input half of fp32 D; register path: D staging
-  static constexpr int kStgBytes = kTmaC ? (kCRing * 4096 + (DS == 4 ? 4096 : 0)) : (DS == 4 ? 8192 : 4096);
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kCRing = 2;  // C boxes per warp (TMA path)
+  // bulk groups one chunk commits on the TMA path: 16-bit D leaves in one store, fp32 D in two
+  // (the gate half, then the input half, through the same box)
+  static constexpr int kGroups = DS == 4 ? 2 : 1;
+  // TMA path: the C ring (results leave through the consumed box); register path: D staging
+  static constexpr int kStgBytes = kTmaC ? kCRing * 4096 : (DS == 4 ? 8192 : 4096);
   static constexpr int kStages = max_stages(PAIR ? kDgluTileN / 2 : kDgluTileN, kEpiWarps, kStgBytes,
                                             num_acc(kDgluTileN), 6);
   static_assert(kStages >= 3, "operand ring too shallow");
@@ -330,10 +331,9 @@ struct DgluPolicy {
 
   // ---------------------------------------------------------------- TMA path for 16-bit C
   // Ring of kCRing 4 KB boxes per warp: box u % kCRing holds rows [row0, row0+32) x C columns
-  // [2*j0, 2*j0+64) (the gate and the input block of compact chunk j0).  Use u's box is loaded
-  // two uses ahead; the results overwrite it (16-bit D, or the gate half of fp32 D) and leave by
-  // a bulk store (one bulk group per use), so the box may be reloaded only once that store has
-  // read it.
+  // [2*j0, 2*j0+64) (the gate and the input block of compact chunk j0).  Use u + 2 is loaded when
+  // use u is done; the results overwrite the consumed box and leave by bulk stores (kGroups bulk
+  // groups per use), so a box is reloaded only once those stores have read it.
   __device__ __forceinline__ void c_issue(const EpiCtx& ctx, uint32_t use, int j0, int row0) const {
     const uint32_t b = use % kCRing;
     mbar_arrive_expect_tx(&ctx.bars[b], 4096);
@@ -367,10 +367,11 @@ struct DgluPolicy {
       fence_async_shared();  // earlier generic reads of the ring before the async overwrite
       __syncwarp();
       if (ctx.lane == 0 && nown > 0) {
-        bulk_wait_read<2>();  // the box of use c_uses was stored out of 3 uses ago
+        // the box of use c_uses was last stored out of kCRing uses ago (kGroups groups per use)
+        bulk_wait_read<(kCRing - 1) * Cfg::kGroups>();
         c_issue(ctx, c_uses, w.n0 + 32 * ctx.half, row0);
         if (nown > 1) {
-          bulk_wait_read<1>();
+          bulk_wait_read<(kCRing - 2) * Cfg::kGroups>();
           c_issue(ctx, c_uses + 1, w.n0 + 32 * (ctx.half + kEpiHalves), row0);
         }
       }
@@ -390,7 +391,6 @@ struct DgluPolicy {
     const float pr = __ldg(p.prob + row);
     const int nown = own_chunks(num_chunks(w), half);
     const uint32_t ring = smem_u32(ctx.stg);
-    const uint32_t dstg = ring + kCRing * 4096;  // the input half of fp32 D
     const int gblk = p.gate_first ? 0 : 1;
     float dprob_acc = 0.f;
     bool released = false;
@@ -422,25 +422,20 @@ struct DgluPolicy {
         stage_block(box, lane, gblk, gv);
         stage_block(box, lane, 1 - gblk, iv);
         staging_flush(box, lane, 2 * j0, row0);
-      } else {  // fp32: the gate block over the consumed C box, the input block in the extra box
+      } else {  // fp32: the gate half, then the input half, each a 32 x 32 box through the C box
         const int first = 2 * j0, second = 2 * j0 + 32;
-        if (lane == 0) bulk_wait_read<0>();  // the extra box's previous store has read it
-        __syncwarp();
         stage_block(box, lane, 0, gv);
-        stage_block(dstg, lane, 0, iv);
-        fence_async_shared();
+        staging_flush(box, lane, p.gate_first ? first : second, row0);
+        if (lane == 0) bulk_wait_read<0>();  // the gate half has left the box
         __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&p.tmap_d, box, p.gate_first ? first : second, row0);
-          tma_store_2d(&p.tmap_d, dstg, p.gate_first ? second : first, row0);
-          bulk_commit_group();
-        }
+        stage_block(box, lane, 0, iv);
+        staging_flush(box, lane, p.gate_first ? second : first, row0);
       }
       if (p.dbias_ws != nullptr) dbias_partials(w, j0, lane, gv, iv);
-      if (i + 2 < nown) {  // refill the box of use u - 1 with this warp's chunk i + 2
+      if (i + 2 < nown) {  // refill with this warp's use u + 2 the box last used kCRing - 2 uses ago
         __syncwarp();
         if (lane == 0) {
-          bulk_wait_read<1>();  // the store out of that box (one group ago) has read it
+          bulk_wait_read<(kCRing - 2) * Cfg::kGroups>();  // the stores out of that box have read it
           c_issue(ctx, u + 2, j0 + 64 * kEpiHalves, row0);
         }
       }

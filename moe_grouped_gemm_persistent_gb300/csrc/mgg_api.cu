@@ -190,14 +190,11 @@ mgg_status validate_wgrad(const mgg_wgrad_args& a) {
   return MGG_OK;
 }
 
-// AUTO picks CTA pairs where they measured faster on GB300: for the dgrad whenever a single CTA
-// would read C through registers (fp32 C, or K >= 4096 where the single CTA's C ring would cost an
-// operand stage), since a pair's halved B slot leaves room for the C ring, eight epilogue warps
-// and four stages (K = 7168: +4%; K = 4096: even; K = 2048 dGeGLU: even, so that one stays single).
-bool dglu_pair(const mgg_dglu_bwd_args& a) {
-  if (a.cta_mode != MGG_CTA_AUTO) return a.cta_mode == MGG_CTA_PAIR;
-  return a.c_dtype == MGG_FP32 || a.K > kTmaCMaxK;
-}
+// AUTO picks CTA pairs where they measured faster on GB300.  For the dgrad that is every shape
+// (M is a multiple of 256): a pair's halved B slot leaves room for eight epilogue warps with the
+// C ring and five operand stages (Mixtral-shaped: 1552 vs 1397 TFLOP/s single; DeepSeek-shaped
+// K = 7168: 1486 vs 1300; dGeGLU with fp32 D: 975 vs 845).
+bool dglu_pair(const mgg_dglu_bwd_args& a) { return a.cta_mode != MGG_CTA_SINGLE; }
 
 // For the wgrad AUTO takes pairs when the experts average at least 1024 tokens (dense accumulate
 // Zipf-shaped layer, ~1000 tokens per expert: +6%); with short reductions (~512 tokens per
