@@ -62,6 +62,7 @@ struct DgluParams {
   int M, K, N, L;
   int num_n, num_kb;
   int a_mn, b_mn;
+  int b_blocked;                // discrete N-major B maps are 3-D (64-column blocks, one box per slot)
   int c_dtype, d_dtype, act, indicator, gate_first;
   float situ_b1, situ_b2, situ_inv_b1, situ_inv_b2;  // dSiTU-GLU scales and their reciprocals
 };
@@ -141,6 +142,9 @@ struct DgluPolicy {
       if (kb == 0 && acq.first_use(w.expert)) tmap_acquire(m);
       if (!p.b_mn) {
         load2(sb, m, bar, kb * BK, ncol);
+      } else if (p.b_blocked) {
+        if constexpr (PAIR) tma_load_3d_pair(sb, m, bar, 0, kb * BK, ncol / 64);
+        else tma_load_3d(sb, m, bar, 0, kb * BK, ncol / 64);
       } else {
 #pragma unroll
         for (int j = 0; j < kBLoad / 64; ++j) load2(sb + j * 8192, m, bar, ncol + 64 * j, kb * BK);
@@ -626,6 +630,7 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     prm.num_kb = (int)((a.K + BK - 1) / BK);
     prm.a_mn = 0;
     prm.b_mn = (a.b_ptrs != nullptr && a.b_major == MGG_MAJOR_MN) ? 1 : 0;
+    prm.b_blocked = Lc.b_blocked ? 1 : 0;
     prm.c_dtype = a.c_dtype;
     prm.d_dtype = a.d_dtype;
     prm.act = a.act;

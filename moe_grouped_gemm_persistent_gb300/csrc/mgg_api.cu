@@ -304,9 +304,20 @@ mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream) {
     const uint32_t box[2] = {64, b_rows};
     if ((s = encode_bf16(&Lc.tmap_b, a.a, 2, dims, strides, box, "discrete K-major B")) != MGG_OK) return s;
   } else {
-    const uint64_t dims[2] = {N, K}, strides[1] = {N * 2};
-    const uint32_t box[2] = {64, 64};
-    if ((s = encode_bf16(&Lc.tmap_b, a.a, 2, dims, strides, box, "discrete N-major B")) != MGG_OK) return s;
+    // N a multiple of 64: a 3-D template of 64-column blocks (dims {64, K, N/64}, strides
+    // {N*2, 128} bytes) so one box fills a ring slot; else one 64 x 64 box per 64 columns
+    if (N % 64 == 0) {
+      const uint64_t dims[3] = {64, K, N / 64}, strides[2] = {N * 2, 128};
+      const uint32_t box[3] = {64, 64, b_rows / 64};
+      const std::string saved = g_err;
+      Lc.b_blocked = encode_bf16(&Lc.tmap_b, a.a, 3, dims, strides, box, "discrete N-major B (blocked)") == MGG_OK;
+      if (!Lc.b_blocked) g_err = saved;
+    }
+    if (!Lc.b_blocked) {
+      const uint64_t dims[2] = {N, K}, strides[1] = {N * 2};
+      const uint32_t box[2] = {64, 64};
+      if ((s = encode_bf16(&Lc.tmap_b, a.a, 2, dims, strides, box, "discrete N-major B")) != MGG_OK) return s;
+    }
   }
   {  // D_row (M, 2N): 32-row boxes of one 128-byte row of columns
     const uint64_t esz = a.d_dtype == MGG_FP32 ? 4 : 2;
@@ -341,22 +352,39 @@ mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {
   Lc.a_ragged = ragged && a.a_major == MGG_MAJOR_K;
   Lc.b_ragged = ragged && a.b_major == MGG_MAJOR_K;
   const uint64_t T = (uint64_t)(a.tokens_sum > 0 ? a.tokens_sum : 256), H = (uint64_t)a.hidden, I = (uint64_t)a.inter;
+  // An MN-major operand whose MN extent is a multiple of 64 is also a 3-D tensor of 64-wide
+  // blocks: dims {64, T, extent/64}, strides {extent*2, 128} bytes.  One box of that map fills a
+  // whole ring slot (its 64 x 64 blocks land 8 KB apart, as the MMA descriptors expect), so the
+  // producer issues one TMA copy per operand and slot instead of one per 64 columns.
+  auto blocked = [&](CUtensorMap* map, const void* base, uint64_t extent, uint32_t blocks, const char* what) {
+    if (extent % 64 != 0) return false;
+    const uint64_t dims[3] = {64, T, extent / 64}, strides[2] = {extent * 2, 128};
+    const uint32_t box[3] = {64, 64, blocks};
+    const std::string saved = g_err;
+    if (encode_bf16(map, base, 3, dims, strides, box, what) == MGG_OK) return true;
+    g_err = saved;  // the driver refused the blocked view: the 2-D map is used instead
+    return false;
+  };
+  const uint32_t b_cols = (uint32_t)(Lc.pair ? Lc.tile_n / 2 : Lc.tile_n);  // B columns one CTA loads
   if (a.a_major == MGG_MAJOR_K) {  // (hidden, T), T contiguous
     const uint64_t dims[2] = {T, H}, strides[1] = {T * 2};
     const uint32_t box[2] = {64, 128};
     if ((s = encode_bf16(&Lc.tmap_a, a.a, 2, dims, strides, box, "A (K-major)")) != MGG_OK) return s;
-  } else {  // (hidden, T) with hidden contiguous: rows of T
+  } else if (!(Lc.a_blocked = blocked(&Lc.tmap_a, a.a, H, 2, "A (M-major, blocked)"))) {
+    // (hidden, T) with hidden contiguous: rows of T
     const uint64_t dims[2] = {H, T}, strides[1] = {H * 2};
     const uint32_t box[2] = {64, 64};
     if ((s = encode_bf16(&Lc.tmap_a, a.a, 2, dims, strides, box, "A (M-major)")) != MGG_OK) return s;
   }
   if (a.b_major == MGG_MAJOR_MN) {  // (T, inter), inter contiguous
-    const uint64_t dims[2] = {I, T}, strides[1] = {I * 2};
-    const uint32_t box[2] = {64, 64};
-    if ((s = encode_bf16(&Lc.tmap_b, a.b, 2, dims, strides, box, "B (N-major)")) != MGG_OK) return s;
+    if (!(Lc.b_blocked = blocked(&Lc.tmap_b, a.b, I, b_cols / 64, "B (N-major, blocked)"))) {
+      const uint64_t dims[2] = {I, T}, strides[1] = {I * 2};
+      const uint32_t box[2] = {64, 64};
+      if ((s = encode_bf16(&Lc.tmap_b, a.b, 2, dims, strides, box, "B (N-major)")) != MGG_OK) return s;
+    }
   } else {  // (T, inter) with T contiguous: rows of T
     const uint64_t dims[2] = {T, I}, strides[1] = {T * 2};
-    const uint32_t box[2] = {64, (uint32_t)(Lc.pair ? Lc.tile_n / 2 : Lc.tile_n)};  // B rows one CTA loads
+    const uint32_t box[2] = {64, b_cols};
     if ((s = encode_bf16(&Lc.tmap_b, a.b, 2, dims, strides, box, "B (K-major)")) != MGG_OK) return s;
   }
   {  // outputs: 32-row boxes of one 128-byte row of columns

@@ -25,7 +25,8 @@ struct DgluLaunch {
   const mgg_dglu_bwd_args* args;
   int num_sms;
   int tile_n;
-  bool pair;  // 256-row tiles on CTA pairs (B maps load half a tile's columns)
+  bool pair;       // 256-row tiles on CTA pairs (B maps load half a tile's columns)
+  bool b_blocked;  // discrete N-major B as a 3-D map of 64-column blocks (one box per slot)
 };
 
 struct WgradLaunch {
@@ -38,6 +39,8 @@ struct WgradLaunch {
   bool a_ragged;  // per-expert A maps built on the device
   bool b_ragged;
   bool pair;      // 256-row tiles on CTA pairs (B maps load half a tile's columns)
+  bool a_blocked; // M-major A as a 3-D map of 64-row blocks (one box per slot), else 2-D
+  bool b_blocked; // N-major B likewise
 };
 
 // Launchers (queue the prep kernel, the persistent kernel and finalisers on `stream`).

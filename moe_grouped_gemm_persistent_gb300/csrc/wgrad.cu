@@ -36,6 +36,7 @@ struct WgradParams {
   int hidden, inter, L;
   int tiles_n, tiles_per_expert;
   int a_mn, b_mn, out_dtype, accumulate;
+  int a_blocked, b_blocked;     // MN-major operand as a 3-D map of 64-wide blocks (one box per slot)
 };
 
 constexpr int kWgradEpiWarps = 4;
@@ -89,6 +90,10 @@ struct WgradPolicy {
     if constexpr (PAIR) tma_load_2d_pair(dst, map, bar, x, y);
     else tma_load_2d(dst, map, bar, x, y);
   }
+  static __device__ __forceinline__ void load3(uint32_t dst, const void* map, uint32_t bar, int x, int y, int z) {
+    if constexpr (PAIR) tma_load_3d_pair(dst, map, bar, x, y, z);
+    else tma_load_3d(dst, map, bar, x, y, z);
+  }
 
   // This CTA's 128 rows of A (m0 + 128 * rank) and its kBLoad columns of B (n0 + kBLoad * rank).
   __device__ void issue_loads(const TileWork& w, int kb, uint32_t sa, uint32_t sb, uint32_t bar, int rank,
@@ -105,12 +110,16 @@ struct WgradPolicy {
       load2(sa, m, bar, kb * BK, mrow);
     } else if (!p.a_mn) {
       load2(sa, &p.tmap_a, bar, k, mrow);
+    } else if (p.a_blocked) {
+      load3(sa, &p.tmap_a, bar, 0, k, mrow / 64);
     } else {
       load2(sa, &p.tmap_a, bar, mrow, k);
       load2(sa + 8192, &p.tmap_a, bar, mrow + 64, k);
     }
     if (p.b_maps != nullptr) {
       load2(sb, p.b_maps + w.expert, bar, kb * BK, ncol);
+    } else if (p.b_mn && p.b_blocked) {
+      load3(sb, &p.tmap_b, bar, 0, k, ncol / 64);
     } else if (p.b_mn) {
 #pragma unroll
       for (int j = 0; j < kBLoad / 64; ++j) load2(sb + j * 8192, &p.tmap_b, bar, ncol + 64 * j, k);
@@ -367,6 +376,8 @@ cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {
   prm.tiles_per_expert = (int)(tiles_m * tiles_n);
   prm.a_mn = (a.a_major == MGG_MAJOR_MN) ? 1 : 0;
   prm.b_mn = (a.b_major == MGG_MAJOR_MN) ? 1 : 0;
+  prm.a_blocked = Lc.a_blocked ? 1 : 0;
+  prm.b_blocked = Lc.b_blocked ? 1 : 0;
   prm.out_dtype = a.out_dtype;
   prm.accumulate = a.accumulate != 0;
   const bool fp32 = a.out_dtype == MGG_FP32;

@@ -67,6 +67,9 @@ DGLU_CASES = {
     "swiglu_fp32c": dict(c_dtype="fp32"),
     "discrete_k": dict(b_mode="discrete", b_major="k"),
     "discrete_n_geglu": dict(b_mode="discrete", b_major="n", act="dgeglu", c_std=4.0, dbias=True),
+    # N % 64 == 0: N-major weights through one 3-D box of 64-column blocks per ring slot
+    "discrete_n_blocked_fp32d": dict(b_mode="discrete", b_major="n", N=192, K=256, act="dgeglu", c_std=4.0,
+                                     d_dtype="fp32", dbias=True),
     "wide_n": dict(N=544, K=192, counts=(512, 256)),
     # K >= 4096 selects the register path for 16-bit C
     "regpath_swiglu": dict(K=4096, N=96, counts=(256, 0, 256)),
@@ -174,6 +177,9 @@ WGRAD_CASES = {
     "ragged_k_n_discrete": dict(input_order="tensor_ragged", out_mode="discrete"),
     "ragged_k_k": dict(input_order="tensor_ragged", b_major="k"),
     "bn256": dict(inter=512, hidden=128, counts=(256, 768, 0)),
+    # MN extents that are multiples of 64: MN-major operands through blocked 3-D maps
+    "m_n_blocked": dict(a_major="m", hidden=256, inter=192),
+    "m_n_blocked_acc_bf16": dict(a_major="m", hidden=320, inter=448, accumulate=True, out_dtype="bf16"),
 }
 
 
