@@ -5,7 +5,8 @@
 //   warp 1      TMEM allocator and MMA issuer: one thread issues tcgen05.mma (bf16 in, fp32
 //               accumulate) into one of the TMEM accumulators (512 / BN of them, at most 4) and
 //               commits the ring slots and the finished accumulator to mbarriers.
-//   warps 2..   epilogue: each warp owns one 32-lane TMEM sub-partition (rows 32*(warp%4) ..
+//   warp 2      scheduler: one thread claims, decodes and publishes the tiles to every role.
+//   warps 3..   epilogue: each warp owns one 32-lane TMEM sub-partition (rows 32*(warp%4) ..
 //               +31 of its CTA's rows), reads the accumulator with tcgen05.ld and hands it to the
 //               operation's epilogue while the MMA already accumulates the next tile.
 //
@@ -20,7 +21,7 @@
 // The operation supplies a policy object P with
 //   total_tiles, status, a_mn, b_mn, dynamic        status[3] is the dynamic scheduler's tile
 //                                                   counter (zeroed by the preparation kernel)
-//   TileWork tile(long long t)                      called once per tile, by the producer thread
+//   TileWork tile(long long t)                      called once per tile, by the scheduler thread
 //   issue_loads(w, kb, sa, sb, bar, rank, acq)      producer thread; `bar` is the address the
 //                                                   loads complete on (the even CTA's in a pair);
 //                                                   `acq` records the maps it has acquired
@@ -42,7 +43,11 @@ namespace mgg {
 constexpr int BM = 128;        // accumulator rows per CTA (UMMA M per CTA)
 constexpr int BK = 64;         // K elements per ring slot: one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;     // K of one kind::f16 MMA
-constexpr int kSchedRing = 8;  // published tiles in flight from the producer to the other roles
+constexpr int kSchedRing = 8;  // published tiles in flight from the scheduler to the other roles
+// The scheduler claims tile n + 1 once the producer has kClaimLeadKb (or fewer) k-slices of tile n
+// left to issue: early enough to hide the claim's atomic and decode, late enough to keep the
+// dynamic schedule's load balance (a tile claimed long before it starts cannot move).
+constexpr int kClaimLeadKb = 6;
 constexpr int kSchedEntry = 32; // bytes of one published tile: index + TileWork
 constexpr int kMaxExperts = 1024;
 constexpr int kAcqWords = kMaxExperts / 32;  // one bit per expert
@@ -63,8 +68,10 @@ struct MapAcquired {
   }
 };
 
-// Threads of a CTA with `epi_warps` epilogue warps (a multiple of 4) after the producer and MMA warps.
-__host__ __device__ constexpr int cta_threads(int epi_warps) { return 64 + 32 * epi_warps; }
+// Threads of a CTA with `epi_warps` epilogue warps (a multiple of 4) after the producer, MMA and
+// scheduler warps.
+constexpr int kFirstEpiWarp = 3;
+__host__ __device__ constexpr int cta_threads(int epi_warps) { return 32 * (kFirstEpiWarp + epi_warps); }
 
 struct TileWork {
   int active;   // 0: the tile is skipped by every role
@@ -85,7 +92,7 @@ constexpr int kMaxSmemBytes = 232448;  // dynamic shared memory per block (227 K
 // Dynamic shared memory of one CTA (the same arithmetic as SmemLayout below).
 __host__ __device__ constexpr int smem_bytes(int bn_load, int stages, int epi_warps, int stg, int nacc) {
   return ((stages * (BM + bn_load) * BK * 2 + epi_warps * stg +
-           (2 * stages + 2 * nacc + 1 + 2 * kSchedRing + 4 * epi_warps) * 8 + 15) / 16 * 16) +
+           (2 * stages + 2 * nacc + 1 + 3 * kSchedRing + 4 * epi_warps) * 8 + 15) / 16 * 16) +
          kSchedRing * kSchedEntry + (1 + epi_warps) * kAcqWords * 4 + 16 + 1024;
 }
 
@@ -103,7 +110,7 @@ struct SmemLayout {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * STG;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1 + 2 * kSchedRing + 4 * EPI_WARPS;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1 + 3 * kSchedRing + 4 * EPI_WARPS;
   static constexpr int SCHED_OFF = (BAR_OFF + NUM_BARS * 8 + 15) / 16 * 16;
   static constexpr int ACQ_OFF = SCHED_OFF + kSchedRing * kSchedEntry;  // producer, then each epilogue warp
   static constexpr int MISC_OFF = ACQ_OFF + (1 + EPI_WARPS) * kAcqWords * 4;
@@ -182,7 +189,8 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   uint64_t* done_bar = tempty_bar + NACC;
   uint64_t* sfull_bar = done_bar + 1;             // [kSchedRing] a tile was published
   uint64_t* sempty_bar = sfull_bar + kSchedRing;  // [kSchedRing] every consumer has read it
-  uint64_t* epi_bars = sempty_bar + kSchedRing;   // [4 * kEpiWarps] owned by the epilogue warps
+  uint64_t* taken_bar = sempty_bar + kSchedRing;  // [kSchedRing] the (even CTA's) producer started it
+  uint64_t* epi_bars = taken_bar + kSchedRing;    // [4 * kEpiWarps] owned by the epilogue warps
   const uint32_t sched_ring = smem_u32(smem + S::SCHED_OFF);  // [kSchedRing] x {t, TileWork}
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
@@ -200,9 +208,10 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   } else if (leader && threadIdx.x == 0) {
     *skip_flag = *reinterpret_cast<volatile int*>(p.status);
   }
-  // consumers of one published tile index: the MMA thread and the epilogue warps of this CTA, plus
-  // in a pair the peer's producer thread and epilogue warps (the peer's MMA warp is idle)
-  constexpr uint32_t kSchedConsumers = PAIR ? 2u * (1u + kEpiWarps) : 1u + kEpiWarps;
+  // consumers of one published tile: the producer and MMA threads and the epilogue warps of this
+  // CTA, plus in a pair the peer's producer thread and epilogue warps (the peer's MMA and
+  // scheduler warps are idle)
+  constexpr uint32_t kSchedConsumers = PAIR ? 3u + 2u * kEpiWarps : 2u + kEpiWarps;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -217,6 +226,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     for (int r = 0; r < kSchedRing; ++r) {
       mbar_init(&sfull_bar[r], 1);
       mbar_init(&sempty_bar[r], kSchedConsumers);
+      mbar_init(&taken_bar[r], 1);
     }
     for (int b = 0; b < 4 * kEpiWarps; ++b) mbar_init(&epi_bars[b], 1);
     uint32_t* acq = reinterpret_cast<uint32_t*>(smem + S::ACQ_OFF);
@@ -251,7 +261,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   const long long kEnd = 0x7fffffffffffffffLL;
 
   // Static schedule: unit u (a CTA, or a pair) takes tiles u, u + units, ...  Dynamic schedule:
-  // the next tile comes from the global counter.  Either way the (even CTA's) producer thread
+  // the next tile comes from the global counter.  Either way the (even CTA's) scheduler thread
   // alone computes each tile's TileWork and publishes {t, TileWork} through the shared-memory
   // ring (into both CTAs of a pair), so the other roles never touch global memory to schedule.
   // The last entry published has t >= total_tiles and ends every role's loop.
@@ -281,22 +291,24 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     return (long long)(((unsigned long long)e0.y << 32) | e0.x);
   };
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer (both CTAs)
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      long long issued = 0;
-      bool ok = true;
+  if (warp == 2) {
+    // ---------------------------------------------------------------- scheduler (even CTA)
+    // Claims tiles (static or from the counter), decodes them and publishes them to every role,
+    // so the producer does not wait for a claim's atomic or for the offsets the decode reads.
+    // Tile n is claimed when the producer is about to finish issuing tile n - 1 (kClaimLeadKb).
+    if (lane == 0 && leader) {
       int* counter = p.status + 3;
-      auto produce_tile = [&](long long n, TileWork& w) -> long long {
-        if (PAIR && !leader) return consume_tile(n, false, w);
+      for (long long n = 0;; ++n) {
         const int r = (int)(n % kSchedRing);
         const uint32_t eph = (uint32_t)(((n / kSchedRing) & 1) ^ 1);
+        if (n >= 1) {
+          const long long m = n - 1;
+          if (!mbar_wait(&taken_bar[m % kSchedRing], (uint32_t)((m / kSchedRing) & 1), wg, 8)) break;
+        }
         // in a pair the odd CTA's consumers release the slot remotely: acquire at cluster scope
-        if (!(PAIR ? mbar_wait_cluster(&sempty_bar[r], eph, wg, 5) : mbar_wait(&sempty_bar[r], eph, wg, 5)))
-          return kEnd;
+        if (!(PAIR ? mbar_wait_cluster(&sempty_bar[r], eph, wg, 5) : mbar_wait(&sempty_bar[r], eph, wg, 5))) break;
         long long t = dynamic ? (long long)atomicAdd(counter, 1) : unit + n * units;
+        TileWork w;
         if (t >= p.total_tiles) {
           t = p.total_tiles;
           w = TileWork{0, 0, 0, 0, 0, 0};
@@ -315,15 +327,29 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
           mbar_arrive_remote(mapa_shared(smem_u32(&sfull_bar[r]), 1));
         }
         mbar_arrive(&sfull_bar[r]);
-        return t;
-      };
+        if (t >= p.total_tiles) break;
+      }
+    }
+  } else if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
       const uint32_t expect = PAIR ? 2u * S::STAGE_BYTES : (uint32_t)S::STAGE_BYTES;
       const MapAcquired acq_producer{reinterpret_cast<uint32_t*>(smem + S::ACQ_OFF)};
       long long n_tile = 0;
       TileWork w;
-      for (long long t = produce_tile(n_tile++, w); t < p.total_tiles && ok; t = produce_tile(n_tile++, w)) {
+      for (long long t = consume_tile(n_tile++, false, w); t < p.total_tiles && ok;
+           t = consume_tile(n_tile++, false, w)) {
+        // k-slices issued before the scheduler may claim the next tile (the even CTA decides)
+        const int lead = (w.active && w.num_kb > kClaimLeadKb) ? w.num_kb - kClaimLeadKb : 0;
+        uint64_t* const taken = &taken_bar[(n_tile - 1) % kSchedRing];
+        if (leader && lead == 0) mbar_arrive(taken);
         if (!w.active) continue;
         for (int kb = 0; kb < w.num_kb; ++kb) {
+          if (leader && kb == lead && kb > 0) mbar_arrive(taken);
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wg, 1)) {
             ok = false;
             break;
@@ -401,11 +427,11 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     }
   } else {
     // ---------------------------------------------------------------- epilogue warps (both CTAs)
+    const int e = warp - kFirstEpiWarp;     // index among the epilogue warps
     const int q = warp & 3;                 // TMEM sub-partition this warp may access
-    const int half = (warp - 2) >> 2;       // which of the sub-partition's warps
-    const EpiCtx ctx{q, half, lane, (int)rank, smem + S::EPI_OFF + (warp - 2) * P::STG_BYTES,
-                     epi_bars + 4 * (warp - 2),
-                     MapAcquired{reinterpret_cast<uint32_t*>(smem + S::ACQ_OFF) + (warp - 1) * kAcqWords}, wg};
+    const int half = e >> 2;                // which of the sub-partition's warps
+    const EpiCtx ctx{q, half, lane, (int)rank, smem + S::EPI_OFF + e * P::STG_BYTES, epi_bars + 4 * e,
+                     MapAcquired{reinterpret_cast<uint32_t*>(smem + S::ACQ_OFF) + (1 + e) * kAcqWords}, wg};
     uint32_t local = 0;
     long long n_tile = 0;
     TileWork w;
