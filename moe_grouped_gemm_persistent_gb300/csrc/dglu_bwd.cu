@@ -290,12 +290,25 @@ struct DgluPolicy {
 
   __device__ __forceinline__ void dbias_partials(const TileWork& w, int j0, int lane, float (&gv)[32],
                                                  float (&iv)[32]) const {
+    dbias_add(w, j0, lane, warp_column_sums(gv, lane), warp_column_sums(iv, lane));
+  }
+
+  // Column l of a staged 32 x 32 fp32 box (128B-swizzled rows, as stage_block writes them), summed
+  // over its 32 rows by lane l: the lanes of one row read 32 distinct banks.
+  static __device__ __forceinline__ float box_column_sum(uint32_t box, int lane) {
+    float sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) sum += ld_shared_f32(box + swz128(r, lane >> 2) + 4 * (lane & 3));
+    return sum;
+  }
+
+  // Adds this warp's column totals (lane l: gate column l in sg, input column l in si) of compact
+  // chunk j0 into the expert's fp32 partials.
+  __device__ __forceinline__ void dbias_add(const TileWork& w, int j0, int lane, float sg, float si) const {
     const int first = 2 * j0, second = 2 * j0 + 32;
     const int gcol = p.gate_first ? first : second;
     const int icol = p.gate_first ? second : first;
     float* ws = p.dbias_ws + (size_t)w.expert * 2 * (size_t)p.N;
-    const float sg = warp_column_sums(gv, lane);
-    const float si = warp_column_sums(iv, lane);
     // lanes 4i gather columns 4i..4i+3 and add them with one 16-byte reduction (4x fewer atomics
     // on addresses that every CTA of the same expert and column panel updates)
     float g4[4], i4[4];
@@ -428,14 +441,18 @@ struct DgluPolicy {
         staging_flush(box, lane, 2 * j0, row0);
       } else {  // fp32: the gate half, then the input half, each a 32 x 32 box through the C box
         const int first = 2 * j0, second = 2 * j0 + 32;
+        const bool db = p.dbias_ws != nullptr;
         stage_block(box, lane, 0, gv);
         staging_flush(box, lane, p.gate_first ? first : second, row0);
+        // dbias column totals straight from the staged fp32 values (the exact D_row values)
+        const float sg = db ? box_column_sum(box, lane) : 0.f;
         if (lane == 0) bulk_wait_read<0>();  // the gate half has left the box
         __syncwarp();
         stage_block(box, lane, 0, iv);
         staging_flush(box, lane, p.gate_first ? second : first, row0);
+        if (db) dbias_add(w, j0, lane, sg, box_column_sum(box, lane));
       }
-      if (p.dbias_ws != nullptr) dbias_partials(w, j0, lane, gv, iv);
+      if (DS == 2 && p.dbias_ws != nullptr) dbias_partials(w, j0, lane, gv, iv);
       if (i + 2 < nown) {  // refill with this warp's use u + 2 the box last used kCRing - 2 uses ago
         __syncwarp();
         if (lane == 0) {
