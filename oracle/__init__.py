@@ -1,4 +1,4 @@
-"""CPU oracle for the BF16 MoE grouped GEMM backward (dGLU dgrad + grouped wgrad).
+"""CPU oracle for the BF16 MoE grouped GEMM backward (dGLU / dsReLU dgrad + grouped wgrad).
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or link
 anything under ``oracle/``; the only callers are ``tests/``,
@@ -11,7 +11,10 @@ define, in float64 unless the pages fix the precision:
 * "Grouped GEMM + dGLU (SM100)", BF16 contract, "Tensors, layouts, and
   equation": R_g = alpha_g^2 A_g B_g^T, X_g = beta_g C_g, the dSwiGLU and dGeGLU
   derivatives on alternating 32-wide gate/input blocks, the dprob row sum and the
-  per-expert dbias.
+  per-expert dbias, the dSiTU-GLU derivatives of the block-scaled "Equations", and the
+  per-expert amax of 16-bit D_row.
+* "Grouped GEMM + dsReLU (SM100)", "Equations": D_row = prob * 2 * C * relu(alpha_g A_g B_g^T),
+  dprob = sum C * relu(.)^2, the per-expert Amax of 16-bit D_row.
 * "Grouped GEMM + WGrad (Unified)", "Operation": Wgrad[e] = A[:, begin:end] @
   B[begin:end, :], overwrite or accumulate_on_output.
 

@@ -1,4 +1,4 @@
-"""Plain float64 CPU oracle for the grouped dGLU dgrad and the grouped wgrad.
+"""Plain float64 CPU oracle for the grouped dGLU and dsReLU dgrad and the grouped wgrad.
 
 TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``): only tests, the smoke
 check and the benchmark's CPU-baseline leg may call this module.
@@ -206,8 +206,12 @@ def dglu_bwd(a: np.ndarray,
       dprob[m] = dprob_in[m] + sum_j R[m, j] * act[m, j];
       dbias[g, col] = dbias_in[g, col] + sum over the expert's rows of D_row[m, col].
 
-    ``rows`` restricts the evaluation to those rows (dbias is then not returned).
-    Returns dict(d_row (R, 2N), dprob (R,), rows, [dbias (L, 2N)]), float64.
+    amax[g, 0] / amax[g, 1] = the largest |dgate| / |dinput| over the expert's rows (the
+    per-group amax of shape (L, 2, 1) that the dGLU page lists among the outputs for 16-bit
+    D_row; its two entries read as the gate and the input block), 0 for an empty expert.
+
+    ``rows`` restricts the evaluation to those rows (dbias and amax are then not returned).
+    Returns dict(d_row (R, 2N), dprob (R,), rows, [dbias (L, 2N), amax (L, 2)]), float64.
     """
     a = np.asarray(a)
     M = a.shape[0]
@@ -228,6 +232,7 @@ def dglu_bwd(a: np.ndarray,
     dbias = np.zeros((L, two_n), dtype=np.float64) if all_rows else None
     if all_rows and dbias_in is not None:
         dbias += np.asarray(dbias_in, np.float64)
+    amax = np.zeros((L, 2), dtype=np.float64) if all_rows else None
     prob = np.asarray(prob, np.float64)
     for g, (lo, hi) in enumerate(ranges):
         sel = np.nonzero((rows >= lo) & (rows < hi))[0]
@@ -257,9 +262,85 @@ def dglu_bwd(a: np.ndarray,
         dprob[sel] += np.sum(R * a_unscaled, axis=1)
         if dbias is not None:
             dbias[g] += out.sum(axis=0)
+        if amax is not None:
+            amax[g, 0] = np.max(np.abs(dgate))
+            amax[g, 1] = np.max(np.abs(dinput))
     res = dict(d_row=d_row, dprob=dprob, rows=rows)
     if dbias is not None:
         res["dbias"] = dbias
+    if amax is not None:
+        res["amax"] = amax
+    return res
+
+
+# --------------------------------------------------------------------------------------
+# Grouped dgrad + dsReLU
+# --------------------------------------------------------------------------------------
+
+def dsrelu(G, prob, c):
+    """dsReLU backward on one block (dsReLU page, "Equations").
+
+    With relu(G) = max(G, 0): D_row = prob * 2 * C * relu(G) and the row terms of dprob are
+    C * relu(G)^2.  G is the alpha-scaled GEMM result, C the forward tensor, prob the row's
+    gating probability.  Returns (d_row, dprob_terms).
+    """
+    G = np.asarray(G, np.float64)
+    c = np.asarray(c, np.float64)
+    r = np.maximum(G, 0.0)
+    return np.asarray(prob, np.float64) * 2.0 * c * r, c * r * r
+
+
+def dsrelu_bwd(a: np.ndarray,
+               get_b: Callable[[int], np.ndarray],
+               c: np.ndarray,
+               offsets: Sequence[int],
+               alpha: Sequence[float],
+               prob: Sequence[float],
+               rows: Optional[np.ndarray] = None,
+               dprob_in: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+    """Grouped GEMM + dsReLU backward (dsReLU page, "Equations"), on BF16 operands.
+
+    a: (M, K) values of A; get_b(g) -> (N, K) values of B_g; c: (M, N) values of C (rows
+    ``rows`` of C when given); offsets: padded_offsets; alpha: (L,); prob: (M,).
+
+    For each expert g and row m in its range:
+      G[m, :] = alpha_g * (A[m, :] @ B_g^T)          (alpha, not alpha^2, as printed)
+      D_row[m, n] = prob[m] * 2 * C[m, n] * relu(G[m, n])
+      dprob[m] = dprob_in[m] + sum_n C[m, n] * relu(G[m, n])^2
+      amax[g] = the largest |D_row| over the expert's rows (the (L, 1) Amax of 16-bit D_row).
+    C and D_row are plain (M, N): no gate/input blocks, no beta.
+    Returns dict(d_row (R, N), dprob (R,), rows, [amax (L,)]), float64.
+    """
+    a = np.asarray(a)
+    M = a.shape[0]
+    L = len(offsets)
+    all_rows = rows is None
+    if all_rows:
+        rows = np.arange(M)
+    rows = np.asarray(rows, dtype=np.int64)
+    c = np.asarray(c)
+    n = c.shape[1]
+    d_row = np.zeros((len(rows), n), dtype=np.float64)
+    dprob = np.zeros(len(rows), dtype=np.float64)
+    if dprob_in is not None:
+        dprob += np.asarray(dprob_in, np.float64)[rows]
+    amax = np.zeros(L, dtype=np.float64) if all_rows else None
+    prob = np.asarray(prob, np.float64)
+    for g, (lo, hi) in enumerate(expert_ranges(offsets)):
+        sel = np.nonzero((rows >= lo) & (rows < hi))[0]
+        if sel.size == 0:
+            continue
+        b_g = np.asarray(get_b(g), dtype=np.float64)
+        G = float(alpha[g]) * (np.asarray(a[rows[sel]], dtype=np.float64) @ b_g.T)
+        c_rows = c[sel] if not all_rows else c[rows[sel]]
+        d, terms = dsrelu(G, prob[rows[sel]][:, None], c_rows)
+        d_row[sel] = d
+        dprob[sel] += terms.sum(axis=1)
+        if amax is not None:
+            amax[g] = np.max(np.abs(d))
+    res = dict(d_row=d_row, dprob=dprob, rows=rows)
+    if amax is not None:
+        res["amax"] = amax
     return res
 
 

@@ -525,3 +525,123 @@ def test_planted_mistakes_are_caught(monkeypatch):
     ref = brute_wgrad(A, B, offs)
     bad = O.wgrad(A.reshape(-1), B.reshape(-1), offs, 3, 4, b_major="k")
     assert not all(np.allclose(bad[e], ref[e]) for e in (0, 2, 3))
+
+
+# --------------------------------------------------------------------------------------
+# dsReLU (dsReLU page, "Equations") and the per-expert amax
+# --------------------------------------------------------------------------------------
+
+def fwd_srelu_unit(g, c):
+    """Forward term whose derivatives the dsReLU backward gives: c * relu(g)^2."""
+    return c * max(g, 0.0) ** 2
+
+
+def brute_dsrelu(a, bs, c, offsets, alpha, prob):
+    """Pure-python loops: expert found by scanning the ends, D by a central difference in G of
+    prob * c * relu(G)^2, dprob as the forward term summed over the row, amax by a running max."""
+    M, K = a.shape
+    N = c.shape[1]
+    L = len(offsets)
+    D = np.zeros((M, N))
+    dprob = np.zeros(M)
+    amax = np.zeros(L)
+    for m in range(M):
+        g = next(e for e in range(L) if m < offsets[e])
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += float(a[m, k]) * float(bs[g][n, k])
+            G = alpha[g] * acc
+            D[m, n] = prob[m] * fd(lambda x: fwd_srelu_unit(x, c[m, n]), G, h=1e-7)
+            dprob[m] += fwd_srelu_unit(G, c[m, n])
+            amax[g] = max(amax[g], abs(D[m, n]))
+    return D, dprob, amax
+
+
+def srelu_case(seed, counts, K, N):
+    rng = np.random.default_rng(seed)
+    offsets = np.cumsum(counts).astype(np.int64)
+    M = int(offsets[-1])
+    q = lambda x: np.round(x * 64) / 64
+    a = q(rng.normal(size=(M, K)))
+    bs = [q(rng.normal(size=(N, K))) for _ in counts]
+    c = q(rng.normal(size=(M, N)))
+    alpha = rng.uniform(0.5, 1.5, len(counts))
+    prob = rng.uniform(0, 1, M)
+    return a, bs, c, offsets, alpha, prob
+
+
+def test_dsrelu_bwd_bruteforce():
+    a, bs, c, offsets, alpha, prob = srelu_case(21, [3, 0, 2, 3], K=5, N=40)
+    res = O.dsrelu_bwd(a, lambda g: bs[g], c, offsets, alpha, prob)
+    D, dprob, amax = brute_dsrelu(a, bs, c, offsets, alpha, prob)
+    G_all = np.concatenate([alpha[g] * a[lo:hi] @ bs[g].T for g, (lo, hi) in enumerate(O.expert_ranges(offsets))])
+    assert (G_all > 0).any() and (G_all < 0).any()  # both sides of the relu are exercised
+    np.testing.assert_allclose(res["d_row"], D, rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(res["dprob"], dprob, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(res["amax"], amax, rtol=1e-6)
+    assert res["amax"][1] == 0.0  # empty expert
+
+
+def test_dsrelu_closed_forms_and_special_cases():
+    a, bs, c, offsets, alpha, prob = srelu_case(22, [4, 4], K=6, N=32)
+    G = np.concatenate([alpha[g] * a[lo:hi] @ bs[g].T for g, (lo, hi) in enumerate(O.expert_ranges(offsets))])
+    # C = 1, prob = 1: D_row = 2 relu(G) and dprob = sum relu(G)^2 exactly
+    res = O.dsrelu_bwd(a, lambda g: bs[g], np.ones_like(c), offsets, alpha, np.ones(8))
+    np.testing.assert_allclose(res["d_row"], 2 * np.maximum(G, 0), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(res["dprob"], (np.maximum(G, 0) ** 2).sum(1), rtol=1e-13)
+    # alpha (not alpha^2): doubling alpha doubles D_row and quadruples dprob
+    r1 = O.dsrelu_bwd(a, lambda g: bs[g], c, offsets, alpha, prob)
+    r2 = O.dsrelu_bwd(a, lambda g: bs[g], c, offsets, 2 * alpha, prob)
+    np.testing.assert_allclose(r2["d_row"], 2 * r1["d_row"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(r2["dprob"], 4 * r1["dprob"], rtol=1e-13, atol=1e-13)
+    # prob = 0 zeroes D_row but not dprob (no prob factor); negative G contributes nothing
+    r0 = O.dsrelu_bwd(a, lambda g: bs[g], c, offsets, alpha, np.zeros(8), dprob_in=np.arange(8.0))
+    assert (r0["d_row"] == 0).all()
+    np.testing.assert_allclose(r0["dprob"], r1["dprob"] + np.arange(8.0), rtol=1e-13)
+    neg = O.dsrelu_bwd(a, lambda g: -bs[g], c, offsets, alpha, prob)
+    np.testing.assert_array_equal(neg["d_row"][G > 0], 0.0)
+    # dprob is the derivative in prob of sum prob * C * relu(G)^2
+    fwd = (c * np.maximum(G, 0) ** 2).sum(1)
+    np.testing.assert_allclose(r1["dprob"], fwd, rtol=1e-13)
+    rows = np.array([7, 1, 4])
+    part = O.dsrelu_bwd(a, lambda g: bs[g], c[rows], offsets, alpha, prob, rows=rows)
+    np.testing.assert_array_equal(part["d_row"], r1["d_row"][rows])
+
+
+def test_dglu_amax_is_per_expert_block_max():
+    a, bs, c, offsets, alpha, beta, prob = tiny_case(23, [3, 0, 4], K=4, N=64)
+    res = O.dglu_bwd(a, lambda g: bs[g], c, offsets, alpha, beta, prob, act="dgeglu")
+    D = res["d_row"]
+    gcol, icol = O.glu_columns(64)
+    for g, (lo, hi) in enumerate(O.expert_ranges(offsets)):
+        if hi == lo:
+            assert (res["amax"][g] == 0).all()
+            continue
+        blk = D[lo:hi]
+        assert res["amax"][g, 0] == np.abs(blk[:, gcol]).max()
+        assert res["amax"][g, 1] == np.abs(blk[:, icol]).max()
+    # gate/input roles: with the blocks swapped in the layout the two entries follow their block
+    res2 = O.dglu_bwd(a, lambda g: bs[g], c, offsets, alpha, beta, prob, act="dgeglu", gate_first=False)
+    g2, i2 = O.glu_columns(64, gate_first=False)
+    assert res2["amax"][0, 0] == np.abs(res2["d_row"][0:3][:, g2]).max()
+
+
+def test_dsrelu_planted_mistakes_are_caught(monkeypatch):
+    a, bs, c, offsets, alpha, prob = srelu_case(24, [3, 0, 2, 3], K=5, N=40)
+    D, dprob, amax = brute_dsrelu(a, bs, c, offsets, alpha, prob)
+
+    def ok(r):
+        return (np.allclose(r["d_row"], D, rtol=1e-6, atol=1e-8) and np.allclose(r["dprob"], dprob, rtol=1e-9)
+                and np.allclose(r["amax"], amax, rtol=1e-6))
+
+    assert ok(O.dsrelu_bwd(a, lambda g: bs[g], c, offsets, alpha, prob))
+    assert not ok(O.dsrelu_bwd(a, lambda g: bs[g], c, offsets, alpha ** 2, prob))   # alpha^2 instead of alpha
+    assert not ok(O.dsrelu_bwd(a, lambda g: bs[g][::-1], c, offsets, alpha, prob))    # permuted weight rows
+    with monkeypatch.context() as mp:
+        mp.setattr(O, "dsrelu", lambda G, p, cc: (p * 2.0 * np.asarray(cc) * np.abs(G),
+                                                  np.asarray(cc) * np.asarray(G) ** 2))  # |G| instead of relu
+        assert not ok(O.dsrelu_bwd(a, lambda g: bs[g], c, offsets, alpha, prob))
+    with monkeypatch.context() as mp:
+        mp.setattr(O, "expert_ranges", lambda offs: [(0, 2), (2, 2), (2, 5), (5, 8)])     # shifted ranges
+        assert not ok(O.dsrelu_bwd(a, lambda g: bs[g], c, offsets, alpha, prob))
