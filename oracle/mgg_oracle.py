@@ -496,6 +496,7 @@ __all__ = [
     "GEGLU_ALPHA", "GLU_CLAMP_MAX", "GLU_CLAMP_MIN", "LINEAR_OFFSET", "GLU_BLOCK", "M_ALIGNED", "MAX_EXPERTS",
     "SITU_BETA1", "SITU_BETA2",
     "expert_ranges", "sigmoid", "glu_columns", "dswiglu", "dgeglu", "dsituglu", "scale_x", "dglu_bwd",
+    "dsrelu", "dsrelu_bwd",
     "wgrad_a_block", "wgrad_b_block", "wgrad", "wgrad_elements", "dgrad_tiles", "wgrad_tiles",
     "offsets_valid",
 ]
