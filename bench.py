@@ -38,6 +38,8 @@ WORKLOAD_TEXT = {
     "wgrad64": "grouped wgrad: L=64, hidden=2048, inter=1408, T=65536 Zipf(1.2), FP32 dense accumulate",
     "tiny": "tiny: L=4, counts [256,0,512,256], K=hidden=256, N=128",
     "mixtral_situ": "Mixtral-like shape with the dSiTU-GLU backward (beta1=4, beta2=25), C~N(0,4), BF16 D_row",
+    "dsrelu": "Mixtral-like shape with the dsReLU backward: L=8, K=4096, N=14336, 32768 tokens uniform, "
+              "C (M,N) BF16, BF16 D_row, dprob and per-expert Amax",
     "mixtral_s": "profiling copy of mixtral with L=2 experts, 8192 tokens",
     "geglu_s": "profiling copy of geglu with 12288 tokens",
     "deepseek_s": "profiling copy of deepseek with L=32 experts, 16384 tokens",
@@ -163,7 +165,10 @@ class Problem:
             s = self.dspec
             x = synth.make_dglu_inputs(s, device=dev)
             self.d = x
-            self.d_row = torch.empty(s.M, 2 * s.N, dtype=synth.torch_dtype(s.d_dtype), device=dev)
+            self.srelu = s.act == "dsrelu"
+            cols = s.N if self.srelu else 2 * s.N
+            self.d_row = torch.empty(s.M, cols, dtype=synth.torch_dtype(s.d_dtype), device=dev)
+            self.amax = torch.zeros(s.L, dtype=torch.float32, device=dev) if self.srelu else None
             self.dprob = torch.zeros(s.M, dtype=torch.float32, device=dev)
             self.dbias = torch.zeros(s.L, 2 * s.N, dtype=torch.bfloat16, device=dev) if s.dbias else None
             if s.b_mode == "discrete":
@@ -171,7 +176,8 @@ class Problem:
                 self.b_kw = dict(b_ptrs=self.b_ptrs, b_major=s.b_major, N=s.N)
             else:
                 self.b_kw = dict(b=x["b"])
-            self.d_ws = api.new_workspace(api.dglu_bwd_workspace_size(s.L, s.N), dev)
+            self.d_ws = api.new_workspace(api.dsrelu_bwd_workspace_size(s.L) if self.srelu
+                                          else api.dglu_bwd_workspace_size(s.L, s.N), dev)
         if self.wspec is not None:
             s = self.wspec
             y = synth.make_wgrad_inputs(s, device=dev)
@@ -200,6 +206,11 @@ class Problem:
     def dgrad(self):
         s, x = self.dspec, self.d
         self.dprob.zero_()
+        if self.srelu:
+            self.api.dsrelu_bwd(a=x["a"], c=x["c"], padded_offsets=x["padded_offsets"], alpha=x["alpha"],
+                                prob=x["prob"], dprob=self.dprob, d_row=self.d_row, amax=self.amax,
+                                workspace=self.d_ws, sched=self.sched, cta=self.cta, **self.b_kw)
+            return
         if self.dbias is not None:
             self.dbias.zero_()
         self.api.dglu_bwd(a=x["a"], c=x["c"], padded_offsets=x["padded_offsets"], alpha=x["alpha"], beta=x["beta"],
@@ -227,7 +238,8 @@ class Problem:
             s = self.dspec
             esz = {"bf16": 2, "fp16": 2, "fp32": 4}
             nz = int((s.counts > 0).sum())
-            b["dgrad"] = (s.M * s.K * 2 + nz * s.N * s.K * 2 + s.M * 2 * s.N * (esz[s.c_dtype] + esz[s.d_dtype])
+            cols = s.N if s.act == "dsrelu" else 2 * s.N
+            b["dgrad"] = (s.M * s.K * 2 + nz * s.N * s.K * 2 + s.M * cols * (esz[s.c_dtype] + esz[s.d_dtype])
                           + s.M * 12)
         if self.wspec is not None:
             s = self.wspec
@@ -369,7 +381,10 @@ def oracle_sample(prob_or_specs, dev, budget_s: float, seed: int = 0, max_expert
                 alpha, beta = x["alpha"].cpu().numpy(), x["beta"].cpu().numpy()
                 pr = x["prob"][lo:hi].cpu().numpy()
                 t0 = time.perf_counter()
-                oracle.dglu_bwd(a, lambda g: b_g, c, offs_local, alpha, beta, pr, act=spec.act)
+                if spec.act == "dsrelu":
+                    oracle.dsrelu_bwd(a, lambda g: b_g, c, offs_local, alpha, pr)
+                else:
+                    oracle.dglu_bwd(a, lambda g: b_g, c, offs_local, alpha, beta, pr, act=spec.act)
                 dt = time.perf_counter() - t0
                 fl = 2.0 * (hi - lo) * spec.N * spec.K
             else:

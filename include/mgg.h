@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MGG_ABI_VERSION 3
+#define MGG_ABI_VERSION 4
 
 typedef enum mgg_status {
   MGG_OK = 0,
@@ -106,6 +106,13 @@ typedef enum mgg_input_order { MGG_ORDER_TENSOR2D = 0, MGG_ORDER_TENSOR_RAGGED =
  *   d_row          (M, 2N), stride (2N, 1), dtype d_dtype               [write]
  *   dbias          bf16 (L, 2N), caller-initialised; column sums are ADDED
  *                  (one bf16 rounding of old + sum); NULL = no dbias
+ *   d_col          optional second copy of D_row, same shape, stride and dtype (the dGLU
+ *                  page's column output; without quantisation it holds the D_row values);
+ *                  NULL = off                                            [write]
+ *   amax           optional fp32 (L, 2): per expert the largest |dgate| and |dinput| over
+ *                  its rows (the page's per-group amax of 16-bit D_row; the two entries are
+ *                  the gate and the input block), before output rounding; 0 for an empty
+ *                  expert.  Overwritten (the call zeroes it first).  NULL = off  [write]
  *   workspace      device scratch of at least mgg_dglu_bwd_workspace_size(L, N) bytes,
  *                  256-byte aligned
  *   tile_log       optional int32[4 * tile_log_capacity]: for every output tile the
@@ -126,6 +133,8 @@ typedef struct mgg_dglu_bwd_args {
   float* dprob;
   void* d_row;
   void* dbias;
+  void* d_col;
+  float* amax;
   void* workspace;
   int32_t* tile_log;
   int64_t workspace_bytes;
@@ -141,6 +150,49 @@ typedef struct mgg_dglu_bwd_args {
   float situ_beta1;       /* dSiTU-GLU gate tanh scale, positive finite; 0 = the default 4.0 */
   float situ_beta2;       /* dSiTU-GLU input tanh scale, positive finite; 0 = the default 25.0 */
 } mgg_dglu_bwd_args;
+
+/*
+ * Arguments of mgg_dsrelu_bwd: the dsReLU page's epilogue ("Equations") on the BF16 grouped
+ * GEMM of the dGLU page's layouts.  M = valid rows = padded_offsets[L-1]; N = columns of C,
+ * D_row and the GEMM result G.
+ *
+ *   a, b, b_ptrs, b_major, padded_offsets, prob, dprob, workspace, tile_log: as for
+ *                  mgg_dglu_bwd (dprob: the row sums are ADDED)
+ *   c              (M, N), stride (N, 1), 16-bit (bf16 or fp16)           [read]
+ *   alpha          fp32[L]: G = alpha_g * A_g B_g^T (alpha, not squared)  [read]
+ *   d_row          (M, N), stride (N, 1), dtype d_dtype:
+ *                  D_row = prob * 2 * C * relu(G)                         [write]
+ *   dprob          dprob[m] += sum_n C[m, n] * relu(G[m, n])^2
+ *   d_col          optional copy of D_row (same shape, stride, dtype); NULL = off [write]
+ *   amax           optional fp32 (L): per expert the largest |D_row| before output rounding,
+ *                  0 for an empty expert; overwritten.  NULL = off            [write]
+ *   workspace      at least mgg_dsrelu_bwd_workspace_size(L) bytes, 256-byte aligned
+ * Requirements checked on the host: as for mgg_dglu_bwd with C (M, N); C is 16-bit.
+ */
+typedef struct mgg_dsrelu_bwd_args {
+  int64_t M, K, N, L;
+  const void* a;
+  const void* b;
+  const int64_t* b_ptrs;
+  const void* c;
+  const int32_t* padded_offsets;
+  const float* alpha;
+  const float* prob;
+  float* dprob;
+  void* d_row;
+  void* d_col;
+  float* amax;
+  void* workspace;
+  int32_t* tile_log;
+  int64_t workspace_bytes;
+  int64_t tile_log_capacity;
+  int32_t b_major;        /* mgg_major, discrete weights only */
+  int32_t c_dtype;        /* mgg_dtype: MGG_BF16 or MGG_FP16 */
+  int32_t d_dtype;        /* mgg_dtype */
+  int32_t sched;          /* mgg_sched */
+  int32_t cta_mode;       /* mgg_cta_mode */
+  int32_t reserved;       /* must be 0 */
+} mgg_dsrelu_bwd_args;
 
 /*
  * Arguments of mgg_wgrad (wgrad page, BF16 contract).  T = tokens_sum = offsets[L-1].
@@ -189,6 +241,7 @@ int mgg_abi_version(void);
 
 /* sizeof the argument structs as compiled into the library (binding layout checks). */
 size_t mgg_sizeof_dglu_bwd_args(void);
+size_t mgg_sizeof_dsrelu_bwd_args(void);
 size_t mgg_sizeof_wgrad_args(void);
 
 /* Last error message of the calling thread ("" after a successful call). */
@@ -201,11 +254,15 @@ const char* mgg_status_string(int status);
  * (status word, per-expert tensor-map slots, fp32 dbias partial sums). */
 size_t mgg_dglu_bwd_workspace_size(int64_t L, int64_t N);
 
+/* Workspace bytes for mgg_dsrelu_bwd with L experts (status word, per-expert tensor-map slots). */
+size_t mgg_dsrelu_bwd_workspace_size(int64_t L);
+
 /* Workspace bytes for mgg_wgrad with L experts (status word, per-expert tensor-map
  * slots for ragged inputs and discrete outputs, the expert order of the scheduler). */
 size_t mgg_wgrad_workspace_size(int64_t L);
 
-/* Number of output tiles mgg_dglu_bwd / mgg_wgrad enumerate (tile_log capacity). */
+/* Number of output tiles mgg_dglu_bwd / mgg_wgrad enumerate (tile_log capacity); mgg_dsrelu_bwd
+ * enumerates mgg_dglu_bwd_num_tiles(M, N) tiles of the same shape. */
 int64_t mgg_dglu_bwd_num_tiles(int64_t M, int64_t N);
 int64_t mgg_wgrad_num_tiles(int64_t L, int64_t hidden, int64_t inter);
 /* Tile shape (rows, columns) of the output tiles each operation logs. */
@@ -214,6 +271,9 @@ void mgg_wgrad_tile_shape(int64_t inter, int32_t* tile_m, int32_t* tile_n);
 
 /* Grouped GEMM + dGLU backward.  Queues its kernels on `stream` (a cudaStream_t). */
 mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream);
+
+/* Grouped GEMM + dsReLU backward.  Queues its kernels on `stream` (a cudaStream_t). */
+mgg_status mgg_dsrelu_bwd(const mgg_dsrelu_bwd_args* args, void* stream);
 
 /* Grouped wgrad.  Queues its kernels on `stream` (a cudaStream_t). */
 mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream);

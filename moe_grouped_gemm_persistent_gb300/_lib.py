@@ -31,12 +31,25 @@ class DgluBwdArgs(ctypes.Structure):
         ("M", c_int64), ("K", c_int64), ("N", c_int64), ("L", c_int64),
         ("a", c_void_p), ("b", c_void_p), ("b_ptrs", c_void_p), ("c", c_void_p),
         ("padded_offsets", c_void_p), ("alpha", c_void_p), ("beta", c_void_p), ("prob", c_void_p),
-        ("dprob", c_void_p), ("d_row", c_void_p), ("dbias", c_void_p), ("workspace", c_void_p),
-        ("tile_log", c_void_p),
+        ("dprob", c_void_p), ("d_row", c_void_p), ("dbias", c_void_p), ("d_col", c_void_p), ("amax", c_void_p),
+        ("workspace", c_void_p), ("tile_log", c_void_p),
         ("workspace_bytes", c_int64), ("tile_log_capacity", c_int64),
         ("b_major", c_int32), ("c_dtype", c_int32), ("d_dtype", c_int32), ("act", c_int32),
         ("geglu_filter", c_int32), ("gate_first", c_int32), ("sched", c_int32), ("cta_mode", c_int32),
         ("situ_beta1", ctypes.c_float), ("situ_beta2", ctypes.c_float),
+    ]
+
+
+class DsreluBwdArgs(ctypes.Structure):
+    _fields_ = [
+        ("M", c_int64), ("K", c_int64), ("N", c_int64), ("L", c_int64),
+        ("a", c_void_p), ("b", c_void_p), ("b_ptrs", c_void_p), ("c", c_void_p),
+        ("padded_offsets", c_void_p), ("alpha", c_void_p), ("prob", c_void_p),
+        ("dprob", c_void_p), ("d_row", c_void_p), ("d_col", c_void_p), ("amax", c_void_p),
+        ("workspace", c_void_p), ("tile_log", c_void_p),
+        ("workspace_bytes", c_int64), ("tile_log_capacity", c_int64),
+        ("b_major", c_int32), ("c_dtype", c_int32), ("d_dtype", c_int32), ("sched", c_int32),
+        ("cta_mode", c_int32), ("reserved", c_int32),
     ]
 
 
@@ -55,16 +68,19 @@ class WgradArgs(ctypes.Structure):
 SIGNATURES = [
     ("mgg_abi_version", c_int, []),
     ("mgg_sizeof_dglu_bwd_args", c_size_t, []),
+    ("mgg_sizeof_dsrelu_bwd_args", c_size_t, []),
     ("mgg_sizeof_wgrad_args", c_size_t, []),
     ("mgg_last_error", c_char_p, []),
     ("mgg_status_string", c_char_p, [c_int]),
     ("mgg_dglu_bwd_workspace_size", c_size_t, [c_int64, c_int64]),
+    ("mgg_dsrelu_bwd_workspace_size", c_size_t, [c_int64]),
     ("mgg_wgrad_workspace_size", c_size_t, [c_int64]),
     ("mgg_dglu_bwd_num_tiles", c_int64, [c_int64, c_int64]),
     ("mgg_wgrad_num_tiles", c_int64, [c_int64, c_int64, c_int64]),
     ("mgg_dglu_bwd_tile_shape", None, [ctypes.POINTER(c_int32), ctypes.POINTER(c_int32)]),
     ("mgg_wgrad_tile_shape", None, [c_int64, ctypes.POINTER(c_int32), ctypes.POINTER(c_int32)]),
     ("mgg_dglu_bwd", c_int, [ctypes.POINTER(DgluBwdArgs), c_void_p]),
+    ("mgg_dsrelu_bwd", c_int, [ctypes.POINTER(DsreluBwdArgs), c_void_p]),
     ("mgg_wgrad", c_int, [ctypes.POINTER(WgradArgs), c_void_p]),
     ("mgg_wgrad_noalloc", c_int, [ctypes.POINTER(WgradArgs), c_void_p]),
     ("mgg_read_device_status", c_int, [c_void_p, c_void_p]),

@@ -10,7 +10,8 @@ from typing import Optional, Sequence
 import torch
 
 from . import _lib
-from ._lib import ACTS, CTA_MODES, DTYPES, FILTERS, MAJORS, ORDERS, SCHEDS, DgluBwdArgs, WgradArgs, check, load
+from ._lib import (ACTS, CTA_MODES, DTYPES, FILTERS, MAJORS, ORDERS, SCHEDS, DgluBwdArgs, DsreluBwdArgs, WgradArgs,
+                   check, load)
 
 _TORCH_TO_DT = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}
 
@@ -69,7 +70,7 @@ def new_workspace(nbytes: int, device) -> torch.Tensor:
 def make_dglu_args(*, a, c, padded_offsets, alpha, beta, prob, dprob, d_row, b=None, b_ptrs=None, N=None,
                    dbias=None, act="dswiglu", geglu_filter="value", gate_first=True, b_major="k",
                    sched="static", workspace=None, tile_log=None, situ_beta1=4.0, situ_beta2=25.0,
-                   cta="auto") -> DgluBwdArgs:
+                   cta="auto", d_col=None, amax=None) -> DgluBwdArgs:
     M, K = a.shape
     L = padded_offsets.numel()
     if N is None:
@@ -83,6 +84,7 @@ def make_dglu_args(*, a, c, padded_offsets, alpha, beta, prob, dprob, d_row, b=N
     args.padded_offsets = _ptr(padded_offsets)
     args.alpha, args.beta, args.prob = _ptr(alpha), _ptr(beta), _ptr(prob)
     args.dprob, args.d_row, args.dbias = _ptr(dprob), _ptr(d_row), _ptr(dbias)
+    args.d_col, args.amax = _ptr(d_col), _ptr(amax)
     args.workspace = _ptr(workspace)
     args.workspace_bytes = workspace.numel() if workspace is not None else 0
     args.tile_log = _ptr(tile_log)
@@ -106,10 +108,13 @@ def dglu_bwd(*, a: torch.Tensor, c: torch.Tensor, padded_offsets: torch.Tensor, 
              dbias: Optional[torch.Tensor] = None, act: str = "dswiglu", geglu_filter: str = "value",
              gate_first: bool = True, b_major: str = "k", sched: str = "dynamic",
              workspace: Optional[torch.Tensor] = None, tile_log: Optional[torch.Tensor] = None, stream=None,
-             situ_beta1: float = 4.0, situ_beta2: float = 25.0, cta: str = "auto"):
+             situ_beta1: float = 4.0, situ_beta2: float = 25.0, cta: str = "auto",
+             d_col: Optional[torch.Tensor] = None, amax: Optional[torch.Tensor] = None):
     """Grouped GEMM + dGLU backward (see include/mgg.h, mgg_dglu_bwd).
 
     ``cta`` is "auto", "single" (128-row tiles per CTA) or "pair" (256-row tiles per CTA pair).
+    ``d_col`` (a second D_row) and ``amax`` (fp32 (L, 2), per expert max |dgate|, |dinput|) are
+    optional outputs.
 
     d_row is written; dprob and dbias (when given) are accumulated into.  Returns the
     workspace used (allocated here when not given).
@@ -121,8 +126,53 @@ def dglu_bwd(*, a: torch.Tensor, c: torch.Tensor, padded_offsets: torch.Tensor, 
     args = make_dglu_args(a=a, c=c, padded_offsets=padded_offsets, alpha=alpha, beta=beta, prob=prob, dprob=dprob,
                           d_row=d_row, b=b, b_ptrs=b_ptrs, N=n, dbias=dbias, act=act, geglu_filter=geglu_filter,
                           gate_first=gate_first, b_major=b_major, sched=sched, workspace=workspace,
-                          tile_log=tile_log, situ_beta1=situ_beta1, situ_beta2=situ_beta2, cta=cta)
+                          tile_log=tile_log, situ_beta1=situ_beta1, situ_beta2=situ_beta2, cta=cta, d_col=d_col,
+                          amax=amax)
     check(load().mgg_dglu_bwd(args, _stream(stream)))
+    return workspace
+
+
+def dsrelu_bwd_workspace_size(L: int) -> int:
+    return int(load().mgg_dsrelu_bwd_workspace_size(L))
+
+
+def make_dsrelu_args(*, a, c, padded_offsets, alpha, prob, dprob, d_row, b=None, b_ptrs=None, N=None, b_major="k",
+                     d_col=None, amax=None, sched="static", workspace=None, tile_log=None, cta="auto") -> DsreluBwdArgs:
+    M, K = a.shape
+    args = DsreluBwdArgs()
+    args.M, args.K, args.N, args.L = M, K, (N if N is not None else c.shape[1]), padded_offsets.numel()
+    args.a, args.b, args.b_ptrs, args.c = _ptr(a), _ptr(b), _ptr(b_ptrs), _ptr(c)
+    args.padded_offsets, args.alpha, args.prob = _ptr(padded_offsets), _ptr(alpha), _ptr(prob)
+    args.dprob, args.d_row, args.d_col, args.amax = _ptr(dprob), _ptr(d_row), _ptr(d_col), _ptr(amax)
+    args.workspace = _ptr(workspace)
+    args.workspace_bytes = workspace.numel() if workspace is not None else 0
+    args.tile_log = _ptr(tile_log)
+    args.tile_log_capacity = tile_log.numel() // 4 if tile_log is not None else 0
+    args.b_major = MAJORS[b_major]
+    args.c_dtype = DTYPES[_TORCH_TO_DT[c.dtype]]
+    args.d_dtype = DTYPES[_TORCH_TO_DT[d_row.dtype]]
+    args.sched = SCHEDS[sched]
+    args.cta_mode = CTA_MODES[cta]
+    args.reserved = 0
+    return args
+
+
+def dsrelu_bwd(*, a: torch.Tensor, c: torch.Tensor, padded_offsets: torch.Tensor, alpha: torch.Tensor,
+               prob: torch.Tensor, dprob: torch.Tensor, d_row: torch.Tensor, b: Optional[torch.Tensor] = None,
+               b_ptrs: Optional[torch.Tensor] = None, N: Optional[int] = None, b_major: str = "k",
+               d_col: Optional[torch.Tensor] = None, amax: Optional[torch.Tensor] = None, sched: str = "dynamic",
+               workspace: Optional[torch.Tensor] = None, tile_log: Optional[torch.Tensor] = None, stream=None,
+               cta: str = "auto"):
+    """Grouped GEMM + dsReLU backward (see include/mgg.h, mgg_dsrelu_bwd): D_row = prob*2*C*relu(G),
+    dprob += sum C*relu(G)^2 with G = alpha_g A_g B_g^T; optional D_col copy and per-expert amax (L,).
+    Returns the workspace used."""
+    L = padded_offsets.numel()
+    if workspace is None:
+        workspace = new_workspace(dsrelu_bwd_workspace_size(L), a.device)
+    args = make_dsrelu_args(a=a, c=c, padded_offsets=padded_offsets, alpha=alpha, prob=prob, dprob=dprob,
+                            d_row=d_row, b=b, b_ptrs=b_ptrs, N=N, b_major=b_major, d_col=d_col, amax=amax,
+                            sched=sched, workspace=workspace, tile_log=tile_log, cta=cta)
+    check(load().mgg_dsrelu_bwd(args, _stream(stream)))
     return workspace
 
 

@@ -31,14 +31,12 @@ struct DgluCfg {
   static constexpr bool kTmaC = TMAC && CS == 2;
   static constexpr int kEpiWarps = 8;
   static constexpr int kCRing = 2;  // C boxes per warp (TMA path)
-  // bulk groups one chunk commits on the TMA path: 16-bit D leaves in one store, fp32 D in two
-  // (the gate half, then the input half, through the same box)
-  static constexpr int kGroups = DS == 4 ? 2 : 1;
   // TMA path: the C ring (results leave through the consumed box); register path: D staging
   static constexpr int kStgBytes = kTmaC ? kCRing * 4096 : (DS == 4 ? 8192 : 4096);
   static constexpr int kStages = max_stages(PAIR ? kDgluTileN / 2 : kDgluTileN, kEpiWarps, kStgBytes,
                                             num_acc(kDgluTileN), 6);
   static_assert(kStages >= 3, "operand ring too shallow");
+  static_assert(!kTmaC || kCRing == 2, "the ring refill waits for all stores of the consumed box");
 };
 
 struct DgluParams {
@@ -46,6 +44,7 @@ struct DgluParams {
   CUtensorMap tmap_b;           // dense B (N, K, L): dims {K, N, L}, box {64, BN, 1}
   CUtensorMap tmap_d;           // D_row (M, 2N): dims {2N, M}, box {128 B of columns, 32}, 128B swizzle
   CUtensorMap tmap_c;           // 16-bit C (M, 2N): dims {2N, M}, box {64, 32}, 128B swizzle
+  CUtensorMap tmap_dcol;        // optional D_col, same geometry as tmap_d (has_dcol)
   const CUtensorMap* b_maps;    // discrete B: one map per expert in the workspace, else null
   const int32_t* offsets;
   const float* alpha;
@@ -54,12 +53,14 @@ struct DgluParams {
   const void* c;
   float* dprob;
   float* dbias_ws;              // fp32 partial sums (L, 2N), null = no dbias
+  float* amax;                  // per-expert |D| maxima ((L, 2) dGLU, (L) dsReLU), zeroed by the prep kernel; or null
+  int has_dcol;                 // 1: every D_row box is also stored through tmap_dcol
   int* status;
   int32_t* tile_log;
   long long tile_log_cap;
   long long total_tiles;
   int dynamic;                  // 1: tiles claimed from the workspace counter
-  int M, K, N, L;
+  int M, K, N, L;               // dsReLU: N = columns of C / D_row (dGLU: 2N of them)
   int num_n, num_kb;
   int a_mn, b_mn;
   int b_blocked;                // discrete N-major B maps are 3-D (64-column blocks, one box per slot)
@@ -76,8 +77,13 @@ __device__ __forceinline__ float fast_tanh(float x) { return 1.0f - 2.0f * rcp_a
 // Byte offset of 16-byte chunk `c16` of row `r` in a 128B-swizzled staging box (rows of 128 B).
 __device__ __forceinline__ uint32_t swz128(int r, int c16) { return (uint32_t)(r * 128 + ((c16 ^ (r & 7)) << 4)); }
 
+// The epilogue a launch runs on the grouped GEMM result: the dGLU page's (gate/input blocks of C
+// and D_row, R = alpha^2 acc) or the dsReLU page's (plain C and D_row of N columns, G = alpha acc).
+constexpr int kOpGlu = 0;
+constexpr int kOpSrelu = 1;
+
 // CS / DS: element size in bytes of C and D_row (2 = bf16/fp16, 4 = fp32).
-template <int BN, int CS, int DS, bool TMAC, bool PAIR>
+template <int BN, int CS, int DS, bool TMAC, bool PAIR, int OP>
 struct DgluPolicy {
   using Cfg = DgluCfg<CS, DS, TMAC, PAIR>;
   static constexpr int kTileM = PAIR ? 2 * BM : BM;   // rows of a tile (a pair's tile spans both CTAs)
@@ -219,13 +225,35 @@ struct DgluPolicy {
     __syncwarp();
   }
 
+  // Bulk store of one staged box to D_row (and to D_col when requested); lane 0 of the warp.
+  __device__ __forceinline__ void store_box(uint32_t stg, int x, int y) const {
+    tma_store_2d(&p.tmap_d, stg, x, y);
+    if (p.has_dcol) tma_store_2d(&p.tmap_dcol, stg, x, y);
+  }
+
   __device__ __forceinline__ void staging_flush(uint32_t stg, int lane, int x, int y) const {
     fence_async_shared();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(&p.tmap_d, stg, x, y);
+      store_box(stg, x, y);
       bulk_commit_group();
     }
+  }
+
+  // Largest |v| of 32 values, folded into a running maximum.
+  static __device__ __forceinline__ float absmax32(const float (&v)[32], float m) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) m = fmaxf(m, fabsf(v[k]));
+    return m;
+  }
+
+  // The warp's running |D| maxima of one tile into the expert's amax (non-negative floats order
+  // like their bit patterns as signed integers).
+  __device__ __forceinline__ void amax_flush(int g, int slot, float m) const {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0 && m > 0.f) atomicMax(reinterpret_cast<int*>(p.amax) + slot, __float_as_int(m));
+    (void)g;
   }
 
   // dGLU math on 32 columns of one row.  On entry gv / iv hold the C values of the gate and the
@@ -337,8 +365,17 @@ struct DgluPolicy {
     }
   }
 
+  // Epilogue uses of a tile: each covers a 32-row x 64-column box of C and D_row per warp.  A dGLU
+  // use is 32 accumulator columns (gate and input block); a dsReLU use 64 accumulator columns
+  // (rounded up: past N the accumulator and the C box hold zeros).
   __device__ __forceinline__ int num_chunks(const TileWork& w) const {
-    return (p.N - w.n0 < BN ? p.N - w.n0 : BN) / 32;
+    const int cols = p.N - w.n0 < BN ? p.N - w.n0 : BN;
+    return OP == kOpGlu ? cols / 32 : (cols + 63) / 64;
+  }
+
+  // First column of C / D_row of use c of tile w.
+  __device__ __forceinline__ int use_col(const TileWork& w, int c) const {
+    return OP == kOpGlu ? 2 * (w.n0 + 32 * c) : w.n0 + 64 * c;
   }
 
   // Chunks of this warp: half, half + kEpiHalves, ...
@@ -349,12 +386,12 @@ struct DgluPolicy {
   // ---------------------------------------------------------------- TMA path for 16-bit C
   // Ring of kCRing 4 KB boxes per warp: box u % kCRing holds rows [row0, row0+32) x C columns
   // [2*j0, 2*j0+64) (the gate and the input block of compact chunk j0).  Use u + 2 is loaded when
-  // use u is done; the results overwrite the consumed box and leave by bulk stores (kGroups bulk
-  // groups per use), so a box is reloaded only once those stores have read it.
-  __device__ __forceinline__ void c_issue(const EpiCtx& ctx, uint32_t use, int j0, int row0) const {
+  // use u is done; the results overwrite the consumed box and leave by bulk stores (16-bit D in
+  // one, fp32 D as two halves), so a box is reloaded only once those stores have read it.
+  __device__ __forceinline__ void c_issue(const EpiCtx& ctx, uint32_t use, int x, int row0) const {
     const uint32_t b = use % kCRing;
     mbar_arrive_expect_tx(&ctx.bars[b], 4096);
-    tma_load_2d(smem_u32(ctx.stg) + b * 4096, &p.tmap_c, smem_u32(&ctx.bars[b]), 2 * j0, row0);
+    tma_load_2d(smem_u32(ctx.stg) + b * 4096, &p.tmap_c, smem_u32(&ctx.bars[b]), x, row0);
   }
 
   __device__ __forceinline__ void read_c_block(uint32_t box, int lane, int blk, float (&v)[32]) const {
@@ -384,12 +421,12 @@ struct DgluPolicy {
       fence_async_shared();  // earlier generic reads of the ring before the async overwrite
       __syncwarp();
       if (ctx.lane == 0 && nown > 0) {
-        // the box of use c_uses was last stored out of kCRing uses ago (kGroups groups per use)
-        bulk_wait_read<(kCRing - 1) * Cfg::kGroups>();
-        c_issue(ctx, c_uses, w.n0 + 32 * ctx.half, row0);
+        // every store out of the ring has read its box (the tile's accumulator is still being
+        // computed, so this wait costs nothing on the critical path)
+        bulk_wait_read<0>();
+        c_issue(ctx, c_uses, use_col(w, ctx.half), row0);
         if (nown > 1) {
-          bulk_wait_read<(kCRing - 2) * Cfg::kGroups>();
-          c_issue(ctx, c_uses + 1, w.n0 + 32 * (ctx.half + kEpiHalves), row0);
+          c_issue(ctx, c_uses + 1, use_col(w, ctx.half + kEpiHalves), row0);
         }
       }
       __syncwarp();
@@ -402,24 +439,26 @@ struct DgluPolicy {
     const int g = w.expert;
     const float alpha_g = __ldg(p.alpha + g);
     const float alpha2 = alpha_g * alpha_g;
-    const float beta_g = __ldg(p.beta + g);
+    const float beta_g = OP == kOpGlu ? __ldg(p.beta + g) : 1.0f;
     const int row0 = w.m0 + ctx.rank * BM + ctx.q * 32;
     const int row = row0 + lane;
     const float pr = __ldg(p.prob + row);
     const int nown = own_chunks(num_chunks(w), half);
     const uint32_t ring = smem_u32(ctx.stg);
     const int gblk = p.gate_first ? 0 : 1;
+    const bool want_amax = p.amax != nullptr;
     float dprob_acc = 0.f;
+    float amx0 = 0.f, amx1 = 0.f;  // running |D| maxima (dGLU: gate, input; dsReLU: amx0)
     bool released = false;
 #pragma unroll 1
     for (int i = 0; i < nown; ++i) {
       const int c = half + i * kEpiHalves;
       const uint32_t u = c_uses + i;
       const uint32_t box = ring + (u % kCRing) * 4096;
-      const int j0 = w.n0 + c * 32;
+      const int x = use_col(w, c);  // first C / D_row column of this use
       uint32_t r[32];
-      tmem_load_32cols(taddr + c * 32, r);
-      if (i == nown - 1) {
+      tmem_load_32cols(taddr + (OP == kOpGlu ? 32 : 64) * c, r);
+      if (OP == kOpGlu && i == nown - 1) {
         rel(lane);
         released = true;
       }
@@ -431,43 +470,96 @@ struct DgluPolicy {
         __syncwarp();
         break;
       }
-      float gv[32], iv[32];
-      read_c_block(box, lane, gblk, gv);
-      read_c_block(box, lane, 1 - gblk, iv);
-      dprob_acc += dglu_math<32>(r, gv, iv, alpha2, beta_g, pr);
-      if constexpr (DS == 2) {  // D_row written back over this lane's own row of the C box
-        stage_block(box, lane, gblk, gv);
-        stage_block(box, lane, 1 - gblk, iv);
-        staging_flush(box, lane, 2 * j0, row0);
-      } else {  // fp32: the gate half, then the input half, each a 32 x 32 box through the C box
-        const int first = 2 * j0, second = 2 * j0 + 32;
-        const bool db = p.dbias_ws != nullptr;
-        stage_block(box, lane, 0, gv);
-        staging_flush(box, lane, p.gate_first ? first : second, row0);
-        // dbias column totals straight from the staged fp32 values (the exact D_row values)
-        const float sg = db ? box_column_sum(box, lane) : 0.f;
-        if (lane == 0) bulk_wait_read<0>();  // the gate half has left the box
-        __syncwarp();
-        stage_block(box, lane, 0, iv);
-        staging_flush(box, lane, p.gate_first ? second : first, row0);
-        if (db) dbias_add(w, j0, lane, sg, box_column_sum(box, lane));
+      if constexpr (OP == kOpGlu) {
+        const int j0 = w.n0 + c * 32;
+        float gv[32], iv[32];
+        read_c_block(box, lane, gblk, gv);
+        read_c_block(box, lane, 1 - gblk, iv);
+        dprob_acc += dglu_math<32>(r, gv, iv, alpha2, beta_g, pr);
+        if (want_amax) {
+          amx0 = absmax32(gv, amx0);
+          amx1 = absmax32(iv, amx1);
+        }
+        if constexpr (DS == 2) {  // D_row written back over this lane's own row of the C box
+          stage_block(box, lane, gblk, gv);
+          stage_block(box, lane, 1 - gblk, iv);
+          staging_flush(box, lane, x, row0);
+        } else {  // fp32: the gate half, then the input half, each a 32 x 32 box through the C box
+          const bool db = p.dbias_ws != nullptr;
+          stage_block(box, lane, 0, gv);
+          staging_flush(box, lane, p.gate_first ? x : x + 32, row0);
+          // dbias column totals straight from the staged fp32 values (the exact D_row values)
+          const float sg = db ? box_column_sum(box, lane) : 0.f;
+          if (lane == 0) bulk_wait_read<0>();  // the gate half has left the box
+          __syncwarp();
+          stage_block(box, lane, 0, iv);
+          staging_flush(box, lane, p.gate_first ? x + 32 : x, row0);
+          if (db) dbias_add(w, j0, lane, sg, box_column_sum(box, lane));
+        }
+        if (DS == 2 && p.dbias_ws != nullptr) dbias_partials(w, j0, lane, gv, iv);
+      } else {
+        // dsReLU on the box's two 32-column blocks: G = alpha acc, D = prob 2 C relu(G),
+        // dprob += C relu(G)^2.  Both blocks of C are read before any result is staged (fp32
+        // results fill the whole box).
+        float c0[32], c1[32];
+        read_c_block(box, lane, 0, c0);
+        read_c_block(box, lane, 1, c1);
+        const float p2 = 2.0f * pr;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float rr = fmaxf(alpha_g * __uint_as_float(r[k]), 0.0f);
+          dprob_acc += c0[k] * rr * rr;
+          c0[k] = p2 * c0[k] * rr;
+        }
+        tmem_load_32cols(taddr + 64 * c + 32, r);
+        if (i == nown - 1) {
+          rel(lane);
+          released = true;
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float rr = fmaxf(alpha_g * __uint_as_float(r[k]), 0.0f);
+          dprob_acc += c1[k] * rr * rr;
+          c1[k] = p2 * c1[k] * rr;
+        }
+        if (want_amax) amx0 = absmax32(c1, absmax32(c0, amx0));
+        if constexpr (DS == 2) {
+          stage_block(box, lane, 0, c0);
+          stage_block(box, lane, 1, c1);
+          staging_flush(box, lane, x, row0);
+        } else {
+          stage_block(box, lane, 0, c0);
+          staging_flush(box, lane, x, row0);
+          if (x + 32 < p.N) {  // a use may end at N after its first half
+            if (lane == 0) bulk_wait_read<0>();  // the first half has left the box
+            __syncwarp();
+            stage_block(box, lane, 0, c1);
+            staging_flush(box, lane, x + 32, row0);
+          }
+        }
       }
-      if (DS == 2 && p.dbias_ws != nullptr) dbias_partials(w, j0, lane, gv, iv);
       if (i + 2 < nown) {  // refill with this warp's use u + 2 the box last used kCRing - 2 uses ago
         __syncwarp();
         if (lane == 0) {
-          bulk_wait_read<(kCRing - 2) * Cfg::kGroups>();  // the stores out of that box have read it
-          c_issue(ctx, u + 2, j0 + 64 * kEpiHalves, row0);
+          bulk_wait_read<0>();  // the stores out of that box (this use's) have read it
+          c_issue(ctx, u + 2, use_col(w, c + 2 * kEpiHalves), row0);
         }
       }
     }
     if (!released) rel(lane);
     c_uses += (uint32_t)nown;
     if (nown > 0) atomicAdd(p.dprob + row, dprob_acc);
+    if (want_amax && nown > 0) {
+      if constexpr (OP == kOpGlu) {
+        amax_flush(g, 2 * g, amx0);
+        amax_flush(g, 2 * g + 1, amx1);
+      } else {
+        amax_flush(g, g, amx0);
+      }
+    }
     if (ctx.q == 0 && half == 0 && lane == 0) log_tile(w, t, ctx.rank);
   }
 
-  // ---------------------------------------------------------------- register path for fp32 C
   __device__ void epilogue_regc(const TileWork& w, long long t, uint32_t taddr, const EpiCtx& ctx,
                                 AccRelease rel) const {
     const int lane = ctx.lane, half = ctx.half;
@@ -481,7 +573,9 @@ struct DgluPolicy {
     const size_t row_off = (size_t)row * 2 * (size_t)p.N;
     const uint32_t stg = smem_u32(ctx.stg);
     const int nchunks = num_chunks(w);
+    const bool want_amax = p.amax != nullptr;
     float dprob_acc = 0.f;
+    float amx0 = 0.f, amx1 = 0.f;
     bool released = false;
 
     uint4 cg[CV], ci[CV];
@@ -501,6 +595,10 @@ struct DgluPolicy {
       unpack_c(cg, gv);
       unpack_c(ci, iv);
       dprob_acc += dglu_math<32>(r, gv, iv, alpha2, beta_g, pr);
+      if (want_amax) {
+        amx0 = absmax32(gv, amx0);
+        amx1 = absmax32(iv, amx1);
+      }
       if constexpr (DS == 2) {  // both 32-column blocks in one 64-column box
         staging_free(lane);
         stage_block(stg, lane, p.gate_first ? 0 : 1, gv);
@@ -514,8 +612,8 @@ struct DgluPolicy {
         fence_async_shared();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&p.tmap_d, stg, p.gate_first ? first : second, row0);
-          tma_store_2d(&p.tmap_d, stg + 4096, p.gate_first ? second : first, row0);
+          store_box(stg, p.gate_first ? first : second, row0);
+          store_box(stg + 4096, p.gate_first ? second : first, row0);
           bulk_commit_group();
         }
       }
@@ -528,28 +626,33 @@ struct DgluPolicy {
     }
     if (!released) rel(lane);
     if (half < nchunks) atomicAdd(p.dprob + row, dprob_acc);
+    if (want_amax && half < nchunks) {
+      amax_flush(g, 2 * g, amx0);
+      amax_flush(g, 2 * g + 1, amx1);
+    }
     if (ctx.q == 0 && half == 0 && lane == 0) log_tile(w, t, ctx.rank);
   }
 
   __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, bool, const EpiCtx& ctx,
                            AccRelease rel) const {
+    static_assert(OP == kOpGlu || Cfg::kTmaC, "the dsReLU epilogue reads C through the TMA ring");
     if constexpr (Cfg::kTmaC) epilogue_tmac(w, t, taddr, ctx, rel);
     else epilogue_regc(w, t, taddr, ctx, rel);
   }
 };
 
-template <int BN, int CS, int DS, bool TMAC, bool PAIR>
+template <int BN, int CS, int DS, bool TMAC, bool PAIR, int OP>
 __global__ void __launch_bounds__(cta_threads(DgluCfg<CS, DS, TMAC, PAIR>::kEpiWarps), 1)
     dglu_bwd_kernel(const __grid_constant__ DgluParams prm) {
-  const DgluPolicy<BN, CS, DS, TMAC, PAIR> pol(prm);
+  const DgluPolicy<BN, CS, DS, TMAC, PAIR, OP> pol(prm);
   persistent_gemm<BN, DgluCfg<CS, DS, TMAC, PAIR>::kStages, PAIR>(pol);
 }
 
-template <int BN, int CS, int DS, bool TMAC, bool PAIR>
+template <int BN, int CS, int DS, bool TMAC, bool PAIR, int OP = kOpGlu>
 static cudaError_t launch_dglu_variant(const DgluParams& prm, int num_sms, cudaStream_t stream) {
   using C = DgluCfg<CS, DS, TMAC, PAIR>;
   constexpr int smem = SmemLayout<PAIR ? BN / 2 : BN, C::kStages, C::kEpiWarps, C::kStgBytes, num_acc(BN)>::DYN_BYTES;
-  auto kern = dglu_bwd_kernel<BN, CS, DS, TMAC, PAIR>;
+  auto kern = dglu_bwd_kernel<BN, CS, DS, TMAC, PAIR, OP>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   static int max_units = 0;  // co-resident CTAs (pairs) of this variant, asked once
@@ -557,9 +660,10 @@ static cudaError_t launch_dglu_variant(const DgluParams& prm, int num_sms, cudaS
                            stream);
 }
 
-// Checks the device-resident arguments and builds the per-expert weight maps.
+// Checks the device-resident arguments, builds the per-expert weight maps and zeroes amax.
 __global__ void dglu_prep_kernel(const int32_t* offsets, int L, long long M, const int64_t* b_ptrs,
-                                 const __grid_constant__ CUtensorMap tmpl, CUtensorMap* maps, int* status) {
+                                 const __grid_constant__ CUtensorMap tmpl, CUtensorMap* maps, int* status,
+                                 float* amax, int n_amax) {
   bool bad_off = false, bad_ptr = false;
   for (int e = threadIdx.x; e < L; e += blockDim.x) {
     const int prev = e ? offsets[e - 1] : 0;
@@ -579,7 +683,10 @@ __global__ void dglu_prep_kernel(const int32_t* offsets, int L, long long M, con
     status[2] = 0;
     status[3] = 0;
   }
-  if (any_off || any_ptr || b_ptrs == nullptr) return;
+  if (any_off || any_ptr) return;  // outputs stay untouched
+  if (amax != nullptr)
+    for (int i = threadIdx.x; i < n_amax; i += blockDim.x) amax[i] = 0.0f;
+  if (b_ptrs == nullptr) return;
   const uint4* src = reinterpret_cast<const uint4*>(&tmpl);
   for (int e = threadIdx.x; e < L; e += blockDim.x) {
     uint4* dst = reinterpret_cast<uint4*>(maps + e);
@@ -597,8 +704,31 @@ __global__ void dbias_finalize_kernel(const float* ws, __nv_bfloat16* dbias, lon
     dbias[i] = __float2bfloat16_rn(__bfloat162float(dbias[i]) + ws[i]);
 }
 
-cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
-  const mgg_dglu_bwd_args& a = *Lc.args;
+// What both grouped-GEMM epilogue calls pass to the launch (from mgg_dglu_bwd_args or
+// mgg_dsrelu_bwd_args).
+struct EpiCall {
+  int64_t M, K, N, L;            // N: compact width (dGLU) or columns of C / D_row (dsReLU)
+  const int64_t* b_ptrs;
+  int b_major;
+  const int32_t* offsets;
+  const float* alpha;
+  const float* beta;             // dGLU only
+  const float* prob;
+  const void* c;
+  float* dprob;
+  void* dbias;                   // dGLU only
+  float* amax;
+  bool d_col;
+  void* workspace;
+  int32_t* tile_log;
+  int64_t tile_log_capacity;
+  int sched, c_dtype, d_dtype;
+  int act, geglu_filter, gate_first;
+  float situ_beta1, situ_beta2;
+};
+
+template <int OP>
+static cudaError_t launch_epi_gemm(const DgluLaunch& Lc, const EpiCall& a, cudaStream_t stream) {
   constexpr int BN = kDgluTileN;
 
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -606,8 +736,8 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
   CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(ws + kWsHeaderBytes);
   float* dbias_ws = reinterpret_cast<float*>(ws + kWsHeaderBytes + kTmapBytes * (size_t)a.L);
 
-  dglu_prep_kernel<<<1, 1024, 0, stream>>>(a.padded_offsets, (int)a.L, (long long)a.M, a.b_ptrs, Lc.tmap_b, maps,
-                                          status);
+  dglu_prep_kernel<<<1, 1024, 0, stream>>>(a.offsets, (int)a.L, (long long)a.M, a.b_ptrs, Lc.tmap_b, maps, status,
+                                          a.amax, (int)(a.L * (OP == kOpGlu ? 2 : 1)));
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (a.dbias != nullptr) {
@@ -626,8 +756,11 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     prm.tmap_b = Lc.tmap_b;
     prm.tmap_d = Lc.tmap_d;
     prm.tmap_c = Lc.tmap_c;
+    prm.tmap_dcol = Lc.tmap_dcol;
+    prm.has_dcol = a.d_col ? 1 : 0;
+    prm.amax = a.amax;
     prm.b_maps = a.b_ptrs != nullptr ? maps : nullptr;
-    prm.offsets = a.padded_offsets;
+    prm.offsets = a.offsets;
     prm.alpha = a.alpha;
     prm.beta = a.beta;
     prm.prob = a.prob;
@@ -660,7 +793,12 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
 
     const int cs = a.c_dtype == MGG_FP32 ? 4 : 2, ds = a.d_dtype == MGG_FP32 ? 4 : 2;
     const int n = Lc.num_sms;
-    if (Lc.pair) {  // pairs take the C ring whenever C is 16-bit
+    if constexpr (OP == kOpSrelu) {  // 16-bit C through the TMA ring (the host checked C's dtype)
+      if (Lc.pair) err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, true, OP>(prm, n, stream)
+                                 : launch_dglu_variant<BN, 2, 4, true, true, OP>(prm, n, stream);
+      else err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, false, OP>(prm, n, stream)
+                         : launch_dglu_variant<BN, 2, 4, true, false, OP>(prm, n, stream);
+    } else if (Lc.pair) {  // pairs take the C ring whenever C is 16-bit
       if (cs == 2) err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, true>(prm, n, stream)
                                  : launch_dglu_variant<BN, 2, 4, true, true>(prm, n, stream);
       else err = ds == 2 ? launch_dglu_variant<BN, 4, 2, false, true>(prm, n, stream)
@@ -685,6 +823,21 @@ cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
     err = cudaGetLastError();
   }
   return err;
+}
+
+cudaError_t launch_dglu_bwd(const DgluLaunch& Lc, cudaStream_t stream) {
+  const mgg_dglu_bwd_args& a = *Lc.args;
+  EpiCall e{a.M, a.K, a.N, a.L, a.b_ptrs, a.b_major, a.padded_offsets, a.alpha, a.beta, a.prob, a.c, a.dprob,
+            a.dbias, a.amax, a.d_col != nullptr, a.workspace, a.tile_log, a.tile_log_capacity, a.sched, a.c_dtype,
+            a.d_dtype, a.act, a.geglu_filter, a.gate_first, a.situ_beta1, a.situ_beta2};
+  return launch_epi_gemm<kOpGlu>(Lc, e, stream);
+}
+
+cudaError_t launch_dsrelu_bwd(const DgluLaunch& Lc, const mgg_dsrelu_bwd_args& a, cudaStream_t stream) {
+  EpiCall e{a.M, a.K, a.N, a.L, a.b_ptrs, a.b_major, a.padded_offsets, a.alpha, nullptr, a.prob, a.c, a.dprob,
+            nullptr, a.amax, a.d_col != nullptr, a.workspace, a.tile_log, a.tile_log_capacity, a.sched, a.c_dtype,
+            a.d_dtype, MGG_ACT_DSWIGLU, MGG_FILTER_VALUE, 1, 0.0f, 0.0f};
+  return launch_epi_gemm<kOpSrelu>(Lc, e, stream);
 }
 
 // ------------------------------------------------------------------------------------

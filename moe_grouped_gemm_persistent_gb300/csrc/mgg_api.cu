@@ -133,10 +133,54 @@ mgg_status validate_dglu(const mgg_dglu_bwd_args& a) {
   if (a.b && !aligned16(a.b)) return fail(MGG_ERR_VALUE, "b must be 16-byte aligned");
   if (a.b_ptrs && !aligned16(a.b_ptrs)) return fail(MGG_ERR_VALUE, "b_ptrs must be 16-byte aligned");
   if (a.dbias && !aligned16(a.dbias)) return fail(MGG_ERR_VALUE, "dbias must be 16-byte aligned");
+  if (a.d_col && !aligned16(a.d_col)) return fail(MGG_ERR_VALUE, "d_col must be 16-byte aligned");
+  if (a.amax && !aligned16(a.amax)) return fail(MGG_ERR_VALUE, "amax must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(a.workspace) & 255u) != 0)
     return fail(MGG_ERR_VALUE, "workspace must be 256-byte aligned");
   if ((size_t)a.workspace_bytes < mgg_dglu_bwd_workspace_size(a.L, a.N))
     return fail(MGG_ERR_VALUE, "workspace too small: need " + std::to_string(mgg_dglu_bwd_workspace_size(a.L, a.N)) +
+                                   " bytes");
+  if (a.tile_log != nullptr) {
+    if (!aligned16(a.tile_log)) return fail(MGG_ERR_VALUE, "tile_log must be 16-byte aligned");
+    if (a.tile_log_capacity < mgg_dglu_bwd_num_tiles(a.M, a.N))
+      return fail(MGG_ERR_VALUE, "tile_log_capacity smaller than the number of tiles");
+  }
+  return MGG_OK;
+}
+
+// ---------------------------------------------------------------- dsReLU validation
+mgg_status validate_dsrelu(const mgg_dsrelu_bwd_args& a) {
+  if (a.L < 1 || a.L > 1024) return fail(MGG_ERR_VALUE, "expert count L must be in [1, 1024]");
+  if (a.M < 0 || a.M % 256 != 0) return fail(MGG_ERR_VALUE, "M (padded rows) must be a non-negative multiple of 256");
+  if (a.M > (int64_t)1 << 30) return fail(MGG_ERR_UNSUPPORTED, "M above 2^30 rows is not supported");
+  if (a.K < 8 || a.K % 8 != 0) return fail(MGG_ERR_VALUE, "K must be a positive multiple of 8 (16-byte rows)");
+  if (a.K > (int64_t)1 << 24) return fail(MGG_ERR_UNSUPPORTED, "K above 2^24 is not supported");
+  if (a.N < 32 || a.N % 32 != 0) return fail(MGG_ERR_VALUE, "N must be a positive multiple of 32");
+  if (a.N > (int64_t)1 << 24) return fail(MGG_ERR_UNSUPPORTED, "N above 2^24 is not supported");
+  if ((a.b == nullptr) == (a.b_ptrs == nullptr))
+    return fail(MGG_ERR_VALUE, "exactly one of the dense weights b and the pointer array b_ptrs must be given");
+  if (a.b_major != MGG_MAJOR_K && a.b_major != MGG_MAJOR_MN) return fail(MGG_ERR_VALUE, "b_major must be K or MN");
+  if (a.b != nullptr && a.b_major != MGG_MAJOR_K) return fail(MGG_ERR_VALUE, "dense weights (N, K, L) are K-major");
+  if (!valid_dtype(a.c_dtype) || !valid_dtype(a.d_dtype)) return fail(MGG_ERR_VALUE, "c_dtype/d_dtype out of range");
+  if (a.c_dtype == MGG_FP32) return fail(MGG_ERR_UNSUPPORTED, "the dsReLU epilogue takes a 16-bit C (bf16 or fp16)");
+  if (a.sched != MGG_SCHED_STATIC && a.sched != MGG_SCHED_DYNAMIC) return fail(MGG_ERR_VALUE, "sched out of range");
+  if (a.cta_mode != MGG_CTA_AUTO && a.cta_mode != MGG_CTA_SINGLE && a.cta_mode != MGG_CTA_PAIR)
+    return fail(MGG_ERR_VALUE, "cta_mode out of range");
+  if (a.reserved != 0) return fail(MGG_ERR_VALUE, "reserved field must be 0");
+  const void* req[] = {a.a, a.c, a.padded_offsets, a.alpha, a.prob, a.dprob, a.d_row, a.workspace};
+  const char* names[] = {"a", "c", "padded_offsets", "alpha", "prob", "dprob", "d_row", "workspace"};
+  for (int i = 0; i < 8; ++i) {
+    if (req[i] == nullptr) return fail(MGG_ERR_VALUE, std::string(names[i]) + " must not be NULL");
+    if (!aligned16(req[i])) return fail(MGG_ERR_VALUE, std::string(names[i]) + " must be 16-byte aligned");
+  }
+  if (a.b && !aligned16(a.b)) return fail(MGG_ERR_VALUE, "b must be 16-byte aligned");
+  if (a.b_ptrs && !aligned16(a.b_ptrs)) return fail(MGG_ERR_VALUE, "b_ptrs must be 16-byte aligned");
+  if (a.d_col && !aligned16(a.d_col)) return fail(MGG_ERR_VALUE, "d_col must be 16-byte aligned");
+  if (a.amax && !aligned16(a.amax)) return fail(MGG_ERR_VALUE, "amax must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(a.workspace) & 255u) != 0)
+    return fail(MGG_ERR_VALUE, "workspace must be 256-byte aligned");
+  if ((size_t)a.workspace_bytes < mgg_dsrelu_bwd_workspace_size(a.L))
+    return fail(MGG_ERR_VALUE, "workspace too small: need " + std::to_string(mgg_dsrelu_bwd_workspace_size(a.L)) +
                                    " bytes");
   if (a.tile_log != nullptr) {
     if (!aligned16(a.tile_log)) return fail(MGG_ERR_VALUE, "tile_log must be 16-byte aligned");
@@ -224,6 +268,8 @@ int mgg_abi_version(void) { return MGG_ABI_VERSION; }
 
 size_t mgg_sizeof_dglu_bwd_args(void) { return sizeof(mgg_dglu_bwd_args); }
 
+size_t mgg_sizeof_dsrelu_bwd_args(void) { return sizeof(mgg_dsrelu_bwd_args); }
+
 size_t mgg_sizeof_wgrad_args(void) { return sizeof(mgg_wgrad_args); }
 
 const char* mgg_last_error(void) { return g_err.c_str(); }
@@ -245,6 +291,11 @@ const char* mgg_status_string(int s) {
 size_t mgg_dglu_bwd_workspace_size(int64_t L, int64_t N) {
   if (L < 0 || N < 0) return 0;
   return round_up(kWsHeaderBytes + kTmapBytes * (size_t)L + sizeof(float) * (size_t)L * 2 * (size_t)N, 256);
+}
+
+size_t mgg_dsrelu_bwd_workspace_size(int64_t L) {
+  if (L < 0) return 0;
+  return round_up(kWsHeaderBytes + kTmapBytes * (size_t)L, 256);
 }
 
 size_t mgg_wgrad_workspace_size(int64_t L) {
@@ -273,6 +324,70 @@ void mgg_wgrad_tile_shape(int64_t inter, int32_t* tile_m, int32_t* tile_n) {
   if (tile_n) *tile_n = wgrad_tile_n(inter);
 }
 
+}  // extern "C"
+
+namespace mgg {
+namespace {
+
+// Maps of one grouped-GEMM epilogue call: A (M, K); B (N, K) per expert (dense, or the
+// discrete template); C and D_row / D_col of `cd_cols` columns (2N for dGLU, N for dsReLU).
+mgg_status build_epi_maps(DgluLaunch& Lc, const void* a_ptr, const void* b, const int64_t* b_ptrs, int b_major,
+                          const void* c, int c_dtype, void* d_row, void* d_col, int d_dtype, int64_t M_, int64_t K_,
+                          int64_t N_, int64_t L_, uint64_t cd_cols) {
+  mgg_status s;
+  const uint32_t b_rows = (uint32_t)(Lc.pair ? kDgluTileN / 2 : kDgluTileN);  // B rows one CTA loads
+  const uint64_t M = (uint64_t)(M_ > 0 ? M_ : 256), K = (uint64_t)K_, N = (uint64_t)N_, L = (uint64_t)L_;
+  {
+    const uint64_t dims[2] = {K, M}, strides[1] = {K * 2};
+    const uint32_t box[2] = {64, 128};
+    if ((s = encode_bf16(&Lc.tmap_a, a_ptr, 2, dims, strides, box, "A")) != MGG_OK) return s;
+  }
+  if (b != nullptr) {
+    const uint64_t dims[3] = {K, N, L}, strides[2] = {K * 2, N * K * 2};
+    const uint32_t box[3] = {64, b_rows, 1};
+    if ((s = encode_bf16(&Lc.tmap_b, b, 3, dims, strides, box, "dense B")) != MGG_OK) return s;
+  } else if (b_major == MGG_MAJOR_K) {
+    const uint64_t dims[2] = {K, N}, strides[1] = {K * 2};
+    const uint32_t box[2] = {64, b_rows};
+    if ((s = encode_bf16(&Lc.tmap_b, a_ptr, 2, dims, strides, box, "discrete K-major B")) != MGG_OK) return s;
+  } else {
+    // N a multiple of 64: a 3-D template of 64-column blocks (dims {64, K, N/64}, strides
+    // {N*2, 128} bytes) so one box fills a ring slot; else one 64 x 64 box per 64 columns
+    (void)b_ptrs;
+    if (N % 64 == 0) {
+      const uint64_t dims[3] = {64, K, N / 64}, strides[2] = {N * 2, 128};
+      const uint32_t box[3] = {64, 64, b_rows / 64};
+      const std::string saved = g_err;
+      Lc.b_blocked = encode_bf16(&Lc.tmap_b, a_ptr, 3, dims, strides, box, "discrete N-major B (blocked)") == MGG_OK;
+      if (!Lc.b_blocked) g_err = saved;
+    }
+    if (!Lc.b_blocked) {
+      const uint64_t dims[2] = {N, K}, strides[1] = {N * 2};
+      const uint32_t box[2] = {64, 64};
+      if ((s = encode_bf16(&Lc.tmap_b, a_ptr, 2, dims, strides, box, "discrete N-major B")) != MGG_OK) return s;
+    }
+  }
+  {  // D_row / D_col (M, cd_cols): 32-row boxes of one 128-byte row of columns
+    const uint64_t esz = d_dtype == MGG_FP32 ? 4 : 2;
+    const uint64_t dims[2] = {cd_cols, M}, strides[1] = {cd_cols * esz};
+    const uint32_t box[2] = {(uint32_t)(128 / esz), 32};
+    if ((s = encode_map(&Lc.tmap_d, d_dtype, d_row, 2, dims, strides, box, "D_row")) != MGG_OK) return s;
+    if (d_col != nullptr && (s = encode_map(&Lc.tmap_dcol, d_dtype, d_col, 2, dims, strides, box, "D_col")) != MGG_OK)
+      return s;
+  }
+  if (c_dtype != MGG_FP32) {  // C (M, cd_cols): 32-row boxes of 64 columns
+    const uint64_t dims[2] = {cd_cols, M}, strides[1] = {cd_cols * 2};
+    const uint32_t box[2] = {64, 32};
+    if ((s = encode_map(&Lc.tmap_c, c_dtype, c, 2, dims, strides, box, "C")) != MGG_OK) return s;
+  }
+  return MGG_OK;
+}
+
+}  // namespace
+}  // namespace mgg
+
+extern "C" {
+
 mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream) {
   g_err.clear();
   if (args == nullptr) return fail(MGG_ERR_VALUE, "args is NULL");
@@ -288,49 +403,31 @@ mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream) {
   Lc.num_sms = dev.num_sms;
   Lc.tile_n = kDgluTileN;
   Lc.pair = dglu_pair(a);
-  const uint32_t b_rows = (uint32_t)(Lc.pair ? kDgluTileN / 2 : kDgluTileN);  // B rows one CTA loads
-  const uint64_t M = (uint64_t)(a.M > 0 ? a.M : 256), K = (uint64_t)a.K, N = (uint64_t)a.N, L = (uint64_t)a.L;
-  {
-    const uint64_t dims[2] = {K, M}, strides[1] = {K * 2};
-    const uint32_t box[2] = {64, 128};
-    if ((s = encode_bf16(&Lc.tmap_a, a.a, 2, dims, strides, box, "A")) != MGG_OK) return s;
-  }
-  if (a.b != nullptr) {
-    const uint64_t dims[3] = {K, N, L}, strides[2] = {K * 2, N * K * 2};
-    const uint32_t box[3] = {64, b_rows, 1};
-    if ((s = encode_bf16(&Lc.tmap_b, a.b, 3, dims, strides, box, "dense B")) != MGG_OK) return s;
-  } else if (a.b_major == MGG_MAJOR_K) {
-    const uint64_t dims[2] = {K, N}, strides[1] = {K * 2};
-    const uint32_t box[2] = {64, b_rows};
-    if ((s = encode_bf16(&Lc.tmap_b, a.a, 2, dims, strides, box, "discrete K-major B")) != MGG_OK) return s;
-  } else {
-    // N a multiple of 64: a 3-D template of 64-column blocks (dims {64, K, N/64}, strides
-    // {N*2, 128} bytes) so one box fills a ring slot; else one 64 x 64 box per 64 columns
-    if (N % 64 == 0) {
-      const uint64_t dims[3] = {64, K, N / 64}, strides[2] = {N * 2, 128};
-      const uint32_t box[3] = {64, 64, b_rows / 64};
-      const std::string saved = g_err;
-      Lc.b_blocked = encode_bf16(&Lc.tmap_b, a.a, 3, dims, strides, box, "discrete N-major B (blocked)") == MGG_OK;
-      if (!Lc.b_blocked) g_err = saved;
-    }
-    if (!Lc.b_blocked) {
-      const uint64_t dims[2] = {N, K}, strides[1] = {N * 2};
-      const uint32_t box[2] = {64, 64};
-      if ((s = encode_bf16(&Lc.tmap_b, a.a, 2, dims, strides, box, "discrete N-major B")) != MGG_OK) return s;
-    }
-  }
-  {  // D_row (M, 2N): 32-row boxes of one 128-byte row of columns
-    const uint64_t esz = a.d_dtype == MGG_FP32 ? 4 : 2;
-    const uint64_t dims[2] = {2 * N, M}, strides[1] = {2 * N * esz};
-    const uint32_t box[2] = {(uint32_t)(128 / esz), 32};
-    if ((s = encode_map(&Lc.tmap_d, a.d_dtype, a.d_row, 2, dims, strides, box, "D_row")) != MGG_OK) return s;
-  }
-  if (a.c_dtype != MGG_FP32) {  // C (M, 2N): 32-row boxes of 64 columns (one gate + one input block)
-    const uint64_t dims[2] = {2 * N, M}, strides[1] = {2 * N * 2};
-    const uint32_t box[2] = {64, 32};
-    if ((s = encode_map(&Lc.tmap_c, a.c_dtype, a.c, 2, dims, strides, box, "C")) != MGG_OK) return s;
-  }
+  if ((s = build_epi_maps(Lc, a.a, a.b, a.b_ptrs, a.b_major, a.c, a.c_dtype, a.d_row, a.d_col, a.d_dtype, a.M, a.K,
+                          a.N, a.L, 2 * (uint64_t)a.N)) != MGG_OK)
+    return s;
   return from_cuda(launch_dglu_bwd(Lc, static_cast<cudaStream_t>(stream)), "mgg_dglu_bwd launch");
+}
+
+mgg_status mgg_dsrelu_bwd(const mgg_dsrelu_bwd_args* args, void* stream) {
+  g_err.clear();
+  if (args == nullptr) return fail(MGG_ERR_VALUE, "args is NULL");
+  const mgg_dsrelu_bwd_args& a = *args;
+  mgg_status s = validate_dsrelu(a);
+  if (s != MGG_OK) return s;
+  DevInfo dev;
+  if ((s = check_device(&dev)) != MGG_OK) return s;
+
+  DgluLaunch Lc;
+  memset(&Lc, 0, sizeof(Lc));
+  Lc.args = nullptr;
+  Lc.num_sms = dev.num_sms;
+  Lc.tile_n = kDgluTileN;
+  Lc.pair = a.cta_mode != MGG_CTA_SINGLE;  // AUTO: pairs, as for the dGLU dgrad
+  if ((s = build_epi_maps(Lc, a.a, a.b, a.b_ptrs, a.b_major, a.c, a.c_dtype, a.d_row, a.d_col, a.d_dtype, a.M, a.K,
+                          a.N, a.L, (uint64_t)a.N)) != MGG_OK)
+    return s;
+  return from_cuda(launch_dsrelu_bwd(Lc, a, static_cast<cudaStream_t>(stream)), "mgg_dsrelu_bwd launch");
 }
 
 mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {

@@ -22,7 +22,8 @@ struct DgluLaunch {
   CUtensorMap tmap_b;  // dense 3-D map, or the per-expert template (discrete)
   CUtensorMap tmap_d;  // D_row store map
   CUtensorMap tmap_c;  // C load map (16-bit C only)
-  const mgg_dglu_bwd_args* args;
+  CUtensorMap tmap_dcol;  // D_col store map (when requested)
+  const mgg_dglu_bwd_args* args;  // null for mgg_dsrelu_bwd
   int num_sms;
   int tile_n;
   bool pair;       // 256-row tiles on CTA pairs (B maps load half a tile's columns)
@@ -45,6 +46,7 @@ struct WgradLaunch {
 
 // Launchers (queue the prep kernel, the persistent kernel and finalisers on `stream`).
 cudaError_t launch_dglu_bwd(const DgluLaunch& L, cudaStream_t stream);
+cudaError_t launch_dsrelu_bwd(const DgluLaunch& L, const mgg_dsrelu_bwd_args& a, cudaStream_t stream);
 cudaError_t launch_wgrad(const WgradLaunch& L, cudaStream_t stream);
 
 // Test hook: copies `tmpl` into `out` on the device and replaces address / dim0 / stride of

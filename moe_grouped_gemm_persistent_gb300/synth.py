@@ -80,7 +80,7 @@ class DgluSpec:
     K: int
     N: int
     counts: np.ndarray          # per-expert rows (multiples of 256)
-    act: str = "dswiglu"        # "dswiglu" | "dgeglu"
+    act: str = "dswiglu"        # "dswiglu" | "dgeglu" | "dsituglu" | "dsrelu" (C, D_row (M, N))
     b_mode: str = "dense"       # "dense" | "discrete"
     b_major: str = "k"          # "k" | "n" (discrete only)
     c_dtype: str = "bf16"
@@ -163,6 +163,10 @@ def workload_specs(name: str):
         counts = dgrad_counts(0, 8, 32768, None)
         return DgluSpec("mixtral_situ", L=8, K=4096, N=14336, counts=counts, b_std=0.02, act="dsituglu",
                         c_std=4.0), None
+    # the Mixtral-like layer with the dsReLU backward (squared-ReLU experts: C, D_row (M, N))
+    if name == "dsrelu":
+        counts = dgrad_counts(0, 8, 32768, None)
+        return DgluSpec("dsrelu", L=8, K=4096, N=14336, counts=counts, b_std=0.02, act="dsrelu"), None
     # reduced copies of the layers above, sized for profiler captures (a few GB on the device)
     if name == "mixtral_s":
         counts = dgrad_counts(0, 2, 8192, None)
@@ -217,8 +221,8 @@ def make_dglu_inputs(spec: DgluSpec, device="cpu"):
 
     Returns a dict: a (M,K) bf16; b (L,N,K) bf16 dense or list of L per-expert matrices
     (each (N,K) K-major, or an (K,N) row-major tensor whose transpose view is the
-    n-major (N,K) matrix); c (M,2N); alpha, beta (L,) fp32 ~U(0.5,1.5); prob (M,)
-    fp32 ~U(0,1); padded_offsets (L,) int32.
+    n-major (N,K) matrix); c (M,2N), or (M,N) for "dsrelu"; alpha, beta (L,) fp32 ~U(0.5,1.5);
+    prob (M,) fp32 ~U(0,1); padded_offsets (L,) int32.
     """
     torch = _torch()
     gen = torch.Generator(device=device)
@@ -236,7 +240,7 @@ def make_dglu_inputs(spec: DgluSpec, device="cpu"):
             else:
                 # n-major (N,K): element (n,k) at k*N + n -> a row-major (K,N) buffer
                 b.append(_normal(gen, (K, N), spec.b_std, bf16, device))
-    c = _normal(gen, (M, 2 * N), spec.c_std, torch_dtype(spec.c_dtype), device)
+    c = _normal(gen, (M, N if spec.act == "dsrelu" else 2 * N), spec.c_std, torch_dtype(spec.c_dtype), device)
     alpha = _uniform(gen, (L,), 0.5, 1.5, device)
     beta = _uniform(gen, (L,), 0.5, 1.5, device)
     prob = _uniform(gen, (M,), 0.0, 1.0, device)

@@ -39,13 +39,15 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_struct_layouts_match_library(lib):
-    assert lib.mgg_abi_version() == 3
+    assert lib.mgg_abi_version() == 4
     assert lib.mgg_sizeof_dglu_bwd_args() == ctypes.sizeof(_lib.DgluBwdArgs)
+    assert lib.mgg_sizeof_dsrelu_bwd_args() == ctypes.sizeof(_lib.DsreluBwdArgs)
     assert lib.mgg_sizeof_wgrad_args() == ctypes.sizeof(_lib.WgradArgs)
 
 
 def test_sizes_and_tile_counts(lib):
     assert lib.mgg_dglu_bwd_workspace_size(4, 128) == 256 + 4 * 128 + 4 * 256 * 4
+    assert lib.mgg_dsrelu_bwd_workspace_size(4) == 768  # 256-byte header + 4 tensor maps of 128 B
     assert lib.mgg_wgrad_workspace_size(64) % 256 == 0
     assert lib.mgg_wgrad_workspace_size(64) >= 256 + 3 * 64 * 128 + 64 * 4
     assert lib.mgg_dglu_bwd_num_tiles(1024, 128) == 8
@@ -67,6 +69,17 @@ def dglu_args(**over):
         setattr(a, f, FAKE)
     a.workspace_bytes = 1 << 20
     a.gate_first = 1
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def dsrelu_args(**over):
+    a = _lib.DsreluBwdArgs()
+    a.M, a.K, a.N, a.L = 1024, 256, 128, 4
+    for f in ("a", "b", "c", "padded_offsets", "alpha", "prob", "dprob", "d_row", "workspace"):
+        setattr(a, f, FAKE)
+    a.workspace_bytes = 1 << 20
     for k, v in over.items():
         setattr(a, k, v)
     return a
@@ -122,3 +135,20 @@ def test_valid_args_without_device_report_arch(lib):
         pytest.skip("a GPU is present")
     assert lib.mgg_dglu_bwd(dglu_args(), None) == _lib.MGG_ERR_ARCH
     assert lib.mgg_wgrad(wgrad_args(), None) == _lib.MGG_ERR_ARCH
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(L=0), 1), (dict(M=1000), 1), (dict(K=100), 1), (dict(N=48), 1), (dict(b_ptrs=FAKE), 1), (dict(b=None), 1),
+    (dict(b_major=1), 1), (dict(c_dtype=2), 2), (dict(c_dtype=7), 1), (dict(d_dtype=-1), 1), (dict(a=FAKE + 8), 1),
+    (dict(c=None), 1), (dict(d_col=FAKE + 4), 1), (dict(amax=FAKE + 4), 1), (dict(workspace_bytes=512), 1),
+    (dict(workspace=FAKE + 16), 1), (dict(sched=3), 1), (dict(cta_mode=5), 1), (dict(reserved=1), 1),
+])
+def test_dsrelu_validation_rejects_before_launch(lib, over, expect):
+    st = lib.mgg_dsrelu_bwd(dsrelu_args(**over), None)
+    assert st == expect, lib.mgg_last_error()
+    assert lib.mgg_last_error()
+
+
+def test_dglu_validation_of_new_outputs(lib):
+    assert lib.mgg_dglu_bwd(dglu_args(d_col=FAKE + 8), None) == 1
+    assert lib.mgg_dglu_bwd(dglu_args(amax=FAKE + 4), None) == 1
