@@ -30,13 +30,18 @@ template <int CS, int DS, bool TMAC, bool PAIR>
 struct DgluCfg {
   static constexpr bool kTmaC = TMAC && CS == 2;
   static constexpr int kEpiWarps = 8;
-  static constexpr int kCRing = 2;  // C boxes per warp (TMA path)
+  // C boxes per warp (TMA path).  Three boxes would let a refill wait for stores a use older, but
+  // cost a pair one of its five operand stages, which measured 5-10% slower on every shape.
+  static constexpr int kCRing = 2;
+  // bulk groups one use commits on the TMA path: 16-bit D leaves in one store, fp32 D in two
+  // (always both: a dsReLU use that ends at N after its first half commits an empty second group)
+  static constexpr int kGroups = DS == 4 ? 2 : 1;
   // TMA path: the C ring (results leave through the consumed box); register path: D staging
   static constexpr int kStgBytes = kTmaC ? kCRing * 4096 : (DS == 4 ? 8192 : 4096);
   static constexpr int kStages = max_stages(PAIR ? kDgluTileN / 2 : kDgluTileN, kEpiWarps, kStgBytes,
                                             num_acc(kDgluTileN), 6);
   static_assert(kStages >= 3, "operand ring too shallow");
-  static_assert(!kTmaC || kCRing == 2, "the ring refill waits for all stores of the consumed box");
+  static_assert(kCRing == 2, "the C-ring waits are written for any depth, measured and tested at 2");
 };
 
 struct DgluParams {
@@ -387,7 +392,8 @@ struct DgluPolicy {
   // Ring of kCRing 4 KB boxes per warp: box u % kCRing holds rows [row0, row0+32) x C columns
   // [2*j0, 2*j0+64) (the gate and the input block of compact chunk j0).  Use u + 2 is loaded when
   // use u is done; the results overwrite the consumed box and leave by bulk stores (16-bit D in
-  // one, fp32 D as two halves), so a box is reloaded only once those stores have read it.
+  // one group, fp32 D as two halves in two), so a box is reloaded only once those stores have
+  // read it: with 2 boxes that is the use just finished, with 3 the one before it.
   __device__ __forceinline__ void c_issue(const EpiCtx& ctx, uint32_t use, int x, int row0) const {
     const uint32_t b = use % kCRing;
     mbar_arrive_expect_tx(&ctx.bars[b], 4096);
@@ -535,13 +541,16 @@ struct DgluPolicy {
             __syncwarp();
             stage_block(box, lane, 0, c1);
             staging_flush(box, lane, x + 32, row0);
+          } else if (lane == 0) {
+            bulk_commit_group();  // an empty group keeps kGroups groups per use
           }
         }
       }
       if (i + 2 < nown) {  // refill with this warp's use u + 2 the box last used kCRing - 2 uses ago
         __syncwarp();
         if (lane == 0) {
-          bulk_wait_read<0>();  // the stores out of that box (this use's) have read it
+          // the stores out of that box have read it (at most the later uses' groups still read)
+          bulk_wait_read<(kCRing - 2) * Cfg::kGroups>();
           c_issue(ctx, u + 2, use_col(w, c + 2 * kEpiHalves), row0);
         }
       }
