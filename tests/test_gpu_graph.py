@@ -1,4 +1,4 @@
-"""CUDA-graph replay of the two ABI calls with caller-owned workspaces.
+"""CUDA-graph replay of the ABI calls (dGLU dgrad, dsReLU dgrad, wgrad) with caller-owned workspaces.
 
 The pages' wgrad API lets callers keep a descriptor workspace alive for CUDA Graph replay
 ("Block-scaled contract"), and the wgrad class API accepts later calls with a different
@@ -49,6 +49,14 @@ def _check(spec_d, spec_w, x, y, d_row, dprob, out):
         assert rel_fro(to_np(out[e].cpu()), wref[e]) <= TOL["fp32"], e
 
 
+def _check_srelu(x, c_s, d_s, dprob_s, amax_s):
+    ref = oracle.dsrelu_bwd(to_np(x["a"]), lambda g: to_np(x["b"][g]), to_np(c_s.cpu()), x["padded_offsets"].numpy(),
+                            x["alpha"].numpy(), x["prob"].numpy())
+    assert rel_fro(to_np(d_s.cpu()), ref["d_row"]) <= TOL["bf16"]
+    assert rel_fro(to_np(dprob_s.cpu()), ref["dprob"]) <= TOL_DPROB
+    np.testing.assert_allclose(amax_s.cpu().numpy(), ref["amax"], rtol=2e-3, atol=0)
+
+
 @pytest.mark.parametrize("sched,cta", [("static", "single"), ("dynamic", "single"), ("dynamic", "pair")])
 def test_graph_replay_with_new_values_and_new_offsets(dev, sched, cta):
     counts = np.array([512, 0, 256, 768], dtype=np.int64)
@@ -64,8 +72,18 @@ def test_graph_replay_with_new_values_and_new_offsets(dev, sched, cta):
     ws_d = api.new_workspace(api.dglu_bwd_workspace_size(L, N), dev)
     ws_w = api.new_workspace(api.wgrad_workspace_size(L), dev)
     d, w = bufs["d"], bufs["w"]
+    # a dsReLU call on the same rows (C (M, N) drawn once; its weights are the dGLU call's)
+    c_s = torch.randn(M, N, generator=torch.Generator().manual_seed(17)).to(torch.bfloat16).to(dev)
+    d_s = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    dprob_s = torch.zeros(M, dtype=torch.float32, device=dev)
+    amax_s = torch.empty(L, dtype=torch.float32, device=dev)
+    ws_s = api.new_workspace(api.dsrelu_bwd_workspace_size(L), dev)
 
     def step(stream):
+        dprob_s.zero_()
+        api.dsrelu_bwd(a=d["a"], b=d["b"], c=c_s, padded_offsets=d["padded_offsets"], alpha=d["alpha"],
+                       prob=d["prob"], dprob=dprob_s, d_row=d_s, amax=amax_s, workspace=ws_s, sched=sched,
+                       stream=stream, cta=cta)
         dprob.zero_()
         api.dglu_bwd(a=d["a"], b=d["b"], c=d["c"], padded_offsets=d["padded_offsets"], alpha=d["alpha"],
                      beta=d["beta"], prob=d["prob"], dprob=dprob, d_row=d_row, workspace=ws_d, sched=sched,
@@ -89,6 +107,7 @@ def test_graph_replay_with_new_values_and_new_offsets(dev, sched, cta):
     torch.cuda.synchronize(dev)
     assert api.read_device_status(ws_d) == 0 and api.read_device_status(ws_w) == 0
     _check(spec_d, spec_w, x, y, d_row, dprob, out)
+    _check_srelu(x, c_s, d_s, dprob_s, amax_s)
 
     # replay 2: another token distribution with the same totals (offsets are device data)
     counts2 = np.array([256, 768, 0, 512], dtype=np.int64)
@@ -98,4 +117,6 @@ def test_graph_replay_with_new_values_and_new_offsets(dev, sched, cta):
     g.replay()
     torch.cuda.synchronize(dev)
     assert api.read_device_status(ws_d) == 0 and api.read_device_status(ws_w) == 0
+    assert api.read_device_status(ws_s) == 0
     _check(spec_d2, spec_w2, x, y, d_row, dprob, out)
+    _check_srelu(x, c_s, d_s, dprob_s, amax_s)
