@@ -265,9 +265,10 @@ struct DgluPolicy {
   // input block, on exit dgate / dinput; returns this row's partial of sum_j R * act.
   // One activation over a 32-column chunk; the activation is fixed per launch, so the branch is
   // taken once per chunk and only that activation's unrolled loop runs.
-  template <int ACT, int NV>
-  __device__ __forceinline__ float dglu_math_act(const uint32_t* r, float* gv, float* iv, float alpha2, float beta_g,
-                                                 float pr) const {
+  // dSiTU-GLU, one element at a time (its two tanh terms leave little to pack).
+  template <int NV>
+  __device__ __forceinline__ float dsitu_math(const uint32_t* r, float* gv, float* iv, float alpha2, float beta_g,
+                                              float pr) const {
     float dprob_acc = 0.f;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
@@ -275,41 +276,81 @@ struct DgluPolicy {
       const float x_g = __fmul_rn(beta_g, gv[k]);  // one fp32 product, never contracted
       const float x_i = __fmul_rn(beta_g, iv[k]);
       const float Rp = R * pr;
-      float dg, di, act;
-      if constexpr (ACT == MGG_ACT_DSWIGLU) {
-        const float s = fast_sigmoid(x_g);
-        di = Rp * (x_g * s);
-        dg = Rp * x_i * s * (1.0f + x_g * (1.0f - s));
-        act = x_g * s * x_i;
-      } else if constexpr (ACT == MGG_ACT_DSITUGLU) {
-        const float s = fast_sigmoid(x_g);
-        const float tg = fast_tanh(x_g * p.situ_inv_b1);
-        const float tu = fast_tanh(x_i * p.situ_inv_b2);
-        const float Tg = p.situ_b1 * tg * s;
-        const float Tu = p.situ_b2 * tu;
-        const float dTg = (1.0f - tg * tg) * s + p.situ_b1 * tg * s * (1.0f - s);
-        const float dTu = 1.0f - tu * tu;
-        dg = Rp * Tu * dTg;
-        di = Rp * Tg * dTu;
-        act = Tg * Tu;
-      } else {
-        const float cgt = fminf(x_g, 7.0f);
-        const float cit = fminf(fmaxf(x_i, -7.0f), 7.0f);
-        const bool g_in = x_g <= 7.0f;
-        const bool i_in = (x_i >= -7.0f) && (x_i <= 7.0f);
-        const float gf = g_in ? (p.indicator ? 1.0f : x_g) : 0.0f;
-        const float inf_ = i_in ? (p.indicator ? 1.0f : x_i) : 0.0f;
-        const float s = fast_sigmoid(1.702f * cgt);
-        const float ci1 = cit + 1.0f;
-        dg = Rp * ci1 * s * (1.0f + 1.702f * cgt * (1.0f - s)) * gf;
-        di = Rp * cgt * s * inf_;
-        act = cgt * s * ci1;
-      }
-      dprob_acc += R * act;
-      gv[k] = dg;
-      iv[k] = di;
+      const float s = fast_sigmoid(x_g);
+      const float tg = fast_tanh(x_g * p.situ_inv_b1);
+      const float tu = fast_tanh(x_i * p.situ_inv_b2);
+      const float Tg = p.situ_b1 * tg * s;
+      const float Tu = p.situ_b2 * tu;
+      const float dTg = (1.0f - tg * tg) * s + p.situ_b1 * tg * s * (1.0f - s);
+      const float dTu = 1.0f - tu * tu;
+      dprob_acc += R * (Tg * Tu);
+      gv[k] = Rp * Tu * dTg;
+      iv[k] = Rp * Tg * dTu;
     }
     return dprob_acc;
+  }
+
+  // dSwiGLU / dGeGLU on element pairs with the packed fp32 instructions (add/mul/fma.f32x2): the
+  // epilogue is bound by instruction issue, and each packed instruction does two lanes' worth.
+  // Every product and sum is still one IEEE round-to-nearest fp32 operation per element; the
+  // sigmoid is 1 / (1 + 2^(-z log2 e)) on the SFU's ex2/rcp.  x_g and x_i stay single products
+  // (the clamp and filter decisions are taken on them in fp32).
+  template <int ACT, int NV>
+  __device__ __forceinline__ float dglu_math_act(const uint32_t* r, float* gv, float* iv, float alpha2, float beta_g,
+                                                 float pr) const {
+    static_assert(NV % 2 == 0, "pairs of elements");
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float2 one2 = make_float2(1.0f, 1.0f);
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+    const float2 a2 = make_float2(alpha2, alpha2);
+    const float2 b2 = make_float2(beta_g, beta_g);
+    const float2 p2 = make_float2(pr, pr);
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < NV; k += 2) {
+      const float2 R = __fmul2_rn(a2, make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])));
+      const float2 xg = __fmul2_rn(b2, make_float2(gv[k], gv[k + 1]));
+      const float2 xi = __fmul2_rn(b2, make_float2(iv[k], iv[k + 1]));
+      const float2 Rp = __fmul2_rn(R, p2);
+      float2 dg, di, act;
+      if constexpr (ACT == MGG_ACT_DSWIGLU) {
+        const float2 z = __fmul2_rn(xg, make_float2(-kLog2e, -kLog2e));
+        const float2 den = __fadd2_rn(make_float2(ex2_approx(z.x), ex2_approx(z.y)), one2);
+        const float2 s = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+        const float2 xs = __fmul2_rn(xg, s);                                  // x_g s
+        const float2 oms = __ffma2_rn(s, neg1, one2);                         // 1 - s
+        const float2 inner = __ffma2_rn(xg, oms, one2);                       // 1 + x_g (1 - s)
+        di = __fmul2_rn(Rp, xs);
+        dg = __fmul2_rn(__fmul2_rn(Rp, __fmul2_rn(xi, s)), inner);
+        act = __fmul2_rn(xs, xi);
+      } else {
+        static_assert(ACT == MGG_ACT_DGEGLU, "dSiTU-GLU has its own path");
+        const float2 cgt = make_float2(fminf(xg.x, 7.0f), fminf(xg.y, 7.0f));
+        const float2 cit = make_float2(fminf(fmaxf(xi.x, -7.0f), 7.0f), fminf(fmaxf(xi.y, -7.0f), 7.0f));
+        const bool ind = p.indicator != 0;
+        const float2 gf = make_float2(xg.x <= 7.0f ? (ind ? 1.0f : xg.x) : 0.0f,
+                                      xg.y <= 7.0f ? (ind ? 1.0f : xg.y) : 0.0f);
+        const float2 inf_ = make_float2((xi.x >= -7.0f && xi.x <= 7.0f) ? (ind ? 1.0f : xi.x) : 0.0f,
+                                        (xi.y >= -7.0f && xi.y <= 7.0f) ? (ind ? 1.0f : xi.y) : 0.0f);
+        const float2 kc = __fmul2_rn(cgt, make_float2(1.702f, 1.702f));     // 1.702 cgt
+        const float2 z = __fmul2_rn(kc, make_float2(-kLog2e, -kLog2e));
+        const float2 den = __fadd2_rn(make_float2(ex2_approx(z.x), ex2_approx(z.y)), one2);
+        const float2 s = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+        const float2 ci1 = __fadd2_rn(cit, one2);
+        const float2 oms = __ffma2_rn(s, neg1, one2);                         // 1 - s
+        const float2 inner = __ffma2_rn(kc, oms, one2);                       // 1 + 1.702 cgt (1 - s)
+        const float2 gs = __fmul2_rn(cgt, s);
+        dg = __fmul2_rn(__fmul2_rn(__fmul2_rn(Rp, __fmul2_rn(ci1, s)), inner), gf);
+        di = __fmul2_rn(__fmul2_rn(Rp, gs), inf_);
+        act = __fmul2_rn(gs, ci1);
+      }
+      acc = __ffma2_rn(R, act, acc);
+      gv[k] = dg.x;
+      gv[k + 1] = dg.y;
+      iv[k] = di.x;
+      iv[k + 1] = di.y;
+    }
+    return acc.x + acc.y;
   }
 
   // NV values per call: r points at the NV accumulator words, gv / iv at NV gate / input values.
@@ -317,7 +358,7 @@ struct DgluPolicy {
   __device__ __forceinline__ float dglu_math(const uint32_t* r, float* gv, float* iv, float alpha2, float beta_g,
                                              float pr) const {
     if (p.act == MGG_ACT_DSWIGLU) return dglu_math_act<MGG_ACT_DSWIGLU, NV>(r, gv, iv, alpha2, beta_g, pr);
-    if (p.act == MGG_ACT_DSITUGLU) return dglu_math_act<MGG_ACT_DSITUGLU, NV>(r, gv, iv, alpha2, beta_g, pr);
+    if (p.act == MGG_ACT_DSITUGLU) return dsitu_math<NV>(r, gv, iv, alpha2, beta_g, pr);
     return dglu_math_act<MGG_ACT_DGEGLU, NV>(r, gv, iv, alpha2, beta_g, pr);
   }
 
@@ -326,13 +367,38 @@ struct DgluPolicy {
     dbias_add(w, j0, lane, warp_column_sums(gv, lane), warp_column_sums(iv, lane));
   }
 
-  // Column l of a staged 32 x 32 fp32 box (128B-swizzled rows, as stage_block writes them), summed
-  // over its 32 rows by lane l: the lanes of one row read 32 distinct banks.
-  static __device__ __forceinline__ float box_column_sum(uint32_t box, int lane) {
-    float sum = 0.f;
+  // Adds the column totals of a staged 32 x 32 fp32 box (128B-swizzled rows, as stage_block writes
+  // them) into the 32 consecutive fp32 partials at ws.  Lane l reads 16-byte column group l & 7 of
+  // rows 8 (l >> 3) .. 8 (l >> 3) + 7 (the eight lanes of a quarter-warp hit all 32 banks once),
+  // two shuffle rounds add the four row quarters, and lanes 0..7 add their four columns with one
+  // 16-byte reduction.
+  static __device__ __forceinline__ void box_dbias_add(uint32_t box, int lane, float* ws) {
+    const int cg = lane & 7, rq = lane >> 3;
+    float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int r = 0; r < 32; ++r) sum += ld_shared_f32(box + swz128(r, lane >> 2) + 4 * (lane & 3));
-    return sum;
+    for (int i = 0; i < 8; ++i) {
+      const uint4 v = ld_shared_v4(box + swz128(rq * 8 + i, cg));
+      s01 = __fadd2_rn(s01, make_float2(__uint_as_float(v.x), __uint_as_float(v.y)));
+      s23 = __fadd2_rn(s23, make_float2(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
+#pragma unroll
+    for (int off = 8; off <= 16; off <<= 1) {
+      s01 = __fadd2_rn(s01, make_float2(__shfl_xor_sync(0xffffffffu, s01.x, off),
+                                        __shfl_xor_sync(0xffffffffu, s01.y, off)));
+      s23 = __fadd2_rn(s23, make_float2(__shfl_xor_sync(0xffffffffu, s23.x, off),
+                                        __shfl_xor_sync(0xffffffffu, s23.y, off)));
+    }
+    if (lane < 8) {
+      const float v4[4] = {s01.x, s01.y, s23.x, s23.y};
+      red_add_v4(ws + 4 * cg, v4);
+    }
+  }
+
+  // The expert's fp32 dbias partials for the gate (second = 0) or input (second = 1) block of
+  // compact chunk j0.
+  __device__ __forceinline__ float* dbias_ws_at(const TileWork& w, int j0, int second) const {
+    const int first_half = (p.gate_first != 0) == (second == 0) ? 0 : 32;
+    return p.dbias_ws + (size_t)w.expert * 2 * (size_t)p.N + 2 * j0 + first_half;
   }
 
   // Adds this warp's column totals (lane l: gate column l in sg, input column l in si) of compact
@@ -495,12 +561,12 @@ struct DgluPolicy {
           stage_block(box, lane, 0, gv);
           staging_flush(box, lane, p.gate_first ? x : x + 32, row0);
           // dbias column totals straight from the staged fp32 values (the exact D_row values)
-          const float sg = db ? box_column_sum(box, lane) : 0.f;
+          if (db) box_dbias_add(box, lane, dbias_ws_at(w, j0, 0));
           if (lane == 0) bulk_wait_read<0>();  // the gate half has left the box
           __syncwarp();
           stage_block(box, lane, 0, iv);
           staging_flush(box, lane, p.gate_first ? x + 32 : x, row0);
-          if (db) dbias_add(w, j0, lane, sg, box_column_sum(box, lane));
+          if (db) box_dbias_add(box, lane, dbias_ws_at(w, j0, 1));
         }
         if (DS == 2 && p.dbias_ws != nullptr) dbias_partials(w, j0, lane, gv, iv);
       } else {

@@ -178,6 +178,13 @@ __device__ __forceinline__ void red_add_v4(float* addr, const float (&v)[4]) {
                : "memory");
 }
 
+// 2^x on the SFU (PTX ex2.approx, flush-to-zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Approximate reciprocal (one MUFU operation); rcp(+inf) = 0.
 __device__ __forceinline__ float rcp_approx(float x) {
   float y;

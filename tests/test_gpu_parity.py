@@ -113,14 +113,18 @@ def test_dglu_bwd_parity(dev, case, sched, cta):
     np.testing.assert_array_equal(tiles_from_log(gpu["tile_log"]), want)
 
 
-@pytest.mark.parametrize("gate_first,filt", [(False, "value"), (True, "indicator"), (False, "indicator")])
-def test_dglu_block_order_and_filter_modes(dev, gate_first, filt):
-    spec = synth.small_dglu_spec("modes", act="dgeglu", c_std=4.0)
+@pytest.mark.parametrize("gate_first,filt,d_dtype", [(False, "value", "bf16"), (True, "indicator", "bf16"),
+                                                     (False, "indicator", "bf16"), (False, "value", "fp32")])
+def test_dglu_block_order_and_filter_modes(dev, gate_first, filt, d_dtype):
+    # the fp32 case also sums dbias from the staged fp32 boxes with the input block first
+    spec = synth.small_dglu_spec("modes", act="dgeglu", c_std=4.0, d_dtype=d_dtype, dbias=d_dtype == "fp32")
     x = synth.make_dglu_inputs(spec)
     gpu = run_dglu_gpu(spec, x, dev, gate_first=gate_first, geglu_filter=filt)
     ref = run_dglu_oracle(spec, x, gate_first=gate_first, geglu_filter=filt)
-    check_close("d_row", to_np(gpu["d_row"]), ref["d_row"], TOL["bf16"])
+    check_close("d_row", to_np(gpu["d_row"]), ref["d_row"], TOL[d_dtype])
     check_close("dprob", to_np(gpu["dprob"]), ref["dprob"], TOL_DPROB)
+    if spec.dbias:
+        check_close("dbias", to_np(gpu["dbias"]), ref["dbias"], TOL["bf16"])
 
 
 @pytest.mark.parametrize("betas", [(2.0, 5.0), (0.5, 40.0)])
