@@ -295,7 +295,7 @@ struct DgluPolicy {
   // Every product and sum is still one IEEE round-to-nearest fp32 operation per element; the
   // sigmoid is 1 / (1 + 2^(-z log2 e)) on the SFU's ex2/rcp.  x_g and x_i stay single products
   // (the clamp and filter decisions are taken on them in fp32).
-  template <int ACT, int NV>
+  template <int ACT, int NV, bool IND = false>
   __device__ __forceinline__ float dglu_math_act(const uint32_t* r, float* gv, float* iv, float alpha2, float beta_g,
                                                  float pr) const {
     static_assert(NV % 2 == 0, "pairs of elements");
@@ -327,11 +327,11 @@ struct DgluPolicy {
         static_assert(ACT == MGG_ACT_DGEGLU, "dSiTU-GLU has its own path");
         const float2 cgt = make_float2(fminf(xg.x, 7.0f), fminf(xg.y, 7.0f));
         const float2 cit = make_float2(fminf(fmaxf(xi.x, -7.0f), 7.0f), fminf(fmaxf(xi.y, -7.0f), 7.0f));
-        const bool ind = p.indicator != 0;
-        const float2 gf = make_float2(xg.x <= 7.0f ? (ind ? 1.0f : xg.x) : 0.0f,
-                                      xg.y <= 7.0f ? (ind ? 1.0f : xg.y) : 0.0f);
-        const float2 inf_ = make_float2((xi.x >= -7.0f && xi.x <= 7.0f) ? (ind ? 1.0f : xi.x) : 0.0f,
-                                        (xi.y >= -7.0f && xi.y <= 7.0f) ? (ind ? 1.0f : xi.y) : 0.0f);
+        // filters: the indicator (1 inside the clamp range) or the value itself (IND = false)
+        const float2 gf = make_float2(xg.x <= 7.0f ? (IND ? 1.0f : xg.x) : 0.0f,
+                                      xg.y <= 7.0f ? (IND ? 1.0f : xg.y) : 0.0f);
+        const float2 inf_ = make_float2(fabsf(xi.x) <= 7.0f ? (IND ? 1.0f : xi.x) : 0.0f,
+                                        fabsf(xi.y) <= 7.0f ? (IND ? 1.0f : xi.y) : 0.0f);
         const float2 kc = __fmul2_rn(cgt, make_float2(1.702f, 1.702f));     // 1.702 cgt
         const float2 z = __fmul2_rn(kc, make_float2(-kLog2e, -kLog2e));
         const float2 den = __fadd2_rn(make_float2(ex2_approx(z.x), ex2_approx(z.y)), one2);
@@ -359,7 +359,8 @@ struct DgluPolicy {
                                              float pr) const {
     if (p.act == MGG_ACT_DSWIGLU) return dglu_math_act<MGG_ACT_DSWIGLU, NV>(r, gv, iv, alpha2, beta_g, pr);
     if (p.act == MGG_ACT_DSITUGLU) return dsitu_math<NV>(r, gv, iv, alpha2, beta_g, pr);
-    return dglu_math_act<MGG_ACT_DGEGLU, NV>(r, gv, iv, alpha2, beta_g, pr);
+    if (p.indicator) return dglu_math_act<MGG_ACT_DGEGLU, NV, true>(r, gv, iv, alpha2, beta_g, pr);
+    return dglu_math_act<MGG_ACT_DGEGLU, NV, false>(r, gv, iv, alpha2, beta_g, pr);
   }
 
   __device__ __forceinline__ void dbias_partials(const TileWork& w, int j0, int lane, float (&gv)[32],

@@ -17,6 +17,9 @@
 
 namespace mgg {
 
+// Workspace status word holding the number of experts whose tiles have work (prep kernel).
+constexpr int kWgradActiveWord = 4;
+
 struct WgradParams {
   CUtensorMap tmap_a;          // tensor2d A: K-major dims {T, h} box {64, 128}; M-major dims {h, T} box {64, 64}
   CUtensorMap tmap_b;          // tensor2d B: N-major dims {i, T} box {64, 64}; K-major dims {T, i} box {64, BN}
@@ -62,15 +65,19 @@ struct WgradPolicy {
   int a_mn, b_mn;
   int dynamic;
 
+  // The tiles of the experts that have work (all of them when overwriting; in accumulate mode the
+  // preparation kernel counts the non-empty ones, which the LPT order puts first), so the two ends
+  // of the dynamic schedule are a long and a short tile with work rather than skipped ones.
   __device__ WgradPolicy(const WgradParams& prm)
-      : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(prm.a_mn), b_mn(prm.b_mn),
-        dynamic(prm.dynamic) {}
+      : p(prm),
+        total_tiles(min(prm.total_tiles, (long long)__ldcg(prm.status + kWgradActiveWord) * prm.tiles_per_expert)),
+        status(prm.status), a_mn(prm.a_mn), b_mn(prm.b_mn), dynamic(prm.dynamic) {}
 
   // Tiles in LPT order (experts by decreasing token count).  The dynamic schedule hands them out
   // alternately from the long end and the short end, so each SM interleaves MMA-bound long
   // reductions with store-bound short ones; the static schedule deals them round-robin.
   __device__ TileWork tile(long long t) const {
-    const long long idx = !p.dynamic ? t : (t & 1) ? p.total_tiles - 1 - (t >> 1) : (t >> 1);
+    const long long idx = !p.dynamic ? t : (t & 1) ? total_tiles - 1 - (t >> 1) : (t >> 1);
     const int slot = (int)(idx / p.tiles_per_expert);
     const int local = (int)(idx % p.tiles_per_expert);
     const int e = __ldg(p.order + slot);
@@ -239,7 +246,8 @@ __global__ void wgrad_prep_kernel(const int32_t* offsets, int L, long long T, co
                                   const __grid_constant__ CUtensorMap tmpl_a, const __grid_constant__ CUtensorMap tmpl_b,
                                   const __grid_constant__ CUtensorMap tmpl_out, const void* a, const void* b,
                                   int hidden, int inter, int a_ragged, int b_ragged, CUtensorMap* a_maps,
-                                  CUtensorMap* b_maps, CUtensorMap* out_maps, int32_t* order, int* status) {
+                                  CUtensorMap* b_maps, CUtensorMap* out_maps, int32_t* order, int* status,
+                                  int accumulate) {
   __shared__ int s_cnt[1024];
   bool bad_off = false, bad_ptr = false;
   for (int e = threadIdx.x; e < L; e += blockDim.x) {
@@ -255,11 +263,13 @@ __global__ void wgrad_prep_kernel(const int32_t* offsets, int L, long long T, co
   }
   const int any_off = __syncthreads_or(bad_off);
   const int any_ptr = __syncthreads_or(bad_ptr);
+  const int nonempty = __syncthreads_count((int)threadIdx.x < L && s_cnt[threadIdx.x] > 0);
   if (threadIdx.x == 0) {
     status[0] = any_off ? (int)MGG_ERR_DEVICE_OFFSETS : any_ptr ? (int)MGG_ERR_DEVICE_POINTER : 0;
     status[1] = 0;
     status[2] = 0;
     status[3] = 0;
+    status[kWgradActiveWord] = (any_off || any_ptr) ? 0 : accumulate ? nonempty : L;  // experts with tiles
   }
   if (any_off || any_ptr) return;
   // stable rank by decreasing count
@@ -340,7 +350,8 @@ cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {
 
   wgrad_prep_kernel<<<1, 1024, 0, stream>>>(a.offsets, (int)a.L, (long long)a.tokens_sum, a.out_ptrs, Lc.tmap_a,
                                             Lc.tmap_b, Lc.tmap_out, a.a, a.b, (int)a.hidden, (int)a.inter,
-                                            Lc.a_ragged, Lc.b_ragged, a_maps, b_maps, out_maps, order, status);
+                                            Lc.a_ragged, Lc.b_ragged, a_maps, b_maps, out_maps, order, status,
+                                            a.accumulate ? 1 : 0);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
