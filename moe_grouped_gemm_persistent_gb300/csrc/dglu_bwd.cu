@@ -291,35 +291,35 @@ struct DgluPolicy {
   }
 
   // dSwiGLU / dGeGLU on element pairs with the packed fp32 instructions (add/mul/fma.f32x2): the
-  // epilogue is bound by instruction issue, and each packed instruction does two lanes' worth.
-  // Every product and sum is still one IEEE round-to-nearest fp32 operation per element; the
-  // sigmoid is 1 / (1 + 2^(-z log2 e)) on the SFU's ex2/rcp.  x_g and x_i stay single products
-  // (the clamp and filter decisions are taken on them in fp32).
+  // epilogue is bound by instruction latency and issue, and each packed instruction does two
+  // lanes' worth.  Every product and sum is one IEEE round-to-nearest fp32 operation per element;
+  // the sigmoid is 1 / (1 + 2^(-z log2 e)) on the SFU's ex2/rcp.  x_g and x_i stay single products
+  // (the clamp and filter decisions are taken on them in fp32).  R p = acc (alpha^2 p) and the
+  // dprob sum is alpha^2 sum acc * act, the factor applied once at the end.
   template <int ACT, int NV, bool IND = false>
   __device__ __forceinline__ float dglu_math_act(const uint32_t* r, float* gv, float* iv, float alpha2, float beta_g,
                                                  float pr) const {
     static_assert(NV % 2 == 0, "pairs of elements");
     constexpr float kLog2e = 1.4426950408889634f;
     const float2 one2 = make_float2(1.0f, 1.0f);
-    const float2 neg1 = make_float2(-1.0f, -1.0f);
-    const float2 a2 = make_float2(alpha2, alpha2);
     const float2 b2 = make_float2(beta_g, beta_g);
-    const float2 p2 = make_float2(pr, pr);
+    const float ap = alpha2 * pr;
+    const float2 ap2 = make_float2(ap, ap);
     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < NV; k += 2) {
-      const float2 R = __fmul2_rn(a2, make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])));
+      const float2 acc_v = make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1]));
       const float2 xg = __fmul2_rn(b2, make_float2(gv[k], gv[k + 1]));
       const float2 xi = __fmul2_rn(b2, make_float2(iv[k], iv[k + 1]));
-      const float2 Rp = __fmul2_rn(R, p2);
+      const float2 Rp = __fmul2_rn(acc_v, ap2);
       float2 dg, di, act;
       if constexpr (ACT == MGG_ACT_DSWIGLU) {
         const float2 z = __fmul2_rn(xg, make_float2(-kLog2e, -kLog2e));
         const float2 den = __fadd2_rn(make_float2(ex2_approx(z.x), ex2_approx(z.y)), one2);
         const float2 s = make_float2(rcp_approx(den.x), rcp_approx(den.y));
-        const float2 xs = __fmul2_rn(xg, s);                                  // x_g s
-        const float2 oms = __ffma2_rn(s, neg1, one2);                         // 1 - s
-        const float2 inner = __ffma2_rn(xg, oms, one2);                       // 1 + x_g (1 - s)
+        const float2 xs = __fmul2_rn(xg, s);                                        // x_g s
+        const float2 oms = __ffma2_rn(s, make_float2(-1.0f, -1.0f), one2);          // 1 - s
+        const float2 inner = __ffma2_rn(xg, oms, one2);                             // 1 + x_g (1 - s)
         di = __fmul2_rn(Rp, xs);
         dg = __fmul2_rn(__fmul2_rn(Rp, __fmul2_rn(xi, s)), inner);
         act = __fmul2_rn(xs, xi);
@@ -332,25 +332,25 @@ struct DgluPolicy {
                                       xg.y <= 7.0f ? (IND ? 1.0f : xg.y) : 0.0f);
         const float2 inf_ = make_float2(fabsf(xi.x) <= 7.0f ? (IND ? 1.0f : xi.x) : 0.0f,
                                         fabsf(xi.y) <= 7.0f ? (IND ? 1.0f : xi.y) : 0.0f);
-        const float2 kc = __fmul2_rn(cgt, make_float2(1.702f, 1.702f));     // 1.702 cgt
-        const float2 z = __fmul2_rn(kc, make_float2(-kLog2e, -kLog2e));
+        constexpr float kA = 1.702f;
+        const float2 z = __fmul2_rn(cgt, make_float2(-kA * kLog2e, -kA * kLog2e));  // -1.702 cgt log2 e
         const float2 den = __fadd2_rn(make_float2(ex2_approx(z.x), ex2_approx(z.y)), one2);
         const float2 s = make_float2(rcp_approx(den.x), rcp_approx(den.y));
         const float2 ci1 = __fadd2_rn(cit, one2);
-        const float2 oms = __ffma2_rn(s, neg1, one2);                         // 1 - s
-        const float2 inner = __ffma2_rn(kc, oms, one2);                       // 1 + 1.702 cgt (1 - s)
+        const float2 aoms = __ffma2_rn(s, make_float2(-kA, -kA), make_float2(kA, kA));  // 1.702 (1 - s)
+        const float2 inner = __ffma2_rn(cgt, aoms, one2);                               // 1 + 1.702 cgt (1 - s)
         const float2 gs = __fmul2_rn(cgt, s);
         dg = __fmul2_rn(__fmul2_rn(__fmul2_rn(Rp, __fmul2_rn(ci1, s)), inner), gf);
         di = __fmul2_rn(__fmul2_rn(Rp, gs), inf_);
         act = __fmul2_rn(gs, ci1);
       }
-      acc = __ffma2_rn(R, act, acc);
+      acc = __ffma2_rn(acc_v, act, acc);
       gv[k] = dg.x;
       gv[k + 1] = dg.y;
       iv[k] = di.x;
       iv[k + 1] = di.y;
     }
-    return acc.x + acc.y;
+    return alpha2 * (acc.x + acc.y);
   }
 
   // NV values per call: r points at the NV accumulator words, gv / iv at NV gate / input values.
