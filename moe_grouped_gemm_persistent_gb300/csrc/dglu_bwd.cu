@@ -231,9 +231,10 @@ struct DgluPolicy {
   }
 
   // Bulk store of one staged box to D_row (and to D_col when requested); lane 0 of the warp.
+  // D_row (and D_col) are written once: streamed out of L2 ahead of the reused A / B lines.
   __device__ __forceinline__ void store_box(uint32_t stg, int x, int y) const {
-    tma_store_2d(&p.tmap_d, stg, x, y);
-    if (p.has_dcol) tma_store_2d(&p.tmap_dcol, stg, x, y);
+    tma_store_2d_evict_first(&p.tmap_d, stg, x, y);
+    if (p.has_dcol) tma_store_2d_evict_first(&p.tmap_dcol, stg, x, y);
   }
 
   __device__ __forceinline__ void staging_flush(uint32_t stg, int lane, int x, int y) const {
@@ -464,7 +465,8 @@ struct DgluPolicy {
   __device__ __forceinline__ void c_issue(const EpiCtx& ctx, uint32_t use, int x, int row0) const {
     const uint32_t b = use % kCRing;
     mbar_arrive_expect_tx(&ctx.bars[b], 4096);
-    tma_load_2d(smem_u32(ctx.stg) + b * 4096, &p.tmap_c, smem_u32(&ctx.bars[b]), x, row0);
+    // C is read once: evict-first keeps the reused A / B lines in L2
+    tma_load_2d_evict_first(smem_u32(ctx.stg) + b * 4096, &p.tmap_c, smem_u32(&ctx.bars[b]), x, row0);
   }
 
   __device__ __forceinline__ void read_c_block(uint32_t box, int lane, int blk, float (&v)[32]) const {

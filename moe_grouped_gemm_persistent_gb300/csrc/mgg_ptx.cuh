@@ -124,6 +124,30 @@ __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int3
                : "memory");
 }
 
+// Streaming variants: an L2 eviction-priority hint (createpolicy ... evict_first, applied to the
+// whole access) marks lines that are read or written once, so they leave L2 before data that is
+// still being reused there (the GEMM operands).
+__device__ __forceinline__ void tma_load_2d_evict_first(uint32_t dst, const void* map, uint32_t bar, int32_t x,
+                                                        int32_t y) {
+  asm volatile(
+      "{\n\t.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%3, %4}], [%2], pol;\n\t}" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d_evict_first(const void* map, uint32_t src, int32_t x, int32_t y) {
+  asm volatile(
+      "{\n\t.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], pol;\n\t}" ::"l"(
+          map),
+      "r"(src), "r"(x), "r"(y)
+      : "memory");
+}
+
 // Element-wise global += shared (fp32 add performed at the memory side).
 __device__ __forceinline__ void tma_reduce_add_2d(const void* map, uint32_t src, int32_t x, int32_t y) {
   asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

@@ -100,7 +100,7 @@ def check_dglu_sampled(spec, x, d_row, dprob, rng, n_experts):
     assert rel_fro(np.concatenate(dp_got), np.concatenate(dp_ref)) <= TOL_DPROB
 
 
-@pytest.mark.parametrize("name", ["mixtral", "geglu", "deepseek"])
+@pytest.mark.parametrize("name", ["mixtral", "geglu", "deepseek", "mixtral_situ"])
 def test_dgrad_full_size(dev, name):
     spec, _ = synth.workload_specs(name)
     rng = np.random.default_rng(7)
@@ -119,6 +119,56 @@ def test_dgrad_full_size(dev, name):
                 assert (dbias[g] == 0).all()
         assert rel_fro(f32(dbias), sums.cpu().numpy()) <= TOL["bf16"]
     del x, d_row, dprob, dbias
+    torch.cuda.empty_cache()
+
+
+def test_dsrelu_full_size(dev):
+    """The Mixtral-shaped dsReLU layer: sampled D_row rows and dprob vs the oracle, the tile log
+    vs the schedule, D_col = D_row bit for bit, amax = the per-expert max |D_row|."""
+    spec, _ = synth.workload_specs("dsrelu")
+    rng = np.random.default_rng(11)
+    x = synth.make_dglu_inputs(spec, device=dev)
+    M, N, L = spec.M, spec.N, spec.L
+    d_row = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    d_col = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    dprob = torch.zeros(M, dtype=torch.float32, device=dev)
+    amax = torch.full((L,), -1.0, dtype=torch.float32, device=dev)
+    log = torch.empty(4 * api.dglu_bwd_num_tiles(M, N), dtype=torch.int32, device=dev)
+    ws = api.dsrelu_bwd(a=x["a"], b=x["b"], c=x["c"], padded_offsets=x["padded_offsets"], alpha=x["alpha"],
+                        prob=x["prob"], dprob=dprob, d_row=d_row, d_col=d_col, amax=amax, tile_log=log)
+    assert api.read_device_status(ws) == 0, api.last_error()
+    tm, tn = api.dglu_bwd_tile_shape()
+    offs = np.cumsum(spec.counts)
+    np.testing.assert_array_equal(tiles_from_log(log.cpu()), oracle.dgrad_tiles(offs, N, tm, tn))
+    assert torch.equal(d_row.view(torch.int16), d_col.view(torch.int16))
+    ranges = oracle.expert_ranges(offs)
+    experts = sampled_experts(spec.counts, rng, 6)
+    rows = sample_rows(spec.counts, experts, rng)
+    got_all, ref_all, dp_got, dp_ref = [], [], [], []
+    for g in experts:
+        lo, hi = ranges[g]
+        sel = rows[(rows >= lo) & (rows < hi)]
+        idx = torch.as_tensor(sel, device=dev)
+        b_g = f32(x["b"][g])
+        offs_local = np.zeros(L, dtype=np.int64)
+        offs_local[g:] = len(sel)
+        res = oracle.dsrelu_bwd(f32(x["a"][idx]), lambda e: b_g, f32(x["c"][idx]), offs_local, f32(x["alpha"]),
+                                f32(x["prob"][idx]))
+        got = f32(d_row[idx])
+        assert not np.isnan(got).any()
+        err = rel_fro(got, res["d_row"])
+        assert err <= TOL["bf16"], f"expert {g}: d_row relative error {err:.3e}"
+        got_all.append(got)
+        ref_all.append(res["d_row"])
+        dp_got.append(f32(dprob[idx]))
+        dp_ref.append(res["dprob"])
+    assert rel_fro(np.concatenate(got_all), np.concatenate(ref_all)) <= TOL["bf16"]
+    assert rel_fro(np.concatenate(dp_got), np.concatenate(dp_ref)) <= TOL_DPROB
+    # amax is taken on the fp32 values before rounding; the bf16 D_row is within 2^-8 of them
+    want = torch.stack([d_row[lo:hi].float().abs().max() if hi > lo else torch.zeros((), device=dev)
+                        for lo, hi in ranges])
+    np.testing.assert_allclose(f32(amax), f32(want), rtol=4e-3, atol=0)
+    del x, d_row, d_col, dprob
     torch.cuda.empty_cache()
 
 
