@@ -55,7 +55,7 @@ struct WgradPolicy {
   static constexpr int kBLoad = PAIR ? BN / 2 : BN;
   static constexpr int EPI_WARPS = kWgradEpiWarps;
   static constexpr int STG_BYTES = kWgradStgBytes;
-  static constexpr int kEpiHalves = EPI_WARPS / 4;
+  static_assert(EPI_WARPS == 4, "one epilogue warp per TMEM sub-partition: it drains every column");
   static constexpr int CW = 128 / OS;  // output columns per staged chunk (one 128-byte row)
   const WgradParams& p;
   static constexpr int kBoxes = STG_BYTES / 4096;
@@ -139,7 +139,7 @@ struct WgradPolicy {
 
   __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, bool have_acc, const EpiCtx& ctx,
                            AccRelease rel) const {
-    const int q = ctx.q, half = ctx.half, lane = ctx.lane;
+    const int q = ctx.q, lane = ctx.lane;
     uint8_t* stg_ptr = ctx.stg;
     const int e = w.expert;
     const int row0 = w.m0 + ctx.rank * BM + q * 32;
@@ -155,76 +155,82 @@ struct WgradPolicy {
     const bool reduce = p.accumulate && OS == 4;
     const bool add_old = p.accumulate && OS == 2;
     bool released = false;
+    // One TMEM load per 64 accumulator columns (tcgen05.ld 32x32b.x64): two 32-column chunks of
+    // fp32 output or one 64-column chunk of 16-bit output.  Fewer, wider loads wait less on tensor
+    // memory while the MMA of the next tile writes the other accumulator.
+    constexpr int kPerLoad = 64 / CW;
 #pragma unroll 1
-    for (int c = half; c < nchunks; c += kEpiHalves) {
-      const int col0 = w.n0 + c * CW;
-      float v[CW];
+    for (int c0 = 0; c0 < nchunks; c0 += kPerLoad) {
+      float v[64];
       if (have_acc) {
-        uint32_t r[32];
-        tmem_load_32cols(taddr + c * CW, r);
+        uint32_t r[64];
+        tmem_load_64cols(taddr + c0 * CW, r);  // BN is a multiple of 64: never past this accumulator
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
-        if constexpr (CW == 64) {
-          tmem_load_32cols(taddr + c * CW + 32, r);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[32 + k] = __uint_as_float(r[k]);
-        }
-        if (c + kEpiHalves >= nchunks) {
+        for (int k = 0; k < 64; ++k) v[k] = __uint_as_float(r[k]);
+        if (c0 + kPerLoad >= nchunks) {
           rel(lane);
           released = true;
         }
       } else {
 #pragma unroll
-        for (int k = 0; k < CW; ++k) v[k] = 0.f;
+        for (int k = 0; k < 64; ++k) v[k] = 0.f;
       }
-      if (add_old && row < p.hidden) {
-        const char* base = discrete ? reinterpret_cast<const char*>(__ldg(p.out_ptrs + e))
-                                    : static_cast<const char*>(p.out) + (size_t)e * p.hidden * (size_t)p.inter * OS;
-        const int n = p.inter - col0 < CW ? p.inter - col0 : CW;
-        const size_t idx = (size_t)row * p.inter + col0;
 #pragma unroll
-        for (int h = 0; h < CW / 32; ++h) {
-          float old[32];
-          load32_n(base, p.out_dtype, idx + 32 * h, old, n - 32 * h);
+      for (int j = 0; j < kPerLoad; ++j) {
+        const int c = c0 + j;
+        if (c >= nchunks) break;
+        const int col0 = w.n0 + c * CW;
+        if (add_old && row < p.hidden) {
+          const char* base = discrete ? reinterpret_cast<const char*>(__ldg(p.out_ptrs + e))
+                                      : static_cast<const char*>(p.out) + (size_t)e * p.hidden * (size_t)p.inter * OS;
+          const int n = p.inter - col0 < CW ? p.inter - col0 : CW;
+          const size_t idx = (size_t)row * p.inter + col0;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[32 * h + k] += old[k];
+          for (int h = 0; h < CW / 32; ++h) {
+            float old[32];
+            load32_n(base, p.out_dtype, idx + 32 * h, old, n - 32 * h);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[CW * j + 32 * h + k] += old[k];
+          }
         }
-      }
-      if (!rows_in) continue;  // rows past hidden (single-CTA tiles only): nothing to write
-      // the box was last filled kBoxes stores ago: wait until at most kBoxes - 1 stores still read
-      const uint32_t box = stg + (stg_uses % kBoxes) * 4096u;
-      ++stg_uses;
-      if (lane == 0) bulk_wait_read<kBoxes - 1>();
-      __syncwarp();
-      if constexpr (OS == 4) {
+        if (!rows_in) continue;  // rows past hidden (single-CTA tiles only): nothing to write
+        // the box was last filled kBoxes stores ago: wait until at most kBoxes - 1 stores still read
+        const uint32_t box = stg + (stg_uses % kBoxes) * 4096u;
+        ++stg_uses;
+        if (lane == 0) bulk_wait_read<kBoxes - 1>();
+        __syncwarp();
+        const float* vc = v + CW * j;
+        if constexpr (OS == 4) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          st_shared_v4(box + swz128w(lane, i), __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
-                       __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
-      } else {
-        const int dt = p.out_dtype;
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          st_shared_v4(box + swz128w(lane, i), pack2(v[8 * i], v[8 * i + 1], dt), pack2(v[8 * i + 2], v[8 * i + 3], dt),
-                       pack2(v[8 * i + 4], v[8 * i + 5], dt), pack2(v[8 * i + 6], v[8 * i + 7], dt));
-      }
-      fence_async_shared();
-      __syncwarp();
-      if (lane == 0) {
-        if (discrete) {
-          if (reduce) tma_reduce_add_2d(map, box, col0, row0);
-          else tma_store_2d(map, box, col0, row0);
+          for (int i = 0; i < 8; ++i)
+            st_shared_v4(box + swz128w(lane, i), __float_as_uint(vc[4 * i]), __float_as_uint(vc[4 * i + 1]),
+                         __float_as_uint(vc[4 * i + 2]), __float_as_uint(vc[4 * i + 3]));
         } else {
-          if (reduce) tma_reduce_add_3d(map, box, col0, row0, e);
-          else tma_store_3d(map, box, col0, row0, e);
+          const int dt = p.out_dtype;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            st_shared_v4(box + swz128w(lane, i), pack2(vc[8 * i], vc[8 * i + 1], dt),
+                         pack2(vc[8 * i + 2], vc[8 * i + 3], dt), pack2(vc[8 * i + 4], vc[8 * i + 5], dt),
+                         pack2(vc[8 * i + 6], vc[8 * i + 7], dt));
         }
-        bulk_commit_group();
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          if (discrete) {
+            if (reduce) tma_reduce_add_2d(map, box, col0, row0);
+            else tma_store_2d(map, box, col0, row0);
+          } else {
+            if (reduce) tma_reduce_add_3d(map, box, col0, row0, e);
+            else tma_store_3d(map, box, col0, row0, e);
+          }
+          bulk_commit_group();
+        }
       }
     }
     if (have_acc && !released) rel(lane);
     // one entry per CTA tile of 128 rows (a pair's tile logs two)
     const long long idx = PAIR ? 2 * t + ctx.rank : t;
-    if (p.tile_log != nullptr && q == 0 && half == 0 && lane == 0 && idx < p.tile_log_cap) {
+    if (p.tile_log != nullptr && q == 0 && lane == 0 && idx < p.tile_log_cap) {
       int32_t* l = p.tile_log + 4 * idx;
       l[0] = e;
       l[1] = w.m0 + ctx.rank * BM;
