@@ -53,8 +53,9 @@ mgg_status encode_map(CUtensorMap* map, int dtype, const void* addr, int rank, c
                       const uint64_t* strides, const uint32_t* box, const char* what) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return fail(MGG_ERR_RUNTIME, "cuTensorMapEncodeTiled is not available from the CUDA driver");
-  cuuint64_t gdim[3], gstr[2];
-  cuuint32_t bdim[3], estr[3] = {1, 1, 1};
+  if (rank < 1 || rank > 4) return fail(MGG_ERR_RUNTIME, std::string("tensor map rank out of range for the ") + what);
+  cuuint64_t gdim[4], gstr[3];
+  cuuint32_t bdim[4], estr[4] = {1, 1, 1, 1};
   for (int i = 0; i < rank; ++i) {
     gdim[i] = dims[i];
     bdim[i] = box[i];
@@ -487,12 +488,28 @@ mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {
   {  // outputs: 32-row boxes of one 128-byte row of columns
     const uint64_t esz = a.out_dtype == MGG_FP32 ? 4 : 2, L = (uint64_t)a.L;
     const uint32_t cw = (uint32_t)(128 / esz);
-    if (a.out != nullptr) {
+    // FP32 outputs with inter % 64 == 0 are also viewed as 32-column blocks (dims {32, hidden,
+    // inter/32 [, L]}, strides {inter*4, 128 [, hidden*inter*4]} bytes): one box of two blocks
+    // stores the two 32-column chunks of one 64-column TMEM load (8 KB) with a single TMA copy.
+    if (a.out_dtype == MGG_FP32 && I % 64 == 0) {
+      const std::string saved = g_err;
+      if (a.out != nullptr) {
+        const uint64_t dims[4] = {32, H, I / 32, L}, strides[3] = {I * 4, 128, H * I * 4};
+        const uint32_t box[4] = {32, 32, 2, 1};
+        Lc.out_blocked = encode_map(&Lc.tmap_out, a.out_dtype, a.out, 4, dims, strides, box, "dense output (blocked)") == MGG_OK;
+      } else {
+        const uint64_t dims[3] = {32, H, I / 32}, strides[2] = {I * 4, 128};
+        const uint32_t box[3] = {32, 32, 2};
+        Lc.out_blocked = encode_map(&Lc.tmap_out, a.out_dtype, a.a, 3, dims, strides, box, "per-expert output (blocked)") == MGG_OK;
+      }
+      if (!Lc.out_blocked) g_err = saved;  // the driver refused the blocked view: the plain map is used
+    }
+    if (!Lc.out_blocked && a.out != nullptr) {
       const uint64_t dims[3] = {I, H, L}, strides[2] = {I * esz, H * I * esz};
       const uint32_t box[3] = {cw, 32, 1};
       if ((s = encode_map(&Lc.tmap_out, a.out_dtype, a.out, 3, dims, strides, box, "dense output")) != MGG_OK)
         return s;
-    } else {  // per-expert template; the preparation kernel substitutes each expert's address
+    } else if (!Lc.out_blocked) {  // per-expert template; the preparation kernel substitutes each expert's address
       const uint64_t dims[2] = {I, H}, strides[1] = {I * esz};
       const uint32_t box[2] = {cw, 32};
       if ((s = encode_map(&Lc.tmap_out, a.out_dtype, a.a, 2, dims, strides, box, "per-expert output")) != MGG_OK)

@@ -42,6 +42,7 @@ struct WgradLaunch {
   bool pair;      // 256-row tiles on CTA pairs (B maps load half a tile's columns)
   bool a_blocked; // M-major A as a 3-D map of 64-row blocks (one box per slot), else 2-D
   bool b_blocked; // N-major B likewise
+  bool out_blocked; // FP32 output as 32-column blocks (one TMA copy per two chunks), else plain
 };
 
 // Launchers (queue the prep kernel, the persistent kernel and finalisers on `stream`).

@@ -163,6 +163,21 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* map, uint32_t src,
       : "memory");
 }
 
+__device__ __forceinline__ void tma_store_4d(const void* map, uint32_t src, int32_t x, int32_t y, int32_t z,
+                                             int32_t w) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(map),
+               "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_reduce_add_4d(const void* map, uint32_t src, int32_t x, int32_t y, int32_t z,
+                                                  int32_t w) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(map),
+      "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until the committed bulk groups have finished reading their shared-memory sources.

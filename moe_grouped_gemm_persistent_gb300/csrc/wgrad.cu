@@ -23,7 +23,8 @@ constexpr int kWgradActiveWord = 4;
 struct WgradParams {
   CUtensorMap tmap_a;          // tensor2d A: K-major dims {T, h} box {64, 128}; M-major dims {h, T} box {64, 64}
   CUtensorMap tmap_b;          // tensor2d B: N-major dims {i, T} box {64, 64}; K-major dims {T, i} box {64, BN}
-  CUtensorMap tmap_out;        // dense output: dims {i, h, L}, box {128 B of columns, 32, 1}, 128B swizzle
+  CUtensorMap tmap_out;        // dense output: dims {i, h, L}, box {128 B of columns, 32, 1}, 128B swizzle;
+                               // blocked FP32: dims {32, h, i/32, L}, box {32, 32, 2, 1}
   const CUtensorMap* a_maps;   // tensor_ragged K-major A: per-expert maps (dims {K_e, h}), else null
   const CUtensorMap* b_maps;   // tensor_ragged K-major B: per-expert maps (dims {K_e, i}), else null
   const CUtensorMap* out_maps; // discrete outputs: per-expert maps (dims {i, h}), else null
@@ -40,6 +41,7 @@ struct WgradParams {
   int tiles_n, tiles_per_expert;
   int a_mn, b_mn, out_dtype, accumulate;
   int a_blocked, b_blocked;     // MN-major operand as a 3-D map of 64-wide blocks (one box per slot)
+  int out_blocked;              // FP32 output map of 32-column blocks: one store per 64-column load
 };
 
 constexpr int kWgradEpiWarps = 4;
@@ -174,6 +176,34 @@ struct WgradPolicy {
       } else {
 #pragma unroll
         for (int k = 0; k < 64; ++k) v[k] = 0.f;
+      }
+      if constexpr (OS == 4) {
+        if (p.out_blocked) {  // inter % 64 == 0: both 32-column chunks exist; one 8 KB store for the pair
+          if (!rows_in) continue;
+          if (lane == 0) bulk_wait_read<0>();  // both boxes of the ring have been read
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              st_shared_v4(stg + j * 4096u + swz128w(lane, i), __float_as_uint(v[32 * j + 4 * i]),
+                           __float_as_uint(v[32 * j + 4 * i + 1]), __float_as_uint(v[32 * j + 4 * i + 2]),
+                           __float_as_uint(v[32 * j + 4 * i + 3]));
+          fence_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            const int blk = (w.n0 >> 5) + c0;  // first 32-column block of the pair
+            if (discrete) {
+              if (reduce) tma_reduce_add_3d(map, stg, 0, row0, blk);
+              else tma_store_3d(map, stg, 0, row0, blk);
+            } else {
+              if (reduce) tma_reduce_add_4d(map, stg, 0, row0, blk, e);
+              else tma_store_4d(map, stg, 0, row0, blk, e);
+            }
+            bulk_commit_group();
+          }
+          continue;
+        }
       }
 #pragma unroll
       for (int j = 0; j < kPerLoad; ++j) {
@@ -395,6 +425,7 @@ cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {
   prm.b_mn = (a.b_major == MGG_MAJOR_MN) ? 1 : 0;
   prm.a_blocked = Lc.a_blocked ? 1 : 0;
   prm.b_blocked = Lc.b_blocked ? 1 : 0;
+  prm.out_blocked = Lc.out_blocked ? 1 : 0;
   prm.out_dtype = a.out_dtype;
   prm.accumulate = a.accumulate != 0;
   const bool fp32 = a.out_dtype == MGG_FP32;

@@ -184,11 +184,18 @@ WGRAD_CASES = {
     # MN extents that are multiples of 64: MN-major operands through blocked 3-D maps
     "m_n_blocked": dict(a_major="m", hidden=256, inter=192),
     "m_n_blocked_acc_bf16": dict(a_major="m", hidden=320, inter=448, accumulate=True, out_dtype="bf16"),
+    # FP32 outputs with inter % 64 == 0: one TMA copy stores two 32-column chunks (blocked output map),
+    # for dense and per-expert outputs, overwrite and accumulate; hidden = 192 leaves warps with no rows
+    "out_blocked_ragged_discrete": dict(input_order="tensor_ragged", out_mode="discrete", inter=320),
+    "out_blocked_acc": dict(accumulate=True, inter=384),
+    "out_blocked_discrete_acc": dict(out_mode="discrete", accumulate=True, inter=256),
 }
 
 
 WGRAD_SCHED = [(c, "static") for c in WGRAD_CASES] + [("k_n_fp32", "dynamic"), ("k_n_fp32_acc", "dynamic"),
-                                                        ("ragged_k_n_discrete", "dynamic"), ("many_experts", "dynamic")]
+                                                        ("ragged_k_n_discrete", "dynamic"), ("many_experts", "dynamic"),
+                                                        ("out_blocked_ragged_discrete", "dynamic"),
+                                                        ("out_blocked_discrete_acc", "dynamic")]
 WGRAD_CASES["many_experts"] = dict(hidden=256, inter=128, counts=(256, 0, 2048, 0, 512, 256, 0, 768, 256, 1024))
 
 
