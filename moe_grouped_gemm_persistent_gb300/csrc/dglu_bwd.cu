@@ -26,10 +26,14 @@ namespace mgg {
 //  single CTA loads 48 KB per stage (3 stages next to the TMA-C ring), a CTA of a pair 32 KB
 //  (5 stages); a single CTA takes the TMA-C path when K <= kTmaCMaxK.
 
-template <int CS, int DS, bool TMAC, bool PAIR>
+// EPI: epilogue warps, 8 (two per TMEM sub-partition, each taking every other chunk) or 4.  Four
+// leave room for one more operand stage, which pays where the epilogue's per-element work is
+// light (dSwiGLU or dsReLU with 16-bit D_row); the dGeGLU / dSiTU-GLU math and fp32 D_row need 8.
+template <int CS, int DS, bool TMAC, bool PAIR, int EPI = 8>
 struct DgluCfg {
+  static_assert(EPI == 4 || EPI == 8, "one or two epilogue warps per TMEM sub-partition");
   static constexpr bool kTmaC = TMAC && CS == 2;
-  static constexpr int kEpiWarps = 8;
+  static constexpr int kEpiWarps = EPI;
   // C boxes per warp (TMA path).  Three boxes would let a refill wait for stores a use older, but
   // cost a pair one of its five operand stages, which measured 5-10% slower on every shape.
   static constexpr int kCRing = 2;
@@ -88,9 +92,9 @@ constexpr int kOpGlu = 0;
 constexpr int kOpSrelu = 1;
 
 // CS / DS: element size in bytes of C and D_row (2 = bf16/fp16, 4 = fp32).
-template <int BN, int CS, int DS, bool TMAC, bool PAIR, int OP>
+template <int BN, int CS, int DS, bool TMAC, bool PAIR, int OP, int EPI>
 struct DgluPolicy {
-  using Cfg = DgluCfg<CS, DS, TMAC, PAIR>;
+  using Cfg = DgluCfg<CS, DS, TMAC, PAIR, EPI>;
   static constexpr int kTileM = PAIR ? 2 * BM : BM;   // rows of a tile (a pair's tile spans both CTAs)
   static constexpr int kBLoad = PAIR ? BN / 2 : BN;   // B rows this CTA loads
   static constexpr int EPI_WARPS = Cfg::kEpiWarps;
@@ -719,18 +723,18 @@ struct DgluPolicy {
   }
 };
 
-template <int BN, int CS, int DS, bool TMAC, bool PAIR, int OP>
-__global__ void __launch_bounds__(cta_threads(DgluCfg<CS, DS, TMAC, PAIR>::kEpiWarps), 1)
+template <int BN, int CS, int DS, bool TMAC, bool PAIR, int OP, int EPI>
+__global__ void __launch_bounds__(cta_threads(DgluCfg<CS, DS, TMAC, PAIR, EPI>::kEpiWarps), 1)
     dglu_bwd_kernel(const __grid_constant__ DgluParams prm) {
-  const DgluPolicy<BN, CS, DS, TMAC, PAIR, OP> pol(prm);
-  persistent_gemm<BN, DgluCfg<CS, DS, TMAC, PAIR>::kStages, PAIR>(pol);
+  const DgluPolicy<BN, CS, DS, TMAC, PAIR, OP, EPI> pol(prm);
+  persistent_gemm<BN, DgluCfg<CS, DS, TMAC, PAIR, EPI>::kStages, PAIR>(pol);
 }
 
-template <int BN, int CS, int DS, bool TMAC, bool PAIR, int OP = kOpGlu>
+template <int BN, int CS, int DS, bool TMAC, bool PAIR, int OP = kOpGlu, int EPI = 8>
 static cudaError_t launch_dglu_variant(const DgluParams& prm, int num_sms, cudaStream_t stream) {
-  using C = DgluCfg<CS, DS, TMAC, PAIR>;
+  using C = DgluCfg<CS, DS, TMAC, PAIR, EPI>;
   constexpr int smem = SmemLayout<PAIR ? BN / 2 : BN, C::kStages, C::kEpiWarps, C::kStgBytes, num_acc(BN)>::DYN_BYTES;
-  auto kern = dglu_bwd_kernel<BN, CS, DS, TMAC, PAIR, OP>;
+  auto kern = dglu_bwd_kernel<BN, CS, DS, TMAC, PAIR, OP, EPI>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   static int max_units = 0;  // co-resident CTAs (pairs) of this variant, asked once
@@ -871,19 +875,24 @@ static cudaError_t launch_epi_gemm(const DgluLaunch& Lc, const EpiCall& a, cudaS
 
     const int cs = a.c_dtype == MGG_FP32 ? 4 : 2, ds = a.d_dtype == MGG_FP32 ? 4 : 2;
     const int n = Lc.num_sms;
+    // four epilogue warps (and one more operand stage) where the per-element work is light: the
+    // C ring with 16-bit D_row and the dsReLU or dSwiGLU math
+    const bool light = ds == 2 && (OP == kOpSrelu || a.act == MGG_ACT_DSWIGLU);
     if constexpr (OP == kOpSrelu) {  // 16-bit C through the TMA ring (the host checked C's dtype)
-      if (Lc.pair) err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, true, OP>(prm, n, stream)
-                                 : launch_dglu_variant<BN, 2, 4, true, true, OP>(prm, n, stream);
-      else err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, false, OP>(prm, n, stream)
-                         : launch_dglu_variant<BN, 2, 4, true, false, OP>(prm, n, stream);
+      if (Lc.pair) err = light ? launch_dglu_variant<BN, 2, 2, true, true, OP, 4>(prm, n, stream)
+                               : launch_dglu_variant<BN, 2, 4, true, true, OP>(prm, n, stream);
+      else err = light ? launch_dglu_variant<BN, 2, 2, true, false, OP, 4>(prm, n, stream)
+                       : launch_dglu_variant<BN, 2, 4, true, false, OP>(prm, n, stream);
     } else if (Lc.pair) {  // pairs take the C ring whenever C is 16-bit
-      if (cs == 2) err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, true>(prm, n, stream)
-                                 : launch_dglu_variant<BN, 2, 4, true, true>(prm, n, stream);
+      if (cs == 2 && light) err = launch_dglu_variant<BN, 2, 2, true, true, kOpGlu, 4>(prm, n, stream);
+      else if (cs == 2) err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, true>(prm, n, stream)
+                                      : launch_dglu_variant<BN, 2, 4, true, true>(prm, n, stream);
       else err = ds == 2 ? launch_dglu_variant<BN, 4, 2, false, true>(prm, n, stream)
                          : launch_dglu_variant<BN, 4, 4, false, true>(prm, n, stream);
     } else if (cs == 2 && a.K <= kTmaCMaxK) {
-      err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, false>(prm, n, stream)
-                    : launch_dglu_variant<BN, 2, 4, true, false>(prm, n, stream);
+      if (light) err = launch_dglu_variant<BN, 2, 2, true, false, kOpGlu, 4>(prm, n, stream);
+      else err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, false>(prm, n, stream)
+                         : launch_dglu_variant<BN, 2, 4, true, false>(prm, n, stream);
     } else if (cs == 2) {
       err = ds == 2 ? launch_dglu_variant<BN, 2, 2, false, false>(prm, n, stream)
                     : launch_dglu_variant<BN, 2, 4, false, false>(prm, n, stream);
