@@ -28,7 +28,7 @@ namespace mgg {
 
 // EPI: epilogue warps, 8 (two per TMEM sub-partition, each taking every other chunk) or 4.  Four
 // leave room for one more operand stage, which pays where the epilogue's per-element work is
-// light (dSwiGLU or dsReLU with 16-bit D_row); the dGeGLU / dSiTU-GLU math and fp32 D_row need 8.
+// light (dSwiGLU, dSiTU-GLU or dsReLU with 16-bit D_row); the dGeGLU math and fp32 D_row need 8.
 template <int CS, int DS, bool TMAC, bool PAIR, int EPI = 8>
 struct DgluCfg {
   static_assert(EPI == 4 || EPI == 8, "one or two epilogue warps per TMEM sub-partition");
@@ -76,12 +76,6 @@ struct DgluParams {
   int c_dtype, d_dtype, act, indicator, gate_first;
   float situ_b1, situ_b2, situ_inv_b1, situ_inv_b2;  // dSiTU-GLU scales and their reciprocals
 };
-
-__device__ __forceinline__ float fast_sigmoid(float x) { return rcp_approx(1.0f + __expf(-x)); }
-
-// tanh(x) = 1 - 2 / (1 + e^{2x}); saturates to +-1, absolute error ~1e-7 (enough for the
-// bf16/fp32 gradients it feeds).
-__device__ __forceinline__ float fast_tanh(float x) { return 1.0f - 2.0f * rcp_approx(1.0f + __expf(2.0f * x)); }
 
 // Byte offset of 16-byte chunk `c16` of row `r` in a 128B-swizzled staging box (rows of 128 B).
 __device__ __forceinline__ uint32_t swz128(int r, int c16) { return (uint32_t)(r * 128 + ((c16 ^ (r & 7)) << 4)); }
@@ -270,29 +264,56 @@ struct DgluPolicy {
   // input block, on exit dgate / dinput; returns this row's partial of sum_j R * act.
   // One activation over a 32-column chunk; the activation is fixed per launch, so the branch is
   // taken once per chunk and only that activation's unrolled loop runs.
-  // dSiTU-GLU, one element at a time (its two tanh terms leave little to pack).
+  // dSiTU-GLU on element pairs with the packed fp32 instructions, like dSwiGLU / dGeGLU below:
+  //   s = sigmoid(x_g), tg = tanh(x_g / b1), tu = tanh(x_i / b2), Tg = b1 tg s, Tu = b2 tu,
+  //   dTg = (1 - tg^2) s + Tg (1 - s), dTu = 1 - tu^2,
+  //   dgate = R p Tu dTg, dinput = R p Tg dTu, dprob += R Tg Tu,
+  // with tanh(y) = 1 - 2 / (1 + 2^(2 y log2 e)) and the sigmoid as below (SFU ex2 / rcp).
   template <int NV>
   __device__ __forceinline__ float dsitu_math(const uint32_t* r, float* gv, float* iv, float alpha2, float beta_g,
                                               float pr) const {
-    float dprob_acc = 0.f;
+    static_assert(NV % 2 == 0, "pairs of elements");
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float2 one2 = make_float2(1.0f, 1.0f);
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+    const float2 b2 = make_float2(beta_g, beta_g);
+    const float ap = alpha2 * pr;
+    const float2 ap2 = make_float2(ap, ap);
+    const float kg = 2.0f * kLog2e * p.situ_inv_b1, ku = 2.0f * kLog2e * p.situ_inv_b2;
+    const float2 kg2 = make_float2(kg, kg), ku2 = make_float2(ku, ku);
+    const float2 sb1 = make_float2(p.situ_b1, p.situ_b1), sb2 = make_float2(p.situ_b2, p.situ_b2);
+    const float2 m2 = make_float2(-2.0f, -2.0f);
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const float R = __fmul_rn(alpha2, __uint_as_float(r[k]));
-      const float x_g = __fmul_rn(beta_g, gv[k]);  // one fp32 product, never contracted
-      const float x_i = __fmul_rn(beta_g, iv[k]);
-      const float Rp = R * pr;
-      const float s = fast_sigmoid(x_g);
-      const float tg = fast_tanh(x_g * p.situ_inv_b1);
-      const float tu = fast_tanh(x_i * p.situ_inv_b2);
-      const float Tg = p.situ_b1 * tg * s;
-      const float Tu = p.situ_b2 * tu;
-      const float dTg = (1.0f - tg * tg) * s + p.situ_b1 * tg * s * (1.0f - s);
-      const float dTu = 1.0f - tu * tu;
-      dprob_acc += R * (Tg * Tu);
-      gv[k] = Rp * Tu * dTg;
-      iv[k] = Rp * Tg * dTu;
+    for (int k = 0; k < NV; k += 2) {
+      const float2 acc_v = make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1]));
+      const float2 xg = __fmul2_rn(b2, make_float2(gv[k], gv[k + 1]));  // one fp32 product each
+      const float2 xi = __fmul2_rn(b2, make_float2(iv[k], iv[k + 1]));
+      const float2 Rp = __fmul2_rn(acc_v, ap2);
+      const float2 zs = __fmul2_rn(xg, make_float2(-kLog2e, -kLog2e));
+      const float2 ds = __fadd2_rn(make_float2(ex2_approx(zs.x), ex2_approx(zs.y)), one2);
+      const float2 s = make_float2(rcp_approx(ds.x), rcp_approx(ds.y));
+      const float2 zg = __fmul2_rn(xg, kg2);
+      const float2 dgn = __fadd2_rn(make_float2(ex2_approx(zg.x), ex2_approx(zg.y)), one2);
+      const float2 tg = __ffma2_rn(make_float2(rcp_approx(dgn.x), rcp_approx(dgn.y)), m2, one2);
+      const float2 zu = __fmul2_rn(xi, ku2);
+      const float2 dun = __fadd2_rn(make_float2(ex2_approx(zu.x), ex2_approx(zu.y)), one2);
+      const float2 tu = __ffma2_rn(make_float2(rcp_approx(dun.x), rcp_approx(dun.y)), m2, one2);
+      const float2 Tg = __fmul2_rn(sb1, __fmul2_rn(tg, s));
+      const float2 Tu = __fmul2_rn(sb2, tu);
+      const float2 oms = __ffma2_rn(s, neg1, one2);                                   // 1 - s
+      const float2 omg = __ffma2_rn(__fmul2_rn(tg, tg), neg1, one2);                  // 1 - tg^2
+      const float2 dTg = __ffma2_rn(Tg, oms, __fmul2_rn(omg, s));
+      const float2 dTu = __ffma2_rn(__fmul2_rn(tu, tu), neg1, one2);                  // 1 - tu^2
+      const float2 dg = __fmul2_rn(__fmul2_rn(Rp, Tu), dTg);
+      const float2 di = __fmul2_rn(__fmul2_rn(Rp, Tg), dTu);
+      acc = __ffma2_rn(acc_v, __fmul2_rn(Tg, Tu), acc);
+      gv[k] = dg.x;
+      gv[k + 1] = dg.y;
+      iv[k] = di.x;
+      iv[k + 1] = di.y;
     }
-    return dprob_acc;
+    return alpha2 * (acc.x + acc.y);
   }
 
   // dSwiGLU / dGeGLU on element pairs with the packed fp32 instructions (add/mul/fma.f32x2): the
@@ -876,8 +897,8 @@ static cudaError_t launch_epi_gemm(const DgluLaunch& Lc, const EpiCall& a, cudaS
     const int cs = a.c_dtype == MGG_FP32 ? 4 : 2, ds = a.d_dtype == MGG_FP32 ? 4 : 2;
     const int n = Lc.num_sms;
     // four epilogue warps (and one more operand stage) where the per-element work is light: the
-    // C ring with 16-bit D_row and the dsReLU or dSwiGLU math
-    const bool light = ds == 2 && (OP == kOpSrelu || a.act == MGG_ACT_DSWIGLU);
+    // C ring with 16-bit D_row and the dsReLU, dSwiGLU or (packed) dSiTU-GLU math
+    const bool light = ds == 2 && (OP == kOpSrelu || a.act == MGG_ACT_DSWIGLU || a.act == MGG_ACT_DSITUGLU);
     if constexpr (OP == kOpSrelu) {  // 16-bit C through the TMA ring (the host checked C's dtype)
       if (Lc.pair) err = light ? launch_dglu_variant<BN, 2, 2, true, true, OP, 4>(prm, n, stream)
                                : launch_dglu_variant<BN, 2, 4, true, true, OP>(prm, n, stream);
