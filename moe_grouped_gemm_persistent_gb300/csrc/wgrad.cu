@@ -158,8 +158,8 @@ struct WgradPolicy {
     const bool add_old = p.accumulate && OS == 2;
     bool released = false;
     // One TMEM load per 64 accumulator columns (tcgen05.ld 32x32b.x64): two 32-column chunks of
-    // fp32 output or one 64-column chunk of 16-bit output.  Fewer, wider loads wait less on tensor
-    // memory while the MMA of the next tile writes the other accumulator.
+    // fp32 output or one 64-column chunk of 16-bit output (half the load-and-wait round trips of
+    // one load per 32 columns).
     constexpr int kPerLoad = 64 / CW;
 #pragma unroll 1
     for (int c0 = 0; c0 < nchunks; c0 += kPerLoad) {
