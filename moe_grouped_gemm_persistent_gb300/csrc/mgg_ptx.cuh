@@ -224,6 +224,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// tanh on the SFU (PTX tanh.approx, one MUFU operation; relative error about 2^-11).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Approximate reciprocal (one MUFU operation); rcp(+inf) = 0.
 __device__ __forceinline__ float rcp_approx(float x) {
   float y;
