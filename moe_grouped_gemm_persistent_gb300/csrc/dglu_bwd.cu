@@ -915,9 +915,10 @@ static cudaError_t launch_epi_gemm(const DgluLaunch& Lc, const EpiCall& a, cudaS
       if (light) err = launch_dglu_variant<BN, 2, 2, true, false, kOpGlu, 4>(prm, n, stream);
       else err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, false>(prm, n, stream)
                          : launch_dglu_variant<BN, 2, 4, true, false>(prm, n, stream);
-    } else if (cs == 2) {
-      err = ds == 2 ? launch_dglu_variant<BN, 2, 2, false, false>(prm, n, stream)
-                    : launch_dglu_variant<BN, 2, 4, false, false>(prm, n, stream);
+    } else if (cs == 2) {  // 16-bit C in registers one chunk ahead (single CTAs, K > kTmaCMaxK)
+      if (light) err = launch_dglu_variant<BN, 2, 2, false, false, kOpGlu, 4>(prm, n, stream);
+      else err = ds == 2 ? launch_dglu_variant<BN, 2, 2, false, false>(prm, n, stream)
+                         : launch_dglu_variant<BN, 2, 4, false, false>(prm, n, stream);
     } else {
       err = ds == 2 ? launch_dglu_variant<BN, 4, 2, false, false>(prm, n, stream)
                     : launch_dglu_variant<BN, 4, 4, false, false>(prm, n, stream);
