@@ -122,10 +122,24 @@ def measured_peaks():
     return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def source_sha() -> str:
+# The sources each recorded kernel is built from (its own translation unit, the shared headers,
+# the host code that encodes its tensor maps, the ABI header).
+KERNEL_SOURCES = {
+    "dglu_bwd_kernel": ("dglu_bwd.cu",),
+    "wgrad_kernel": ("wgrad.cu",),
+}
+SHARED_SOURCES = ("mgg_pipeline.cuh", "mgg_ptx.cuh", "mgg_internal.h", "mgg_api.cu")
+
+
+def source_sha(kernel: str = None) -> str:
+    """Hash of the CUDA sources: all of them, or those `kernel` is built from."""
     h = hashlib.sha1()
-    files = sorted(glob.glob(os.path.join(ROOT, "moe_grouped_gemm_persistent_gb300", "csrc", "*")) +
-                   glob.glob(os.path.join(ROOT, "include", "*.h")))
+    csrc = os.path.join(ROOT, "moe_grouped_gemm_persistent_gb300", "csrc")
+    if kernel is None:
+        files = glob.glob(os.path.join(csrc, "*"))
+    else:
+        files = [os.path.join(csrc, f) for f in KERNEL_SOURCES[kernel] + SHARED_SOURCES]
+    files = sorted(files + glob.glob(os.path.join(ROOT, "include", "*.h")))
     for f in files:
         with open(f, "rb") as fh:
             h.update(fh.read())
@@ -140,7 +154,7 @@ def recorded_traffic(kernel: str, workload: str):
     with open(p) as f:
         d = json.load(f)
     ent = d.get(f"{kernel}/{workload}")
-    if not ent or ent.get("source_sha") != source_sha():
+    if not ent or kernel not in KERNEL_SOURCES or ent.get("source_sha") != source_sha(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
