@@ -548,23 +548,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, int dtype) {
   return lo | (hi << 16);
 }
 
-// Stores the first `n` (a multiple of 8, <= 32) of 32 values at element `idx` of `base`.
-__device__ __forceinline__ void store32(void* base, int dtype, size_t idx, const float (&v)[32], int n = 32) {
-  if (dtype == MGG_FP32) {
-    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + idx);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (4 * i < n) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-  } else {
-    uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + idx);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (8 * i < n)
-        p[i] = make_uint4(pack2(v[8 * i], v[8 * i + 1], dtype), pack2(v[8 * i + 2], v[8 * i + 3], dtype),
-                          pack2(v[8 * i + 4], v[8 * i + 5], dtype), pack2(v[8 * i + 6], v[8 * i + 7], dtype));
-  }
-}
-
 // Like load32 but only the first `n` (multiple of 8) elements are read; the rest become 0.
 __device__ __forceinline__ void load32_n(const void* base, int dtype, size_t idx, float (&v)[32], int n) {
   if (n >= 32) {
