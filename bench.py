@@ -7,9 +7,14 @@ DeepSeek-like layer (L=256 experts, hidden 7168, N 2048, 131072 tokens Zipf(1.0)
 rounded to 256 per expert): the one workload that carries both halves.  Other
 workloads (--workload mixtral | geglu | wgrad64 | tiny) time whichever halves they have.
 
+By default the line also carries ``per_config``: the four other layers of the same
+benchmark family (tiny, mixtral, geglu, wgrad64) timed the same way, each part with its
+TFLOP/s, fraction of the measured dense BF16 peak, arithmetic intensity against the measured
+ridge point, the roof that bounds it and the fraction of that attainable roof.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mgg|reference] [--workload NAME]
 Under torchrun every rank runs an independent replica (weak scaling); rank 0 prints
-one JSON line.
+one JSON line.  ``--gpus N`` with N > 1 outside torchrun starts N local ranks itself.
 """
 from __future__ import annotations
 
@@ -157,6 +162,25 @@ def recorded_traffic(kernel: str, workload: str):
     if not ent or kernel not in KERNEL_SOURCES or ent.get("source_sha") != source_sha(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
+
+
+def roofline_of(flops: float, algo_bytes: float, ms: float, peaks) -> dict:
+    """Where one kernel launch sits against the measured roofs: its arithmetic intensity (FLOPs per
+    algorithmic byte) against the ridge point (dense BF16 peak / HBM copy bandwidth) decides the
+    binding roof, attainable = min(tensor peak, intensity x HBM bandwidth).  Work that would take
+    under 10 us at the attainable rate is bound by launch latency, not by either roof."""
+    peak_tf, bw = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    tf = flops / (ms * 1e-3) / 1e12
+    ai = flops / algo_bytes
+    ridge = peak_tf * 1e12 / (bw * 1e9)
+    attainable = min(peak_tf, ai * bw * 1e9 / 1e12)
+    bound = "tensor" if ai >= ridge else "hbm"
+    if flops / (attainable * 1e12) < 10e-6:
+        bound = "launch"
+    return {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_of_peak": round(tf / peak_tf, 4),
+            "algorithmic_gb": round(algo_bytes / 1e9, 4), "achieved_gbs": round(algo_bytes / (ms * 1e-3) / 1e9, 1),
+            "ai_flop_per_byte": round(ai, 1), "ridge_flop_per_byte": round(ridge, 1), "bound": bound,
+            "attainable_tflops": round(attainable, 1), "frac_of_attainable": round(tf / attainable, 4)}
 
 
 # ----------------------------------------------------------------------------------------
@@ -475,6 +499,38 @@ def max_over_ranks(value: float, dev) -> float:
     return float(t.item())
 
 
+PER_CONFIG = ("tiny", "mixtral", "geglu", "wgrad64")
+
+
+def time_per_config(dev, args, peaks) -> dict:
+    """The other layers of the benchmark family, each timed like the headline (warm-up, then
+    `steps` steps between CUDA events, per-part events), with the roofline of every part."""
+    import torch
+    out = {}
+    for name in PER_CONFIG:
+        prob = Problem(name, dev, args.sched, args.cta)
+        steps = max(args.steps, 50) if name == "tiny" else args.steps
+        total_ms, per, clocks = time_steps(prob, steps, args.warmup, 1)
+        flops, algo = prob.flops(), prob.algorithmic_bytes()
+        out[name] = {"description": WORKLOAD_TEXT[name], "steps": steps, "ms_per_step": round(total_ms / steps, 4),
+                     "parts": {k: roofline_of(flops[k], algo[k], ms, peaks) for k, ms in per.items()},
+                     "clocks": clocks}
+        del prob
+        torch.cuda.empty_cache()
+    return out
+
+
+def spawn_local_ranks(n: int) -> int:
+    """`--gpus N` outside torchrun: start N local ranks (one per GPU) with the same arguments."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd, cwd=ROOT)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -489,11 +545,18 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only --workload (by default an N=1 run also times tiny, mixtral, geglu, wgrad64)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
 
+    if args.gpus > 1 and os.environ.get("WORLD_SIZE") in (None, ""):
+        return spawn_local_ranks(args.gpus)
     world = env_int("WORLD_SIZE", 1)
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}: launch one rank per GPU", file=sys.stderr)
+        return 2
     rank = env_int("RANK", 0)
     local_rank = env_int("LOCAL_RANK", 0)
 
@@ -522,20 +585,26 @@ def main():
     value = step_flops * world / (ms_step * 1e-3) / 1e12
     peaks = measured_peaks()
 
-    parts = {}
-    for k, ms in per.items():
-        tf = flops[k] / (ms * 1e-3) / 1e12
-        parts[k] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
-                    "algorithmic_gb": round(prob.algorithmic_bytes()[k] / 1e9, 3),
-                    "achieved_gbs": round(prob.algorithmic_bytes()[k] / (ms * 1e-3) / 1e9, 1)}
+    algo = prob.algorithmic_bytes()
+    parts = {k: roofline_of(flops[k], algo[k], ms, peaks) for k, ms in per.items()}
     dom = max(per, key=lambda k: per[k])
-    ach = flops[dom] / (per[dom] * 1e-3) / 1e12
     kernel_name = {"dgrad": "dglu_bwd_kernel", "wgrad": "wgrad_kernel"}[dom]
-    roofline = {"kernel": kernel_name, "bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
-                "traffic": recorded_traffic(kernel_name, args.workload),
-                "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)",
-                "frac_of_sustained": round(ach / (peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]), 4)}
+    d = parts[dom]
+    tensor_side = {"tflops": d["tflops"], "tensor_peak_tflops": peaks["bf16_tflops"],
+                   "frac_of_tensor_peak": d["frac_of_peak"],
+                   "frac_of_sustained_tensor_peak": round(d["tflops"] / (peaks["bf16_tflops_sustained"]
+                                                                         or peaks["bf16_tflops"]), 4),
+                   "ai_flop_per_byte": d["ai_flop_per_byte"], "ridge_flop_per_byte": d["ridge_flop_per_byte"],
+                   "attainable_tflops": d["attainable_tflops"], "frac_of_attainable": d["frac_of_attainable"]}
+    if d["bound"] == "hbm":  # algorithmic bytes per launch / launch time against the measured copy rate
+        roofline = {"kernel": kernel_name, "bound": "hbm", "achieved": d["achieved_gbs"], "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(d["achieved_gbs"] / peaks["hbm_gbs"], 4)}
+    else:
+        roofline = {"kernel": kernel_name, "bound": "tensor", "achieved": d["tflops"], "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": d["frac_of_peak"]}
+    roofline.update({"traffic": recorded_traffic(kernel_name, args.workload),
+                     "algorithmic_bytes": int(algo[dom]), "flops": flops[dom],
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json: bf16 burst, HBM copy)", **tensor_side})
 
     e2e = None
     if not args.no_e2e:
@@ -552,6 +621,13 @@ def main():
         tf, spent, sample = oracle_sample(prob, dev, args.cpu_seconds)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                "seconds": round(spent, 2), "sample": f"whole experts, seeded order: {sample}"}
+    launches = prob.launches_per_step * args.steps
+
+    per_config = None
+    if world == 1 and args.workload == "deepseek" and not args.no_per_config:
+        del prob
+        torch.cuda.empty_cache()
+        per_config = time_per_config(dev, args, peaks)
 
     if rank == 0:
         line = {
@@ -563,8 +639,8 @@ def main():
                        if args.workload not in ("tiny",) else "inputs fit in L2 (tiny)",
                        "parallelism": f"replicas x{world}", "sched": args.sched, "cta": args.cta},
             "parts": parts, "roofline": roofline, "frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
-            "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
-            "gpu_launches": prob.launches_per_step * args.steps,
+            "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches,
+            "per_config": per_config,
         }
         print(json.dumps(line))
     if world > 1:
@@ -613,4 +689,4 @@ def run_reference(args, world, rank):
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MGG_ABI_VERSION 4
+#define MGG_ABI_VERSION 5
 
 typedef enum mgg_status {
   MGG_OK = 0,
@@ -54,7 +54,9 @@ typedef enum mgg_status {
   MGG_ERR_ARCH = 4,           /* no usable device, or the device is not sm_103 */
   MGG_ERR_DEVICE_OFFSETS = 5, /* device check: offsets not non-decreasing / not 256-multiples / wrong end */
   MGG_ERR_DEVICE_POINTER = 6, /* device check: a pointer-array entry is null or not 16-byte aligned */
-  MGG_ERR_DEVICE_TIMEOUT = 7  /* a pipeline wait inside a kernel exceeded its time limit */
+  MGG_ERR_DEVICE_TIMEOUT = 7, /* a pipeline wait inside a kernel exceeded its time limit */
+  MGG_ERR_DEVICE_BOUNDS = 8   /* bounds-checked build only: a computed global index or TMEM column
+                                 fell outside the call's extents; the access was skipped */
 } mgg_status;
 
 typedef enum mgg_dtype { MGG_BF16 = 0, MGG_FP16 = 1, MGG_FP32 = 2 } mgg_dtype;
@@ -244,6 +246,13 @@ size_t mgg_sizeof_dglu_bwd_args(void);
 size_t mgg_sizeof_dsrelu_bwd_args(void);
 size_t mgg_sizeof_wgrad_args(void);
 
+/* Byte offset of every field of one argument struct as compiled into the library, in declaration
+ * order (which = 0: mgg_dglu_bwd_args, 1: mgg_dsrelu_bwd_args, 2: mgg_wgrad_args).  Writes at most
+ * `cap` offsets into `out` (host memory; may be NULL when cap = 0) and returns the struct's number of
+ * fields, or -1 for an unknown `which`.  Lets a binding check its mirror of the structs field by
+ * field, not only by size. */
+int mgg_args_field_offsets(int which, size_t* out, int cap);
+
 /* Last error message of the calling thread ("" after a successful call). */
 const char* mgg_last_error(void);
 
@@ -283,10 +292,15 @@ mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream);
  * `workspace_bytes` are ignored: the scratch lives in a fixed array inside the library's
  * device memory, sized for at most 1024 experts (397,568 bytes, held on every GPU that loads
  * the library until the process exits); L above that returns MGG_ERR_VALUE.  Nothing is
- * allocated.  The first call on a device resolves the array's address with that device
- * current: make it before any stream capture.  Every call shares the array and it keeps the
- * last call's contents; calls that may overlap on the GPU race on it and must be ordered.
- * The device-side status word of these calls is not exposed. */
+ * allocated.  The first call on a device (and the first after its context was reset) looks
+ * the array's address up with that device current: make it before any stream capture.
+ * Every call shares the array and it keeps the last call's contents; calls that may overlap
+ * on the GPU race on it and must be ordered.
+ * The device-side status word of these calls is not exposed: when the offsets or out_ptrs
+ * contents fail the device check (see mgg_wgrad), the call still returns MGG_OK and leaves
+ * every output untouched.  Callers of this entry point must therefore check their offsets
+ * (non-decreasing, counts multiples of 256, last == tokens_sum) and output pointers (non-null,
+ * 16-byte aligned) on the host before the call. */
 mgg_status mgg_wgrad_noalloc(const mgg_wgrad_args* args, void* stream);
 
 /* Waits for `stream`, then returns the device-side status word of the last call that

@@ -6,7 +6,9 @@ import os
 import threading
 from ctypes import c_char_p, c_int, c_int32, c_int64, c_size_t, c_uint32, c_uint64, c_void_p
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmgg.so")
+# MGG_LIB_VARIANT=checked loads the bounds-checked debugging build (build.py --checked) instead.
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "libmgg_checked.so" if os.environ.get("MGG_LIB_VARIANT") == "checked" else "libmgg.so")
 
 MGG_OK = 0
 MGG_ERR_VALUE = 1
@@ -16,6 +18,7 @@ MGG_ERR_ARCH = 4
 MGG_ERR_DEVICE_OFFSETS = 5
 MGG_ERR_DEVICE_POINTER = 6
 MGG_ERR_DEVICE_TIMEOUT = 7
+MGG_ERR_DEVICE_BOUNDS = 8
 
 DTYPES = {"bf16": 0, "fp16": 1, "fp32": 2}
 ACTS = {"dswiglu": 0, "dgeglu": 1, "dsituglu": 2}
@@ -70,6 +73,7 @@ SIGNATURES = [
     ("mgg_sizeof_dglu_bwd_args", c_size_t, []),
     ("mgg_sizeof_dsrelu_bwd_args", c_size_t, []),
     ("mgg_sizeof_wgrad_args", c_size_t, []),
+    ("mgg_args_field_offsets", c_int, [c_int, ctypes.POINTER(c_size_t), c_int]),
     ("mgg_last_error", c_char_p, []),
     ("mgg_status_string", c_char_p, [c_int]),
     ("mgg_dglu_bwd_workspace_size", c_size_t, [c_int64, c_int64]),
@@ -86,6 +90,8 @@ SIGNATURES = [
     ("mgg_read_device_status", c_int, [c_void_p, c_void_p]),
     ("mgg_test_encode_tmap_2d", c_int, [c_void_p, c_void_p, c_uint64, c_uint64, c_uint64, c_uint32, c_uint32]),
     ("mgg_test_tmap_replace", c_int, [c_void_p, c_void_p, c_void_p, c_uint32, c_uint64, c_int, c_void_p]),
+    ("mgg_test_wait_timeout", c_int, [c_void_p, c_int64, c_int32, c_int32, c_void_p]),
+    ("mgg_test_build_flags", c_int, []),
 ]
 
 _lib = None

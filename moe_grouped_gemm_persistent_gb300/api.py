@@ -223,14 +223,15 @@ def wgrad(*, a: torch.Tensor, b: torch.Tensor, offsets: torch.Tensor, hidden: in
 def wgrad_noalloc(*, a: torch.Tensor, b: torch.Tensor, offsets: torch.Tensor, hidden: int, inter: int,
                   out: Optional[torch.Tensor] = None, out_ptrs: Optional[torch.Tensor] = None,
                   out_dtype: Optional[str] = None, a_major: str = "k", b_major: str = "n",
-                  input_order: str = "tensor2d", accumulate: bool = False, tile_log: Optional[torch.Tensor] = None,
-                  stream=None) -> None:
+                  input_order: str = "tensor2d", accumulate: bool = False, sched: str = "dynamic",
+                  tile_log: Optional[torch.Tensor] = None, stream=None, cta: str = "auto") -> None:
     """Grouped wgrad that allocates nothing (include/mgg.h, mgg_wgrad_noalloc): for callers that
     cannot allocate device memory; its scratch is a fixed array inside the library (<= 1024
-    experts).  Calls share that array, so calls that may overlap on the GPU must be ordered."""
+    experts).  Calls share that array, so calls that may overlap on the GPU must be ordered.
+    Its device-side checks are not reported: check offsets and output pointers on the host."""
     args = make_wgrad_args(a=a, b=b, offsets=offsets, hidden=hidden, inter=inter, out=out, out_ptrs=out_ptrs,
                            out_dtype=out_dtype, a_major=a_major, b_major=b_major, input_order=input_order,
-                           accumulate=accumulate, workspace=None, tile_log=tile_log)
+                           accumulate=accumulate, sched=sched, workspace=None, tile_log=tile_log, cta=cta)
     check(load().mgg_wgrad_noalloc(args, _stream(stream)))
 
 

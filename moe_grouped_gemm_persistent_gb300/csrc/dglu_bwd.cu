@@ -129,6 +129,11 @@ struct DgluPolicy {
     w.m0 = begin + (int)(u % mblocks) * kTileM;
     w.k0 = 0;
     w.num_kb = p.num_kb;
+    // checked build: a tile outside the call's extents is skipped by every role
+    if (!(MGG_IN_BOUNDS(p.status, g >= 0 && g < p.L, 401, g) &&
+          MGG_IN_BOUNDS(p.status, w.m0 >= begin && w.m0 + kTileM <= p.M, 402, w.m0) &&
+          MGG_IN_BOUNDS(p.status, w.n0 >= 0 && w.n0 < p.N, 403, w.n0)))
+      w.active = 0;
     return w;
   }
 
@@ -147,8 +152,9 @@ struct DgluPolicy {
       if constexpr (PAIR) tma_load_3d_pair(sb, &p.tmap_b, bar, kb * BK, ncol, w.expert);
       else tma_load_3d(sb, &p.tmap_b, bar, kb * BK, ncol, w.expert);
     } else {
-      const CUtensorMap* m = p.b_maps + w.expert;
-      if (kb == 0 && acq.first_use(w.expert)) tmap_acquire(m);
+      const int e = MGG_IN_BOUNDS(p.status, w.expert < p.L, 301, w.expert) ? w.expert : 0;
+      const CUtensorMap* m = p.b_maps + e;
+      if (kb == 0 && acq.first_use(e)) tmap_acquire(m);
       if (!p.b_mn) {
         load2(sb, m, bar, kb * BK, ncol);
       } else if (p.b_blocked) {
@@ -256,7 +262,9 @@ struct DgluPolicy {
   __device__ __forceinline__ void amax_flush(int g, int slot, float m) const {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if ((threadIdx.x & 31) == 0 && m > 0.f) atomicMax(reinterpret_cast<int*>(p.amax) + slot, __float_as_int(m));
+    if ((threadIdx.x & 31) == 0 && m > 0.f &&
+        MGG_IN_BOUNDS(p.status, slot >= 0 && slot < (OP == kOpGlu ? 2 : 1) * p.L, 104, slot))
+      atomicMax(reinterpret_cast<int*>(p.amax) + slot, __float_as_int(m));
     (void)g;
   }
 
@@ -392,7 +400,8 @@ struct DgluPolicy {
 
   __device__ __forceinline__ void dbias_partials(const TileWork& w, int j0, int lane, float (&gv)[32],
                                                  float (&iv)[32]) const {
-    dbias_add(w, j0, lane, warp_column_sums(gv, lane), warp_column_sums(iv, lane));
+    const float sg = warp_column_sums(gv, lane), si = warp_column_sums(iv, lane);
+    if (dbias_in_range(w, 2 * j0) && dbias_in_range(w, 2 * j0 + 32)) dbias_add(w, j0, lane, sg, si);
   }
 
   // Adds the column totals of a staged 32 x 32 fp32 box (128B-swizzled rows, as stage_block writes
@@ -427,6 +436,11 @@ struct DgluPolicy {
   __device__ __forceinline__ float* dbias_ws_at(const TileWork& w, int j0, int second) const {
     const int first_half = (p.gate_first != 0) == (second == 0) ? 0 : 32;
     return p.dbias_ws + (size_t)w.expert * 2 * (size_t)p.N + 2 * j0 + first_half;
+  }
+
+  // Checked build: the 32 fp32 dbias partials at column `col` of expert w.expert exist.
+  __device__ __forceinline__ bool dbias_in_range(const TileWork& w, int col) const {
+    return MGG_IN_BOUNDS(p.status, w.expert < p.L && col >= 0 && col + 32 <= 2 * p.N, 103, col);
   }
 
   // Adds this warp's column totals (lane l: gate column l in sg, input column l in si) of compact
@@ -537,13 +551,14 @@ struct DgluPolicy {
   __device__ void epilogue_tmac(const TileWork& w, long long t, uint32_t taddr, const EpiCtx& ctx,
                                 AccRelease rel) const {
     const int lane = ctx.lane, half = ctx.half;
-    const int g = w.expert;
+    const int g = MGG_IN_BOUNDS(p.status, w.expert < p.L, 101, w.expert) ? w.expert : 0;
     const float alpha_g = __ldg(p.alpha + g);
     const float alpha2 = alpha_g * alpha_g;
     const float beta_g = OP == kOpGlu ? __ldg(p.beta + g) : 1.0f;
     const int row0 = w.m0 + ctx.rank * BM + ctx.q * 32;
     const int row = row0 + lane;
-    const float pr = __ldg(p.prob + row);
+    const bool row_ok = MGG_IN_BOUNDS(p.status, row < p.M, 102, row);
+    const float pr = row_ok ? __ldg(p.prob + row) : 0.0f;
     const int nown = own_chunks(num_chunks(w), half);
     const uint32_t ring = smem_u32(ctx.stg);
     const int gblk = p.gate_first ? 0 : 1;
@@ -558,7 +573,8 @@ struct DgluPolicy {
       const uint32_t box = ring + (u % kCRing) * 4096;
       const int x = use_col(w, c);  // first C / D_row column of this use
       uint32_t r[32];
-      tmem_load_32cols(taddr + (OP == kOpGlu ? 32 : 64) * c, r);
+      const int tcol = (OP == kOpGlu ? 32 : 64) * c;  // this use's first accumulator column
+      tmem_load_32cols(taddr + (MGG_IN_BOUNDS(p.status, tcol + (OP == kOpGlu ? 32 : 64) <= BN, 105, tcol) ? tcol : 0), r);
       if (OP == kOpGlu && i == nown - 1) {
         rel(lane);
         released = true;
@@ -590,12 +606,12 @@ struct DgluPolicy {
           stage_block(box, lane, 0, gv);
           staging_flush(box, lane, p.gate_first ? x : x + 32, row0);
           // dbias column totals straight from the staged fp32 values (the exact D_row values)
-          if (db) box_dbias_add(box, lane, dbias_ws_at(w, j0, 0));
+          if (db && dbias_in_range(w, 2 * j0)) box_dbias_add(box, lane, dbias_ws_at(w, j0, 0));
           if (lane == 0) bulk_wait_read<0>();  // the gate half has left the box
           __syncwarp();
           stage_block(box, lane, 0, iv);
           staging_flush(box, lane, p.gate_first ? x + 32 : x, row0);
-          if (db) box_dbias_add(box, lane, dbias_ws_at(w, j0, 1));
+          if (db && dbias_in_range(w, 2 * j0 + 32)) box_dbias_add(box, lane, dbias_ws_at(w, j0, 1));
         }
         if (DS == 2 && p.dbias_ws != nullptr) dbias_partials(w, j0, lane, gv, iv);
       } else {
@@ -652,7 +668,7 @@ struct DgluPolicy {
     }
     if (!released) rel(lane);
     c_uses += (uint32_t)nown;
-    if (nown > 0) atomicAdd(p.dprob + row, dprob_acc);
+    if (nown > 0 && row_ok) atomicAdd(p.dprob + row, dprob_acc);
     if (want_amax && nown > 0) {
       if constexpr (OP == kOpGlu) {
         amax_flush(g, 2 * g, amx0);
@@ -667,13 +683,14 @@ struct DgluPolicy {
   __device__ void epilogue_regc(const TileWork& w, long long t, uint32_t taddr, const EpiCtx& ctx,
                                 AccRelease rel) const {
     const int lane = ctx.lane, half = ctx.half;
-    const int g = w.expert;
+    const int g = MGG_IN_BOUNDS(p.status, w.expert < p.L, 101, w.expert) ? w.expert : 0;
     const float alpha_g = __ldg(p.alpha + g);
     const float alpha2 = alpha_g * alpha_g;
     const float beta_g = __ldg(p.beta + g);
     const int row0 = w.m0 + ctx.rank * BM + ctx.q * 32;
-    const int row = row0 + lane;
-    const float pr = __ldg(p.prob + row);
+    const bool row_ok = MGG_IN_BOUNDS(p.status, row0 + ctx.lane < p.M, 102, row0 + ctx.lane);
+    const int row = row_ok ? row0 + lane : 0;  // checked build: a bad row reads row 0 and adds nothing
+    const float pr = row_ok ? __ldg(p.prob + row) : 0.0f;
     const size_t row_off = (size_t)row * 2 * (size_t)p.N;
     const uint32_t stg = smem_u32(ctx.stg);
     const int nchunks = num_chunks(w);
@@ -688,7 +705,7 @@ struct DgluPolicy {
     for (int c = half; c < nchunks; c += kEpiHalves) {
       const int j0 = w.n0 + c * 32;
       uint32_t r[32];
-      tmem_load_32cols(taddr + c * 32, r);
+      tmem_load_32cols(taddr + (MGG_IN_BOUNDS(p.status, c * 32 + 32 <= BN, 105, c) ? c * 32 : 0), r);
       if (c + kEpiHalves >= nchunks) {  // this warp's last read: the MMA warp may reuse the accumulator
         rel(lane);
         released = true;
@@ -729,7 +746,7 @@ struct DgluPolicy {
       }
     }
     if (!released) rel(lane);
-    if (half < nchunks) atomicAdd(p.dprob + row, dprob_acc);
+    if (half < nchunks && row_ok) atomicAdd(p.dprob + row, dprob_acc);
     if (want_amax && half < nchunks) {
       amax_flush(g, 2 * g, amx0);
       amax_flush(g, 2 * g + 1, amx1);
@@ -753,15 +770,15 @@ __global__ void __launch_bounds__(cta_threads(DgluCfg<CS, DS, TMAC, PAIR, EPI>::
 }
 
 template <int BN, int CS, int DS, bool TMAC, bool PAIR, int OP = kOpGlu, int EPI = 8>
-static cudaError_t launch_dglu_variant(const DgluParams& prm, int num_sms, cudaStream_t stream) {
+static cudaError_t launch_dglu_variant(const DgluParams& prm, int num_sms, int device, cudaStream_t stream) {
   using C = DgluCfg<CS, DS, TMAC, PAIR, EPI>;
   constexpr int smem = SmemLayout<PAIR ? BN / 2 : BN, C::kStages, C::kEpiWarps, C::kStgBytes, num_acc(BN)>::DYN_BYTES;
   auto kern = dglu_bwd_kernel<BN, CS, DS, TMAC, PAIR, OP, EPI>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  static int max_units = 0;  // co-resident CTAs (pairs) of this variant, asked once
-  return launch_persistent(kern, prm, prm.total_tiles, num_sms, PAIR, cta_threads(C::kEpiWarps), smem, &max_units,
-                           stream);
+  static UnitCache cache;  // co-resident CTAs (pairs) of this variant, asked once per device
+  return launch_persistent(kern, prm, prm.total_tiles, num_sms, PAIR, cta_threads(C::kEpiWarps), smem,
+                           cache.slot(device), stream);
 }
 
 // Checks the device-resident arguments, builds the per-expert weight maps and zeroes amax.
@@ -896,32 +913,32 @@ static cudaError_t launch_epi_gemm(const DgluLaunch& Lc, const EpiCall& a, cudaS
     prm.situ_inv_b2 = 1.0f / prm.situ_b2;
 
     const int cs = a.c_dtype == MGG_FP32 ? 4 : 2, ds = a.d_dtype == MGG_FP32 ? 4 : 2;
-    const int n = Lc.num_sms;
+    const int n = Lc.num_sms, dev = Lc.device;
     // four epilogue warps (and one more operand stage) where the per-element work is light: the
     // C ring with 16-bit D_row and the dsReLU, dSwiGLU or (packed) dSiTU-GLU math
     const bool light = ds == 2 && (OP == kOpSrelu || a.act == MGG_ACT_DSWIGLU || a.act == MGG_ACT_DSITUGLU);
     if constexpr (OP == kOpSrelu) {  // 16-bit C through the TMA ring (the host checked C's dtype)
-      if (Lc.pair) err = light ? launch_dglu_variant<BN, 2, 2, true, true, OP, 4>(prm, n, stream)
-                               : launch_dglu_variant<BN, 2, 4, true, true, OP>(prm, n, stream);
-      else err = light ? launch_dglu_variant<BN, 2, 2, true, false, OP, 4>(prm, n, stream)
-                       : launch_dglu_variant<BN, 2, 4, true, false, OP>(prm, n, stream);
+      if (Lc.pair) err = light ? launch_dglu_variant<BN, 2, 2, true, true, OP, 4>(prm, n, dev, stream)
+                               : launch_dglu_variant<BN, 2, 4, true, true, OP>(prm, n, dev, stream);
+      else err = light ? launch_dglu_variant<BN, 2, 2, true, false, OP, 4>(prm, n, dev, stream)
+                       : launch_dglu_variant<BN, 2, 4, true, false, OP>(prm, n, dev, stream);
     } else if (Lc.pair) {  // pairs take the C ring whenever C is 16-bit
-      if (cs == 2 && light) err = launch_dglu_variant<BN, 2, 2, true, true, kOpGlu, 4>(prm, n, stream);
-      else if (cs == 2) err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, true>(prm, n, stream)
-                                      : launch_dglu_variant<BN, 2, 4, true, true>(prm, n, stream);
-      else err = ds == 2 ? launch_dglu_variant<BN, 4, 2, false, true>(prm, n, stream)
-                         : launch_dglu_variant<BN, 4, 4, false, true>(prm, n, stream);
+      if (cs == 2 && light) err = launch_dglu_variant<BN, 2, 2, true, true, kOpGlu, 4>(prm, n, dev, stream);
+      else if (cs == 2) err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, true>(prm, n, dev, stream)
+                                      : launch_dglu_variant<BN, 2, 4, true, true>(prm, n, dev, stream);
+      else err = ds == 2 ? launch_dglu_variant<BN, 4, 2, false, true>(prm, n, dev, stream)
+                         : launch_dglu_variant<BN, 4, 4, false, true>(prm, n, dev, stream);
     } else if (cs == 2 && a.K <= kTmaCMaxK) {
-      if (light) err = launch_dglu_variant<BN, 2, 2, true, false, kOpGlu, 4>(prm, n, stream);
-      else err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, false>(prm, n, stream)
-                         : launch_dglu_variant<BN, 2, 4, true, false>(prm, n, stream);
+      if (light) err = launch_dglu_variant<BN, 2, 2, true, false, kOpGlu, 4>(prm, n, dev, stream);
+      else err = ds == 2 ? launch_dglu_variant<BN, 2, 2, true, false>(prm, n, dev, stream)
+                         : launch_dglu_variant<BN, 2, 4, true, false>(prm, n, dev, stream);
     } else if (cs == 2) {  // 16-bit C in registers one chunk ahead (single CTAs, K > kTmaCMaxK)
-      if (light) err = launch_dglu_variant<BN, 2, 2, false, false, kOpGlu, 4>(prm, n, stream);
-      else err = ds == 2 ? launch_dglu_variant<BN, 2, 2, false, false>(prm, n, stream)
-                         : launch_dglu_variant<BN, 2, 4, false, false>(prm, n, stream);
+      if (light) err = launch_dglu_variant<BN, 2, 2, false, false, kOpGlu, 4>(prm, n, dev, stream);
+      else err = ds == 2 ? launch_dglu_variant<BN, 2, 2, false, false>(prm, n, dev, stream)
+                         : launch_dglu_variant<BN, 2, 4, false, false>(prm, n, dev, stream);
     } else {
-      err = ds == 2 ? launch_dglu_variant<BN, 4, 2, false, false>(prm, n, stream)
-                    : launch_dglu_variant<BN, 4, 4, false, false>(prm, n, stream);
+      err = ds == 2 ? launch_dglu_variant<BN, 4, 2, false, false>(prm, n, dev, stream)
+                    : launch_dglu_variant<BN, 4, 4, false, false>(prm, n, dev, stream);
     }
     if (err != cudaSuccess) return err;
   }

@@ -1,6 +1,8 @@
 // C ABI of libmgg: host-side validation, TMA descriptor encoding, device checks, launch.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -75,9 +77,17 @@ mgg_status encode_bf16(CUtensorMap* map, const void* addr, int rank, const uint6
   return encode_map(map, MGG_BF16, addr, rank, dims, strides, box, what);
 }
 
+// One NVTX range per ABI call (host side: validation, descriptor encoding and the launches), so a
+// profiler timeline shows which call queued which kernels.  Costs nothing without a tool attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
 // ---------------------------------------------------------------- device check
 struct DevInfo {
   int num_sms;
+  int device;
 };
 
 mgg_status check_device(DevInfo* info) {
@@ -92,6 +102,7 @@ mgg_status check_device(DevInfo* info) {
     return fail(MGG_ERR_ARCH, "libmgg is built for sm_103a; the current device has compute capability " +
                                   std::to_string(major) + "." + std::to_string(minor));
   info->num_sms = sms;
+  info->device = dev;
   return MGG_OK;
 }
 
@@ -273,6 +284,51 @@ size_t mgg_sizeof_dsrelu_bwd_args(void) { return sizeof(mgg_dsrelu_bwd_args); }
 
 size_t mgg_sizeof_wgrad_args(void) { return sizeof(mgg_wgrad_args); }
 
+int mgg_args_field_offsets(int which, size_t* out, int cap) {
+#define MGG_OFF(S, f) offsetof(S, f)
+  static const size_t dglu[] = {
+      MGG_OFF(mgg_dglu_bwd_args, M), MGG_OFF(mgg_dglu_bwd_args, K), MGG_OFF(mgg_dglu_bwd_args, N),
+      MGG_OFF(mgg_dglu_bwd_args, L), MGG_OFF(mgg_dglu_bwd_args, a), MGG_OFF(mgg_dglu_bwd_args, b),
+      MGG_OFF(mgg_dglu_bwd_args, b_ptrs), MGG_OFF(mgg_dglu_bwd_args, c), MGG_OFF(mgg_dglu_bwd_args, padded_offsets),
+      MGG_OFF(mgg_dglu_bwd_args, alpha), MGG_OFF(mgg_dglu_bwd_args, beta), MGG_OFF(mgg_dglu_bwd_args, prob),
+      MGG_OFF(mgg_dglu_bwd_args, dprob), MGG_OFF(mgg_dglu_bwd_args, d_row), MGG_OFF(mgg_dglu_bwd_args, dbias),
+      MGG_OFF(mgg_dglu_bwd_args, d_col), MGG_OFF(mgg_dglu_bwd_args, amax), MGG_OFF(mgg_dglu_bwd_args, workspace),
+      MGG_OFF(mgg_dglu_bwd_args, tile_log), MGG_OFF(mgg_dglu_bwd_args, workspace_bytes),
+      MGG_OFF(mgg_dglu_bwd_args, tile_log_capacity), MGG_OFF(mgg_dglu_bwd_args, b_major),
+      MGG_OFF(mgg_dglu_bwd_args, c_dtype), MGG_OFF(mgg_dglu_bwd_args, d_dtype), MGG_OFF(mgg_dglu_bwd_args, act),
+      MGG_OFF(mgg_dglu_bwd_args, geglu_filter), MGG_OFF(mgg_dglu_bwd_args, gate_first),
+      MGG_OFF(mgg_dglu_bwd_args, sched), MGG_OFF(mgg_dglu_bwd_args, cta_mode), MGG_OFF(mgg_dglu_bwd_args, situ_beta1),
+      MGG_OFF(mgg_dglu_bwd_args, situ_beta2)};
+  static const size_t dsrelu[] = {
+      MGG_OFF(mgg_dsrelu_bwd_args, M), MGG_OFF(mgg_dsrelu_bwd_args, K), MGG_OFF(mgg_dsrelu_bwd_args, N),
+      MGG_OFF(mgg_dsrelu_bwd_args, L), MGG_OFF(mgg_dsrelu_bwd_args, a), MGG_OFF(mgg_dsrelu_bwd_args, b),
+      MGG_OFF(mgg_dsrelu_bwd_args, b_ptrs), MGG_OFF(mgg_dsrelu_bwd_args, c),
+      MGG_OFF(mgg_dsrelu_bwd_args, padded_offsets), MGG_OFF(mgg_dsrelu_bwd_args, alpha),
+      MGG_OFF(mgg_dsrelu_bwd_args, prob), MGG_OFF(mgg_dsrelu_bwd_args, dprob), MGG_OFF(mgg_dsrelu_bwd_args, d_row),
+      MGG_OFF(mgg_dsrelu_bwd_args, d_col), MGG_OFF(mgg_dsrelu_bwd_args, amax), MGG_OFF(mgg_dsrelu_bwd_args, workspace),
+      MGG_OFF(mgg_dsrelu_bwd_args, tile_log), MGG_OFF(mgg_dsrelu_bwd_args, workspace_bytes),
+      MGG_OFF(mgg_dsrelu_bwd_args, tile_log_capacity), MGG_OFF(mgg_dsrelu_bwd_args, b_major),
+      MGG_OFF(mgg_dsrelu_bwd_args, c_dtype), MGG_OFF(mgg_dsrelu_bwd_args, d_dtype),
+      MGG_OFF(mgg_dsrelu_bwd_args, sched), MGG_OFF(mgg_dsrelu_bwd_args, cta_mode),
+      MGG_OFF(mgg_dsrelu_bwd_args, reserved)};
+  static const size_t wgrad[] = {
+      MGG_OFF(mgg_wgrad_args, hidden), MGG_OFF(mgg_wgrad_args, inter), MGG_OFF(mgg_wgrad_args, L),
+      MGG_OFF(mgg_wgrad_args, tokens_sum), MGG_OFF(mgg_wgrad_args, a), MGG_OFF(mgg_wgrad_args, b),
+      MGG_OFF(mgg_wgrad_args, offsets), MGG_OFF(mgg_wgrad_args, out), MGG_OFF(mgg_wgrad_args, out_ptrs),
+      MGG_OFF(mgg_wgrad_args, workspace), MGG_OFF(mgg_wgrad_args, tile_log), MGG_OFF(mgg_wgrad_args, workspace_bytes),
+      MGG_OFF(mgg_wgrad_args, tile_log_capacity), MGG_OFF(mgg_wgrad_args, a_major), MGG_OFF(mgg_wgrad_args, b_major),
+      MGG_OFF(mgg_wgrad_args, input_order), MGG_OFF(mgg_wgrad_args, out_dtype), MGG_OFF(mgg_wgrad_args, accumulate),
+      MGG_OFF(mgg_wgrad_args, sched), MGG_OFF(mgg_wgrad_args, cta_mode), MGG_OFF(mgg_wgrad_args, reserved1)};
+#undef MGG_OFF
+  const size_t* tab = which == 0 ? dglu : which == 1 ? dsrelu : which == 2 ? wgrad : nullptr;
+  const int n = which == 0 ? (int)(sizeof(dglu) / sizeof(size_t))
+              : which == 1 ? (int)(sizeof(dsrelu) / sizeof(size_t))
+              : which == 2 ? (int)(sizeof(wgrad) / sizeof(size_t)) : -1;
+  if (tab == nullptr) return -1;
+  for (int i = 0; i < n && i < cap && out != nullptr; ++i) out[i] = tab[i];
+  return n;
+}
+
 const char* mgg_last_error(void) { return g_err.c_str(); }
 
 const char* mgg_status_string(int s) {
@@ -285,6 +341,7 @@ const char* mgg_status_string(int s) {
     case MGG_ERR_DEVICE_OFFSETS: return "MGG_ERR_DEVICE_OFFSETS";
     case MGG_ERR_DEVICE_POINTER: return "MGG_ERR_DEVICE_POINTER";
     case MGG_ERR_DEVICE_TIMEOUT: return "MGG_ERR_DEVICE_TIMEOUT";
+    case MGG_ERR_DEVICE_BOUNDS: return "MGG_ERR_DEVICE_BOUNDS";
     default: return "MGG_UNKNOWN_STATUS";
   }
 }
@@ -301,7 +358,7 @@ size_t mgg_dsrelu_bwd_workspace_size(int64_t L) {
 
 size_t mgg_wgrad_workspace_size(int64_t L) {
   if (L < 0) return 0;
-  return round_up(kWsHeaderBytes + 3 * kTmapBytes * (size_t)L + sizeof(int32_t) * (size_t)L, 256);
+  return wgrad_workspace_bytes((size_t)L);
 }
 
 int64_t mgg_dglu_bwd_num_tiles(int64_t M, int64_t N) {
@@ -391,6 +448,7 @@ extern "C" {
 
 mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream) {
   g_err.clear();
+  const NvtxRange range("mgg_dglu_bwd");
   if (args == nullptr) return fail(MGG_ERR_VALUE, "args is NULL");
   const mgg_dglu_bwd_args& a = *args;
   mgg_status s = validate_dglu(a);
@@ -402,6 +460,7 @@ mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream) {
   memset(&Lc, 0, sizeof(Lc));
   Lc.args = args;
   Lc.num_sms = dev.num_sms;
+  Lc.device = dev.device;
   Lc.tile_n = kDgluTileN;
   Lc.pair = dglu_pair(a);
   if ((s = build_epi_maps(Lc, a.a, a.b, a.b_ptrs, a.b_major, a.c, a.c_dtype, a.d_row, a.d_col, a.d_dtype, a.M, a.K,
@@ -412,6 +471,7 @@ mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream) {
 
 mgg_status mgg_dsrelu_bwd(const mgg_dsrelu_bwd_args* args, void* stream) {
   g_err.clear();
+  const NvtxRange range("mgg_dsrelu_bwd");
   if (args == nullptr) return fail(MGG_ERR_VALUE, "args is NULL");
   const mgg_dsrelu_bwd_args& a = *args;
   mgg_status s = validate_dsrelu(a);
@@ -423,6 +483,7 @@ mgg_status mgg_dsrelu_bwd(const mgg_dsrelu_bwd_args* args, void* stream) {
   memset(&Lc, 0, sizeof(Lc));
   Lc.args = nullptr;
   Lc.num_sms = dev.num_sms;
+  Lc.device = dev.device;
   Lc.tile_n = kDgluTileN;
   Lc.pair = a.cta_mode != MGG_CTA_SINGLE;  // AUTO: pairs, as for the dGLU dgrad
   if ((s = build_epi_maps(Lc, a.a, a.b, a.b_ptrs, a.b_major, a.c, a.c_dtype, a.d_row, a.d_col, a.d_dtype, a.M, a.K,
@@ -433,6 +494,7 @@ mgg_status mgg_dsrelu_bwd(const mgg_dsrelu_bwd_args* args, void* stream) {
 
 mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {
   g_err.clear();
+  const NvtxRange range("mgg_wgrad");
   if (args == nullptr) return fail(MGG_ERR_VALUE, "args is NULL");
   const mgg_wgrad_args& a = *args;
   mgg_status s = validate_wgrad(a);
@@ -444,6 +506,7 @@ mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {
   memset(&Lc, 0, sizeof(Lc));
   Lc.args = args;
   Lc.num_sms = dev.num_sms;
+  Lc.device = dev.device;
   Lc.tile_n = wgrad_tile_n(a.inter);
   Lc.pair = wgrad_pair(a);
   const bool ragged = a.input_order == MGG_ORDER_TENSOR_RAGGED;

@@ -17,6 +17,12 @@ namespace mgg {
 constexpr size_t kWsHeaderBytes = 256;
 constexpr size_t kTmapBytes = 128;
 
+// Workspace bytes of one mgg_wgrad call with L experts: the header, three tensor maps per expert
+// (ragged A, ragged B, discrete output) and the expert order (int32 per expert), rounded to 256.
+constexpr size_t wgrad_workspace_bytes(size_t L) {
+  return (kWsHeaderBytes + 3 * kTmapBytes * L + sizeof(int32_t) * L + 255) / 256 * 256;
+}
+
 struct DgluLaunch {
   CUtensorMap tmap_a;
   CUtensorMap tmap_b;  // dense 3-D map, or the per-expert template (discrete)
@@ -25,6 +31,7 @@ struct DgluLaunch {
   CUtensorMap tmap_dcol;  // D_col store map (when requested)
   const mgg_dglu_bwd_args* args;  // null for mgg_dsrelu_bwd
   int num_sms;
+  int device;      // ordinal of the current device (keys the per-device occupancy caches)
   int tile_n;
   bool pair;       // 256-row tiles on CTA pairs (B maps load half a tile's columns)
   bool b_blocked;  // discrete N-major B as a 3-D map of 64-column blocks (one box per slot)
@@ -36,6 +43,7 @@ struct WgradLaunch {
   CUtensorMap tmap_out;  // dense output (3-D) map, or the per-expert template (discrete)
   const mgg_wgrad_args* args;
   int num_sms;
+  int device;      // ordinal of the current device
   int tile_n;
   bool a_ragged;  // per-expert A maps built on the device
   bool b_ragged;

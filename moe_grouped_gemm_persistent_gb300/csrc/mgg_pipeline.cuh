@@ -36,6 +36,8 @@
 //        called exactly once per tile when have_acc, after the warp's last tcgen05.ld of it.
 #pragma once
 
+#include <atomic>
+
 #include "mgg_ptx.cuh"
 
 namespace mgg {
@@ -464,12 +466,23 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   }
 }
 
+// Co-resident units (CTAs, or CTA pairs) of one kernel variant, per device ordinal (0 = not yet
+// asked): devices of one process may differ in how many clusters they can hold.
+struct UnitCache {
+  static constexpr int kDevices = 64;
+  std::atomic<int> units[kDevices];
+  // The cache slot of `device`, or null (ask every time) for an ordinal past the table.
+  std::atomic<int>* slot(int device) { return device >= 0 && device < kDevices ? &units[device] : nullptr; }
+};
+
 // Launches a persistent kernel: one CTA per SM (single) or one cluster of two CTAs per SM pair,
 // never more units than tiles.  `max_units` caches the number of co-resident units of this
-// kernel (0 = not yet known); a pair needs both SMs of a cluster slot, so it asks the runtime.
+// kernel on the current device (0 = not yet known; null = no cache); a pair needs both SMs of a
+// cluster slot, so it asks the runtime.
 template <class Prm>
 inline cudaError_t launch_persistent(void (*kern)(Prm), const Prm& prm, long long total_tiles, int num_sms,
-                                     bool pair, int threads, int smem, int* max_units, cudaStream_t stream) {
+                                     bool pair, int threads, int smem, std::atomic<int>* max_units,
+                                     cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3((unsigned)threads, 1, 1);
@@ -483,7 +496,7 @@ inline cudaError_t launch_persistent(void (*kern)(Prm), const Prm& prm, long lon
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  int units = *max_units;
+  int units = max_units != nullptr ? max_units->load(std::memory_order_relaxed) : 0;
   if (units <= 0) {
     if (pair) {
       cfg.gridDim = dim3(2, 1, 1);
@@ -493,7 +506,7 @@ inline cudaError_t launch_persistent(void (*kern)(Prm), const Prm& prm, long lon
     } else {
       units = num_sms;
     }
-    *max_units = units;
+    if (max_units != nullptr) max_units->store(units, std::memory_order_relaxed);
   }
   if (total_tiles < units) units = (int)total_tiles;
   cfg.gridDim = dim3((unsigned)(pair ? 2 * units : units), 1, 1);

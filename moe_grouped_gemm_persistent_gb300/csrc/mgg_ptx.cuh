@@ -66,22 +66,24 @@ struct WaitGuard {
   int* status;               // global status word of the call
 };
 
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitGuard g, int where) {
-  const unsigned long long t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 128; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*g.abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *g.abort_flag = 1;
-      if (atomicCAS(g.status, 0, (int)MGG_ERR_DEVICE_TIMEOUT) == 0) {
-        g.status[1] = where;
-        g.status[2] = (int)blockIdx.x;
-      }
-      return false;
-    }
+// Records a pipeline timeout: raises the CTA's abort flag and, if no earlier error was recorded,
+// writes MGG_ERR_DEVICE_TIMEOUT, the waiting role (`where`) and the CTA into the status word.
+__device__ __forceinline__ void record_timeout(WaitGuard g, int where) {
+  *g.abort_flag = 1;
+  if (atomicCAS(g.status, 0, (int)MGG_ERR_DEVICE_TIMEOUT) == 0) {
+    g.status[1] = where;
+    g.status[2] = (int)blockIdx.x;
   }
+}
+
+// Polls the barrier until the phase completes (true), another role of the CTA aborted (false) or
+// `limit_ns` passed (timeout recorded, false).  CLUSTER: the acquire covers a peer CTA's release.
+template <bool CLUSTER>
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, WaitGuard g, int where,
+                                                  unsigned long long limit_ns);
+
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitGuard g, int where) {
+  return mbar_wait_bounded<false>(bar, parity, g, where, kWaitLimitNs);
 }
 
 // Waits for the phase with parity `parity` to complete.  Returns false on timeout/abort.
@@ -90,6 +92,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitGu
   if (mbar_try_wait(a, parity)) return true;
   return mbar_wait_slow(a, parity, g, where);
 }
+
+// ------------------------------------------------------------------------------------
+// bounds-checked build (MGG_CHECKED): every computed global index, tensor-map slot and TMEM
+// column the kernels use is tested against the call's extents before the access; a failure
+// records MGG_ERR_DEVICE_BOUNDS (where, offending value) in the status word and the access is
+// skipped.  In the normal build the checks compile away.
+// ------------------------------------------------------------------------------------
+#ifdef MGG_CHECKED
+static __device__ __noinline__ bool bounds_fail(int* status, int where, long long value) {
+  if (atomicCAS(status, 0, (int)MGG_ERR_DEVICE_BOUNDS) == 0) {
+    status[1] = where;
+    status[2] = (int)(value > 0x7fffffffLL ? 0x7fffffffLL : value < -0x7fffffffLL ? -0x7fffffffLL : value);
+  }
+  return false;
+}
+#define MGG_IN_BOUNDS(status, ok, where, value) ((ok) ? true : ::mgg::bounds_fail((status), (where), (long long)(value)))
+#else
+#define MGG_IN_BOUNDS(status, ok, where, value) true
+#endif
 
 // ------------------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), tensor-map fences
@@ -386,22 +407,24 @@ __device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint32_t bar, uint32_t
   return ok;
 }
 
-static __device__ __noinline__ bool mbar_wait_slow_cluster(uint32_t bar, uint32_t parity, WaitGuard g, int where) {
+template <bool CLUSTER>
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, WaitGuard g, int where,
+                                                  unsigned long long limit_ns) {
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 128; ++i)
-      if (mbar_try_wait_cluster(bar, parity)) return true;
+      if (CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*g.abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *g.abort_flag = 1;
-      if (atomicCAS(g.status, 0, (int)MGG_ERR_DEVICE_TIMEOUT) == 0) {
-        g.status[1] = where;
-        g.status[2] = (int)blockIdx.x;
-      }
+    if (globaltimer_ns() - t0 > limit_ns) {
+      record_timeout(g, where);
       return false;
     }
   }
+}
+
+static __device__ __noinline__ bool mbar_wait_slow_cluster(uint32_t bar, uint32_t parity, WaitGuard g, int where) {
+  return mbar_wait_bounded<true>(bar, parity, g, where, kWaitLimitNs);
 }
 
 // Bounded wait whose acquire covers writes released by the peer CTA of the pair.

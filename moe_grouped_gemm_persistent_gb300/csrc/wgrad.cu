@@ -82,16 +82,24 @@ struct WgradPolicy {
     const long long idx = !p.dynamic ? t : (t & 1) ? total_tiles - 1 - (t >> 1) : (t >> 1);
     const int slot = (int)(idx / p.tiles_per_expert);
     const int local = (int)(idx % p.tiles_per_expert);
-    const int e = __ldg(p.order + slot);
+    TileWork w;
+    // checked build: an expert slot or order entry outside [0, L) makes the tile a skipped one
+    const bool slot_ok = MGG_IN_BOUNDS(p.status, slot >= 0 && slot < p.L, 411, slot);
+    const int e = slot_ok ? __ldg(p.order + slot) : 0;
+    if (!MGG_IN_BOUNDS(p.status, e >= 0 && e < p.L, 412, e) || !slot_ok) {
+      w = TileWork{0, 0, 0, 0, 0, 0};
+      return w;
+    }
     const int begin = e ? __ldg(p.offsets + e - 1) : 0;
     const int end = __ldg(p.offsets + e);
-    TileWork w;
     w.expert = e;
     w.active = (end > begin) || !p.accumulate;
     w.m0 = (local / p.tiles_n) * kTileM;
     w.n0 = (local % p.tiles_n) * BN;
     w.k0 = begin;
     w.num_kb = (end - begin) / BK;
+    if (!(MGG_IN_BOUNDS(p.status, w.m0 < p.hidden, 413, w.m0) && MGG_IN_BOUNDS(p.status, w.n0 < p.inter, 414, w.n0)))
+      w.active = 0;
     return w;
   }
 
@@ -166,7 +174,8 @@ struct WgradPolicy {
       float v[64];
       if (have_acc) {
         uint32_t r[64];
-        tmem_load_64cols(taddr + c0 * CW, r);  // BN is a multiple of 64: never past this accumulator
+        // BN is a multiple of 64: never past this accumulator
+        tmem_load_64cols(taddr + (MGG_IN_BOUNDS(p.status, c0 * CW + 64 <= BN, 204, c0) ? c0 * CW : 0), r);
 #pragma unroll
         for (int k = 0; k < 64; ++k) v[k] = __uint_as_float(r[k]);
         if (c0 + kPerLoad >= nchunks) {
@@ -210,7 +219,7 @@ struct WgradPolicy {
         const int c = c0 + j;
         if (c >= nchunks) break;
         const int col0 = w.n0 + c * CW;
-        if (add_old && row < p.hidden) {
+        if (add_old && row < p.hidden && MGG_IN_BOUNDS(p.status, e < p.L && col0 < p.inter, 202, col0)) {
           const char* base = discrete ? reinterpret_cast<const char*>(__ldg(p.out_ptrs + e))
                                       : static_cast<const char*>(p.out) + (size_t)e * p.hidden * (size_t)p.inter * OS;
           const int n = p.inter - col0 < CW ? p.inter - col0 : CW;
@@ -370,9 +379,9 @@ static cudaError_t launch_wgrad_bn(const WgradLaunch& Lc, WgradParams& prm, cuda
   auto kern = wgrad_kernel<BN, STAGES, OS, PAIR>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::DYN_BYTES);
   if (err != cudaSuccess) return err;
-  static int max_units = 0;  // co-resident CTAs (pairs) of this variant, asked once
+  static UnitCache cache;  // co-resident CTAs (pairs) of this variant, asked once per device
   return launch_persistent(kern, prm, prm.total_tiles, Lc.num_sms, PAIR, cta_threads(kWgradEpiWarps), S::DYN_BYTES,
-                           &max_units, stream);
+                           cache.slot(Lc.device), stream);
 }
 
 cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {

@@ -8,7 +8,7 @@ BF16/FP16/FP32 numbers (the caller decodes storage); results are float64 before
 any output rounding.  Matrix products use numpy's float64 matmul as a library
 step; nothing is blocked, fused or reordered beyond the definitions.
 
-Readings of the pages that the oracle fixes (each also listed in the design doc):
+Readings of the pages that the oracle fixes, where they are silent or ambiguous:
 
 * gate/input block order: gate first by default (dGLU page, BF16 contract:
   "alternating 32-wide gate/input blocks"); ``gate_first=False`` gives the

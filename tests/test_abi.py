@@ -39,10 +39,38 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_struct_layouts_match_library(lib):
-    assert lib.mgg_abi_version() == 4
+    assert lib.mgg_abi_version() == 5
     assert lib.mgg_sizeof_dglu_bwd_args() == ctypes.sizeof(_lib.DgluBwdArgs)
     assert lib.mgg_sizeof_dsrelu_bwd_args() == ctypes.sizeof(_lib.DsreluBwdArgs)
     assert lib.mgg_sizeof_wgrad_args() == ctypes.sizeof(_lib.WgradArgs)
+
+
+@pytest.mark.parametrize("which,struct", [(0, _lib.DgluBwdArgs), (1, _lib.DsreluBwdArgs), (2, _lib.WgradArgs)])
+def test_struct_field_offsets_match_library(lib, which, struct):
+    """Field by field: two swapped fields of equal size would pass a sizeof check."""
+    n = lib.mgg_args_field_offsets(which, None, 0)
+    assert n == len(struct._fields_)
+    buf = (ctypes.c_size_t * n)()
+    assert lib.mgg_args_field_offsets(which, buf, n) == n
+    want = [getattr(struct, name).offset for name, _ in struct._fields_]
+    assert list(buf) == want
+    assert lib.mgg_args_field_offsets(3, None, 0) == -1
+
+
+def test_struct_fields_follow_the_header_order():
+    """The ctypes mirror lists the fields of include/mgg.h's structs in the header's order."""
+    text = open(os.path.join(ROOT, "include", "mgg.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    for cname, struct in (("mgg_dglu_bwd_args", _lib.DgluBwdArgs), ("mgg_dsrelu_bwd_args", _lib.DsreluBwdArgs),
+                          ("mgg_wgrad_args", _lib.WgradArgs)):
+        body = re.search(r"typedef struct %s \{(.*?)\} %s;" % (cname, cname), text, flags=re.S).group(1)
+        names = []
+        for decl in filter(None, (d.strip() for d in body.split(";"))):
+            # "type a, b, c": the first declarator follows the type, the others follow commas
+            parts = decl.split(",")
+            names.append(re.split(r"[\s\*]+", parts[0].strip())[-1])
+            names += [p.strip().lstrip("*") for p in parts[1:]]
+        assert names == [f for f, _ in struct._fields_], cname
 
 
 def test_sizes_and_tile_counts(lib):
@@ -55,8 +83,9 @@ def test_sizes_and_tile_counts(lib):
     assert lib.mgg_wgrad_num_tiles(64, 2048, 1408) == 64 * 16 * 6
     assert lib.mgg_wgrad_num_tiles(4, 256, 128) == 4 * 2 * 1
     assert lib.mgg_wgrad_num_tiles(256, 7168, 2048) == 256 * 56 * 8
-    for s in range(8):
+    for s in range(9):
         assert lib.mgg_status_string(s).decode().startswith("MGG_")
+    assert lib.mgg_status_string(8).decode() == "MGG_ERR_DEVICE_BOUNDS"
 
 
 FAKE = 1 << 20  # an aligned address; validation never dereferences pointers

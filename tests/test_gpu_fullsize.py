@@ -3,8 +3,10 @@ checked against the CPU oracle on sampled rows / elements (the oracle evaluates 
 expert at a time), plus properties that hold at any size:
 
 * dgrad: sampled D_row rows and dprob entries vs the oracle (per sampled expert as well);
-  the tile log equals the oracle's schedule exactly; dbias equals the per-expert column sums
-  of the kernel's own D_row, with zero rows for empty experts.
+  the tile log equals the oracle's schedule exactly; dbias of three whole experts (the
+  smallest, the largest and a random one) vs the oracle's per-expert column sums, and for every
+  expert the column sums of the kernel's own D_row, with zero rows for empty experts.
+* dsReLU: the per-expert amax of whole experts vs the oracle's.
 * wgrad: sampled output elements of many experts and every element of a few experts vs the
   oracle; accumulate leaves empty experts bit-identical; the tile log equals the schedule.
 """
@@ -29,6 +31,31 @@ def dev():
 
 def f32(t):
     return t.detach().float().cpu().numpy()
+
+
+def oracle_whole_expert(spec, x, g, chunk=2048):
+    """The oracle on every row of expert g, evaluated as local one-expert problems over row chunks
+    (the rows partition the expert, so the column sums add up and the maxima combine): returns
+    (dbias row of expert g, amax entry of expert g)."""
+    lo, hi = oracle.expert_ranges(np.cumsum(spec.counts))[g]
+    bm = x["b"][g]
+    b_g = f32(bm) if (spec.b_mode == "dense" or spec.b_major == "k") else f32(bm).T
+    cols = spec.N if spec.act == "dsrelu" else 2 * spec.N
+    dbias = np.zeros(cols)
+    amax = None
+    for r0 in range(lo, hi, chunk):
+        r1 = min(hi, r0 + chunk)
+        offs_local = np.zeros(spec.L, dtype=np.int64)
+        offs_local[g:] = r1 - r0
+        a_rows, c_rows, p_rows = f32(x["a"][r0:r1]), f32(x["c"][r0:r1]), f32(x["prob"][r0:r1])
+        if spec.act == "dsrelu":
+            res = oracle.dsrelu_bwd(a_rows, lambda e: b_g, c_rows, offs_local, f32(x["alpha"]), p_rows)
+        else:
+            res = oracle.dglu_bwd(a_rows, lambda e: b_g, c_rows, offs_local, f32(x["alpha"]), f32(x["beta"]), p_rows,
+                                  act=spec.act)
+            dbias += res["dbias"][g]
+        amax = res["amax"][g] if amax is None else np.maximum(amax, res["amax"][g])
+    return dbias, amax
 
 
 def sampled_experts(counts, rng, n):
@@ -109,6 +136,13 @@ def test_dgrad_full_size(dev, name):
     np.testing.assert_array_equal(tiles_from_log(log.cpu()), oracle.dgrad_tiles(np.cumsum(spec.counts), spec.N, tm, tn))
     check_dglu_sampled(spec, x, d_row, dprob, rng, n_experts=8 if spec.L <= 16 else 12)
     if dbias is not None:
+        # dbias of whole experts against the oracle: the smallest, the largest and a random one
+        nz = [g for g in range(spec.L) if spec.counts[g] > 0]
+        pick = {min(nz, key=lambda g: spec.counts[g]), int(np.argmax(spec.counts)), int(rng.choice(nz))}
+        for g in sorted(pick):
+            want, _ = oracle_whole_expert(spec, x, g)
+            err = rel_fro(f32(dbias[g]), want)
+            assert err <= TOL["bf16"], f"dbias of expert {g} ({spec.counts[g]} rows): relative error {err:.3e}"
         # property at any size: dbias = per-expert column sums of the kernel's own D_row
         offs = np.cumsum(spec.counts)
         sums = torch.zeros(spec.L, 2 * spec.N, dtype=torch.float64, device=dev)
@@ -164,6 +198,11 @@ def test_dsrelu_full_size(dev):
         dp_ref.append(res["dprob"])
     assert rel_fro(np.concatenate(got_all), np.concatenate(ref_all)) <= TOL["bf16"]
     assert rel_fro(np.concatenate(dp_got), np.concatenate(dp_ref)) <= TOL_DPROB
+    # amax of whole experts against the oracle (the smallest and the largest expert)
+    nz = [g for g in range(L) if spec.counts[g] > 0]
+    for g in sorted({min(nz, key=lambda e: spec.counts[e]), int(np.argmax(spec.counts))}):
+        _, want_g = oracle_whole_expert(spec, x, g)
+        assert abs(float(amax[g]) - want_g) <= 2e-3 * want_g, (g, float(amax[g]), want_g)
     # amax is taken on the fp32 values before rounding; the bf16 D_row is within 2^-8 of them
     want = torch.stack([d_row[lo:hi].float().abs().max() if hi > lo else torch.zeros((), device=dev)
                         for lo, hi in ranges])

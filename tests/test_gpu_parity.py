@@ -137,6 +137,82 @@ def test_dsituglu_custom_betas(dev, betas):
     check_close("dprob", to_np(gpu["dprob"]), ref["dprob"], TOL_DPROB)
 
 
+# bf16-exact values on and just past the dGeGLU clamp / filter boundaries (one bf16 ulp at 7 is
+# 2^-5), plus 0 (a value-bearing filter of 0) and -1 (clamped_input + 1 = 0)
+TIE_VALUES = (7.0, -7.0, 7.0 + 2 ** -5, -7.0 - 2 ** -5, 0.0, -1.0)
+
+
+def _plant_ties(spec, x, zero_prob_rows, zero_alpha_expert):
+    """beta = 1 (X = C exactly), tie values planted over C, some prob rows 0, one expert's alpha 0."""
+    c = x["c"].float()
+    M, two_n = c.shape
+    r = torch.arange(M)[:, None]
+    col = torch.arange(two_n)[None, :]
+    sel = ((r * 7 + col * 3) % 5) == 0
+    vals = torch.tensor(TIE_VALUES)[((r + col) % len(TIE_VALUES)).expand(M, two_n)]
+    c = torch.where(sel, vals, c)
+    x["c"] = c.to(x["c"].dtype)
+    assert torch.equal(x["c"].float()[sel], vals[sel])  # every planted value is exact in the C dtype
+    x["beta"] = torch.ones_like(x["beta"])
+    x["prob"][torch.as_tensor(zero_prob_rows)] = 0.0
+    x["alpha"][zero_alpha_expert] = 0.0
+    return x
+
+
+@pytest.mark.parametrize("cta", CTAS)
+@pytest.mark.parametrize("act,filt,d_dtype,K,N,counts", [
+    ("dgeglu", "value", "bf16", 320, 160, (256, 0, 512, 256)),
+    ("dgeglu", "indicator", "bf16", 320, 160, (256, 0, 512, 256)),
+    ("dgeglu", "value", "fp32", 320, 160, (256, 0, 512, 256)),
+    ("dgeglu", "indicator", "fp32", 192, 96, (512, 256)),
+    ("dgeglu", "value", "bf16", 4096, 64, (256, 512)),        # register C path (single CTAs)
+    ("dswiglu", "value", "bf16", 320, 160, (256, 0, 512, 256)),
+    ("dsituglu", "value", "bf16", 320, 160, (256, 0, 512, 256)),
+])
+def test_dglu_exact_ties_zero_prob_rows_zero_alpha(dev, cta, act, filt, d_dtype, K, N, counts):
+    """The clamp and filter decisions at X = +-7 and one ulp past them must be the oracle's, element
+    by element (zero vs non-zero, bit-exact); prob = 0 rows give D = 0 but still add to dprob; an
+    expert with alpha = 0 gives D = 0 and adds exactly nothing to dprob."""
+    # C ~ N(0, 4) makes the dGeGLU clamps fire; the tanh-based sigmoid of dSwiGLU / dSiTU-GLU rounds to
+    # exactly 0 or 1 in fp32 past |x| ~ 17, where float64 does not, so those keep |X| small
+    spec = synth.small_dglu_spec("ties", L=len(counts), counts=counts, K=K, N=N, act=act,
+                                 c_std=4.0 if act == "dgeglu" else 2.0, d_dtype=d_dtype, dbias=d_dtype == "fp32")
+    x = synth.make_dglu_inputs(spec)
+    ranges = _ranges(spec)
+    zero_alpha = len(counts) - 1
+    lo_first = ranges[0][0]
+    zero_rows = [lo_first + 3, lo_first + 100, ranges[-2][1] - 1]
+    x = _plant_ties(spec, x, zero_rows, zero_alpha)
+    gpu = run_dglu_gpu(spec, x, dev, geglu_filter=filt, cta=cta)
+    assert gpu["status"] == 0
+    ref = run_dglu_oracle(spec, x, geglu_filter=filt)
+    got = to_np(gpu["d_row"])
+    check_close("d_row", got, ref["d_row"], TOL[d_dtype], [rg for rg in ranges if rg[1] > rg[0]][:-1])
+    nz_dprob = [rg for g, rg in enumerate(ranges) if g != zero_alpha]
+    check_close("dprob", to_np(gpu["dprob"])[:ranges[zero_alpha][0]], ref["dprob"][:ranges[zero_alpha][0]],
+                TOL_DPROB, nz_dprob)
+    np.testing.assert_array_equal(got == 0, ref["d_row"] == 0)  # every zero / non-zero decision
+    lo, hi = ranges[zero_alpha]
+    assert (gpu["d_row"][lo:hi] == 0).all() and (gpu["dprob"][lo:hi] == 0).all()
+    for m in zero_rows:
+        assert (gpu["d_row"][m] == 0).all() and gpu["dprob"][m] != 0
+    if act == "dgeglu":  # the oracle itself took the tie decisions as the page prints them
+        gcol, icol = oracle.glu_columns(N)
+        c = x["c"].float().numpy()
+        live = np.ones(spec.M, bool)
+        live[zero_rows] = False
+        live[lo:hi] = False
+        gate_past = (c[:, gcol] == 7.0 + 2 ** -5) & live[:, None]
+        inp_past = (np.abs(c[:, icol]) == 7.0 + 2 ** -5) & live[:, None]
+        gate_on = (c[:, gcol] == 7.0) & live[:, None]
+        inp_on = (np.abs(c[:, icol]) == 7.0) & live[:, None] & (c[:, gcol] != 0)  # gate 0 zeroes dinput
+        assert gate_past.any() and inp_past.any() and gate_on.any() and inp_on.any()
+        assert (ref["d_row"][:, gcol][gate_past] == 0).all() and (ref["d_row"][:, icol][inp_past] == 0).all()
+        assert (ref["d_row"][:, icol][inp_on] != 0).all()
+    if spec.dbias:
+        check_close("dbias", to_np(gpu["dbias"]), ref["dbias"], TOL["bf16"])
+
+
 def test_dglu_accumulates_into_dprob_and_dbias(dev):
     spec = synth.small_dglu_spec("acc", dbias=True)
     x = synth.make_dglu_inputs(spec)

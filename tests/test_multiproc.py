@@ -61,3 +61,26 @@ def test_reference_arm_under_torchrun_world2():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+@pytest.mark.timeout(600)
+def test_gpus_flag_starts_local_ranks_itself():
+    """`bench.py --gpus 2` outside torchrun starts two local ranks (rank 0 prints the one line)."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--workload", "tiny", "--steps", "1",
+           "--warmup", "3"]
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=580, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_world_size():
+    cmd = [sys.executable, "bench.py", "--gpus", "2", "--workload", "tiny", "--steps", "1"]
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=120, env=env)
+    assert r.returncode == 2
+    assert "WORLD_SIZE=1" in r.stderr

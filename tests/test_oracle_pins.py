@@ -476,6 +476,42 @@ def test_dgrad_tiles_bruteforce():
     assert 1 not in tiles[:, 0]
 
 
+def _tiles_by_element_cover(offsets, hidden, inter, tm, tn, accumulate):
+    """Tile origins derived from the output elements instead of from a tile loop: every element
+    (e, h, i) an expert must write (all of them in overwrite mode, only non-empty experts under
+    accumulate_on_output) belongs to the tile whose origin is (floor(h / tm) tm, floor(i / tn) tn)."""
+    origins = set()
+    prev = 0
+    for e, end in enumerate(offsets):
+        empty = int(end) == prev
+        prev = int(end)
+        if empty and accumulate:
+            continue
+        for h in range(hidden):
+            for i in range(inter):
+                origins.add((e, (h // tm) * tm, (i // tn) * tn))
+    return sorted(origins)
+
+
+@pytest.mark.parametrize("hidden,inter,tm,tn,accumulate", [
+    (300, 200, 128, 128, False),   # tm == tn: a swapped (h0, i0) or i0 stepped by tm would pass a count check
+    (200, 300, 128, 128, True),
+    (384, 520, 128, 256, False),   # ragged inter tail
+    (512, 136, 256, 128, True),    # pair-sized hidden tiles, inter just past one tile
+    (130, 260, 128, 256, False),
+])
+def test_wgrad_tiles_bruteforce(hidden, inter, tm, tn, accumulate):
+    offsets = [256, 256, 768, 768, 1024]  # experts 1 and 3 empty
+    tiles = O.wgrad_tiles(offsets, hidden, inter, tm, tn, accumulate)
+    assert sorted(map(tuple, tiles.tolist())) == _tiles_by_element_cover(offsets, hidden, inter, tm, tn, accumulate)
+    # the tiles partition each written expert's output: every element lies in exactly one tile
+    for e in sorted(set(tiles[:, 0].tolist())):
+        cover = np.zeros((hidden, inter), dtype=np.int64)
+        for _, h0, i0 in tiles[tiles[:, 0] == e]:
+            cover[h0:h0 + tm, i0:i0 + tn] += 1
+        assert (cover == 1).all()
+
+
 def test_wgrad_tiles_overwrite_includes_empty_accumulate_skips():
     offsets = [512, 512, 768]
     t_ow = O.wgrad_tiles(offsets, 256, 384, 128, 256, accumulate=False)
@@ -525,6 +561,19 @@ def test_planted_mistakes_are_caught(monkeypatch):
     ref = brute_wgrad(A, B, offs)
     bad = O.wgrad(A.reshape(-1), B.reshape(-1), offs, 3, 4, b_major="k")
     assert not all(np.allclose(bad[e], ref[e]) for e in (0, 2, 3))
+
+
+def test_planted_tile_schedule_mistakes_are_caught():
+    """Wrong wgrad schedules that a tile count (or expert membership) alone would accept."""
+    offsets, hidden, inter, tm, tn = [256, 256, 768], 300, 200, 128, 128
+    want = _tiles_by_element_cover(offsets, hidden, inter, tm, tn, False)
+    good = sorted(map(tuple, O.wgrad_tiles(offsets, hidden, inter, tm, tn, False).tolist()))
+    assert good == want
+    swapped = sorted((e, i0, h0) for e, h0, i0 in good)                        # (h0, i0) swapped
+    extents = sorted((e, h0, i0) for e in range(3) for h0 in range(0, inter, tm)  # hidden and inter swapped
+                     for i0 in range(0, hidden, tn))
+    assert len(swapped) == len(good) and swapped != want
+    assert len(extents) == len(good) and extents != want
 
 
 # --------------------------------------------------------------------------------------
