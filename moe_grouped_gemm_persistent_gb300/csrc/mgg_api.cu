@@ -252,13 +252,14 @@ mgg_status validate_wgrad(const mgg_wgrad_args& a) {
 // K = 7168: 1486 vs 1300; dGeGLU with fp32 D: 975 vs 845).
 bool dglu_pair(const mgg_dglu_bwd_args& a) { return a.cta_mode != MGG_CTA_SINGLE; }
 
-// For the wgrad AUTO takes pairs when the experts average at least 1024 tokens (dense accumulate
-// Zipf-shaped layer, ~1000 tokens per expert: +6%); with short reductions (~512 tokens per
-// expert) the pair's coupled epilogues cost more than the halved B traffic saves (-9%).
+// For the wgrad AUTO takes pairs whenever hidden allows them (a multiple of 256): a pair loads
+// 32 KB of operands per SM and k-slice instead of 48 KB, and the SM's operand loads, not the tensor
+// pipe, bound these layers (DeepSeek-shaped, ~630 tokens per expert: 3.79 vs 4.17 ms on one box;
+// Zipf-shaped dense accumulate, ~1000 tokens per expert: 0.312 vs 0.343 ms).
 bool wgrad_pair(const mgg_wgrad_args& a) {
   if (a.hidden % 256 != 0) return false;
   if (a.cta_mode != MGG_CTA_AUTO) return a.cta_mode == MGG_CTA_PAIR;
-  return a.tokens_sum >= 1024 * a.L;
+  return true;
 }
 
 mgg_status from_cuda(cudaError_t e, const char* what) {

@@ -137,7 +137,10 @@ struct EpiCtx {
 };
 
 // Frees one TMEM accumulator for the MMA thread (called by every lane of an epilogue warp):
-// arrives on the accumulator's "empty" barrier, which lives in the even CTA of a pair.
+// arrives on the accumulator's "empty" barrier, which lives in the even CTA of a pair.  Every
+// tcgen05.ld of the accumulator has completed (tcgen05.wait::ld) before this is called, so the MMA
+// can no longer change what the warp read: the odd CTA of a pair arrives with a relaxed (fence-free)
+// remote arrive.
 struct AccRelease {
   uint32_t bar;    // shared::cta address (single CTA) or shared::cluster address (pair)
   bool remote;
@@ -145,7 +148,7 @@ struct AccRelease {
     tc_fence_before();
     __syncwarp();
     if (lane == 0) {
-      if (remote) mbar_arrive_remote(bar);
+      if (remote) mbar_arrive_remote_relaxed(bar);
       else asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
     }
   }
@@ -274,14 +277,20 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     const int r = (int)(n % kSchedRing);
     const uint32_t ph = (uint32_t)((n / kSchedRing) & 1);
     bool ok;
-    if (is_warp) ok = warp_wait<PAIR>(&sfull_bar[r], ph, wg, 6);
-    else ok = PAIR ? mbar_wait_cluster(&sfull_bar[r], ph, wg, 6) : mbar_wait(&sfull_bar[r], ph, wg, 6);
+    // the odd CTA's copy of an entry is written by the even CTA's scheduler (remote stores, then a
+    // release at cluster scope): acquire at cluster scope there; the even CTA's own copy is local
+    const bool remote_entry = PAIR && !leader;
+    if (is_warp) ok = remote_entry ? warp_wait<true>(&sfull_bar[r], ph, wg, 6) : warp_wait<false>(&sfull_bar[r], ph, wg, 6);
+    else ok = remote_entry ? mbar_wait_cluster(&sfull_bar[r], ph, wg, 6) : mbar_wait(&sfull_bar[r], ph, wg, 6);
     if (!ok) return kEnd;
     const uint4 e0 = ld_shared_v4(sched_ring + r * kSchedEntry);
     const uint4 e1 = ld_shared_v4(sched_ring + r * kSchedEntry + 16);
     if (is_warp) __syncwarp();
     if (!is_warp || lane == 0) {
-      if (PAIR && !leader) mbar_arrive_remote(mapa_shared(smem_u32(&sempty_bar[r]), 0));
+      // the odd CTA tells the scheduler it may overwrite this slot: a relaxed arrive whose address
+      // depends on both loaded halves of the entry, so it cannot issue before they have returned
+      if (PAIR && !leader)
+        mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&sempty_bar[r]), 0) + zero_after(e0.x ^ e1.x));
       else mbar_arrive(&sempty_bar[r]);
     }
     w.active = (int)e0.z;

@@ -379,8 +379,28 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t smem_addr, uint32_t ran
   return r;
 }
 
+// Arrive on a barrier of either CTA of the pair with release semantics at cluster scope: this
+// thread's earlier writes (e.g. a published entry written into the peer's shared memory) are
+// visible to whoever acquires the completed phase.  The release costs a memory fence.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Relaxed arrive on a barrier of either CTA of the pair: no fence, so it orders nothing by itself.
+// Used only where the arrive says "I have finished READING" something (a published entry, a TMEM
+// accumulator) and the reads have already returned their values when it issues: a later write by
+// the barrier's waiter can then no longer affect them.  The release form measured ~20% slower on
+// the DeepSeek-shaped wgrad in CTA pairs, whose odd CTA issues nine such arrives per tile.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// 0, computed from `v` by an instruction the compiler cannot fold: adding it to an address makes a
+// later instruction wait until `v` (e.g. a loaded value) is available.
+__device__ __forceinline__ uint32_t zero_after(uint32_t v) {
+  uint32_t z;
+  asm volatile("and.b32 %0, %1, 0;" : "=r"(z) : "r"(v));
+  return z;
 }
 
 __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr) {
