@@ -51,13 +51,16 @@ __device__ __forceinline__ uint32_t swz128w(int r, int c16) { return (uint32_t)(
 
 // OS: output element size in bytes (2 = bf16/fp16, 4 = fp32).  PAIR: 256-row tiles computed by a
 // CTA pair (hidden is then a multiple of 256), each CTA loading half of the tile's B columns.
+// Four epilogue warps, one per TMEM sub-partition, each draining every column of its 32 rows.
+// (Eight warps, two per sub-partition, each reading half of the columns into registers and freeing
+// the accumulator before its stores, measured 5% slower on the DeepSeek-shaped layer: the larger
+// staging costs a pair one of its six operand stages.)
 template <int BN, int OS, bool PAIR>
 struct WgradPolicy {
   static constexpr int kTileM = PAIR ? 2 * BM : BM;
   static constexpr int kBLoad = PAIR ? BN / 2 : BN;
   static constexpr int EPI_WARPS = kWgradEpiWarps;
   static constexpr int STG_BYTES = kWgradStgBytes;
-  static_assert(EPI_WARPS == 4, "one epilogue warp per TMEM sub-partition: it drains every column");
   static constexpr int CW = 128 / OS;  // output columns per staged chunk (one 128-byte row)
   const WgradParams& p;
   static constexpr int kBoxes = STG_BYTES / 4096;
@@ -147,129 +150,134 @@ struct WgradPolicy {
 
   __device__ void prologue(const TileWork&, long long, const EpiCtx&) const {}
 
-  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, bool have_acc, const EpiCtx& ctx,
-                           AccRelease rel) const {
-    const int q = ctx.q, lane = ctx.lane;
-    uint8_t* stg_ptr = ctx.stg;
-    const int e = w.expert;
-    const int row0 = w.m0 + ctx.rank * BM + q * 32;
+  // Writes 64 accumulator columns of this lane's row, starting at tile column `tc` (a multiple of
+  // 64; `n` of them lie inside the output), held in v: added to the old values for 16-bit
+  // accumulation, staged through the warp's shared-memory boxes and sent out by TMA (a bulk
+  // reduce-add for fp32 accumulation).  Lane 0 issues the copies.
+  __device__ __forceinline__ void drain64(const TileWork& w, const EpiCtx& ctx, float (&v)[64], int tc, int n,
+                                          const CUtensorMap* map) const {
+    const int lane = ctx.lane, e = w.expert;
+    const int row0 = w.m0 + ctx.rank * BM + ctx.q * 32;
     const int row = row0 + lane;
-    const bool rows_in = row0 < p.hidden;
-    const uint32_t stg = smem_u32(stg_ptr);
-    const int ncols = p.inter - w.n0 < BN ? p.inter - w.n0 : BN;
-    const int nchunks = (ncols + CW - 1) / CW;
+    const uint32_t stg = smem_u32(ctx.stg);
     const bool discrete = p.out_maps != nullptr;
-    const CUtensorMap* map = discrete ? p.out_maps + e : &p.tmap_out;
-    if (discrete && lane == 0 && ctx.acq.first_use(e)) tmap_acquire(map);
     // fp32 accumulation is a bulk reduce-add at the memory side; 16-bit accumulation reads the old values
     const bool reduce = p.accumulate && OS == 4;
     const bool add_old = p.accumulate && OS == 2;
-    bool released = false;
-    // One TMEM load per 64 accumulator columns (tcgen05.ld 32x32b.x64): two 32-column chunks of
-    // fp32 output or one 64-column chunk of 16-bit output (half the load-and-wait round trips of
-    // one load per 32 columns).
-    constexpr int kPerLoad = 64 / CW;
-#pragma unroll 1
-    for (int c0 = 0; c0 < nchunks; c0 += kPerLoad) {
-      float v[64];
-      if (have_acc) {
-        uint32_t r[64];
-        // BN is a multiple of 64: never past this accumulator
-        tmem_load_64cols(taddr + (MGG_IN_BOUNDS(p.status, c0 * CW + 64 <= BN, 204, c0) ? c0 * CW : 0), r);
-#pragma unroll
-        for (int k = 0; k < 64; ++k) v[k] = __uint_as_float(r[k]);
-        if (c0 + kPerLoad >= nchunks) {
-          rel(lane);
-          released = true;
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 64; ++k) v[k] = 0.f;
-      }
-      if constexpr (OS == 4) {
-        if (p.out_blocked) {  // inter % 64 == 0: both 32-column chunks exist; one 8 KB store for the pair
-          if (!rows_in) continue;
-          if (lane == 0) bulk_wait_read<0>();  // both boxes of the ring have been read
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              st_shared_v4(stg + j * 4096u + swz128w(lane, i), __float_as_uint(v[32 * j + 4 * i]),
-                           __float_as_uint(v[32 * j + 4 * i + 1]), __float_as_uint(v[32 * j + 4 * i + 2]),
-                           __float_as_uint(v[32 * j + 4 * i + 3]));
-          fence_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            const int blk = (w.n0 >> 5) + c0;  // first 32-column block of the pair
-            if (discrete) {
-              if (reduce) tma_reduce_add_3d(map, stg, 0, row0, blk);
-              else tma_store_3d(map, stg, 0, row0, blk);
-            } else {
-              if (reduce) tma_reduce_add_4d(map, stg, 0, row0, blk, e);
-              else tma_store_4d(map, stg, 0, row0, blk, e);
-            }
-            bulk_commit_group();
-          }
-          continue;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kPerLoad; ++j) {
-        const int c = c0 + j;
-        if (c >= nchunks) break;
-        const int col0 = w.n0 + c * CW;
-        if (add_old && row < p.hidden && MGG_IN_BOUNDS(p.status, e < p.L && col0 < p.inter, 202, col0)) {
-          const char* base = discrete ? reinterpret_cast<const char*>(__ldg(p.out_ptrs + e))
-                                      : static_cast<const char*>(p.out) + (size_t)e * p.hidden * (size_t)p.inter * OS;
-          const int n = p.inter - col0 < CW ? p.inter - col0 : CW;
-          const size_t idx = (size_t)row * p.inter + col0;
-#pragma unroll
-          for (int h = 0; h < CW / 32; ++h) {
-            float old[32];
-            load32_n(base, p.out_dtype, idx + 32 * h, old, n - 32 * h);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[CW * j + 32 * h + k] += old[k];
-          }
-        }
-        if (!rows_in) continue;  // rows past hidden (single-CTA tiles only): nothing to write
-        // the box was last filled kBoxes stores ago: wait until at most kBoxes - 1 stores still read
-        const uint32_t box = stg + (stg_uses % kBoxes) * 4096u;
-        ++stg_uses;
-        if (lane == 0) bulk_wait_read<kBoxes - 1>();
+    if (row0 >= p.hidden || n <= 0) return;  // rows past hidden (single-CTA tiles only): nothing to write
+    if constexpr (OS == 4) {
+      if (p.out_blocked) {  // inter % 64 == 0: both 32-column chunks exist; one 8 KB store for the pair
+        if (lane == 0) bulk_wait_read<0>();  // both boxes of the ring have been read
         __syncwarp();
-        const float* vc = v + CW * j;
-        if constexpr (OS == 4) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            st_shared_v4(box + swz128w(lane, i), __float_as_uint(vc[4 * i]), __float_as_uint(vc[4 * i + 1]),
-                         __float_as_uint(vc[4 * i + 2]), __float_as_uint(vc[4 * i + 3]));
-        } else {
-          const int dt = p.out_dtype;
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            st_shared_v4(box + swz128w(lane, i), pack2(vc[8 * i], vc[8 * i + 1], dt),
-                         pack2(vc[8 * i + 2], vc[8 * i + 3], dt), pack2(vc[8 * i + 4], vc[8 * i + 5], dt),
-                         pack2(vc[8 * i + 6], vc[8 * i + 7], dt));
-        }
+            st_shared_v4(stg + j * 4096u + swz128w(lane, i), __float_as_uint(v[32 * j + 4 * i]),
+                         __float_as_uint(v[32 * j + 4 * i + 1]), __float_as_uint(v[32 * j + 4 * i + 2]),
+                         __float_as_uint(v[32 * j + 4 * i + 3]));
         fence_async_shared();
         __syncwarp();
         if (lane == 0) {
+          const int blk = (w.n0 + tc) >> 5;  // first 32-column block of the pair
           if (discrete) {
-            if (reduce) tma_reduce_add_2d(map, box, col0, row0);
-            else tma_store_2d(map, box, col0, row0);
+            if (reduce) tma_reduce_add_3d(map, stg, 0, row0, blk);
+            else tma_store_3d(map, stg, 0, row0, blk);
           } else {
-            if (reduce) tma_reduce_add_3d(map, box, col0, row0, e);
-            else tma_store_3d(map, box, col0, row0, e);
+            if (reduce) tma_reduce_add_4d(map, stg, 0, row0, blk, e);
+            else tma_store_4d(map, stg, 0, row0, blk, e);
           }
           bulk_commit_group();
         }
+        return;
       }
     }
-    if (have_acc && !released) rel(lane);
+#pragma unroll
+    for (int j = 0; j < 64 / CW; ++j) {
+      if (j * CW >= n) break;
+      const int col0 = w.n0 + tc + j * CW;
+      if (add_old && row < p.hidden && MGG_IN_BOUNDS(p.status, e < p.L && col0 < p.inter, 202, col0)) {
+        const char* base = discrete ? reinterpret_cast<const char*>(__ldg(p.out_ptrs + e))
+                                    : static_cast<const char*>(p.out) + (size_t)e * p.hidden * (size_t)p.inter * OS;
+        const int nc = p.inter - col0 < CW ? p.inter - col0 : CW;
+        const size_t idx = (size_t)row * p.inter + col0;
+#pragma unroll
+        for (int h = 0; h < CW / 32; ++h) {
+          float old[32];
+          load32_n(base, p.out_dtype, idx + 32 * h, old, nc - 32 * h);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[CW * j + 32 * h + k] += old[k];
+        }
+      }
+      // the box was last filled kBoxes stores ago: wait until at most kBoxes - 1 stores still read
+      const uint32_t box = stg + (stg_uses % kBoxes) * 4096u;
+      ++stg_uses;
+      if (lane == 0) bulk_wait_read<kBoxes - 1>();
+      __syncwarp();
+      const float* vc = v + CW * j;
+      if constexpr (OS == 4) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          st_shared_v4(box + swz128w(lane, i), __float_as_uint(vc[4 * i]), __float_as_uint(vc[4 * i + 1]),
+                       __float_as_uint(vc[4 * i + 2]), __float_as_uint(vc[4 * i + 3]));
+      } else {
+        const int dt = p.out_dtype;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          st_shared_v4(box + swz128w(lane, i), pack2(vc[8 * i], vc[8 * i + 1], dt),
+                       pack2(vc[8 * i + 2], vc[8 * i + 3], dt), pack2(vc[8 * i + 4], vc[8 * i + 5], dt),
+                       pack2(vc[8 * i + 6], vc[8 * i + 7], dt));
+      }
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        if (discrete) {
+          if (reduce) tma_reduce_add_2d(map, box, col0, row0);
+          else tma_store_2d(map, box, col0, row0);
+        } else {
+          if (reduce) tma_reduce_add_3d(map, box, col0, row0, e);
+          else tma_store_3d(map, box, col0, row0, e);
+        }
+        bulk_commit_group();
+      }
+    }
+  }
+
+  // 64 accumulator columns starting at column tc of this warp's TMEM lanes, as fp32 (zeros when
+  // the tile has no accumulator: an empty expert written in overwrite mode).
+  __device__ __forceinline__ void load64(uint32_t taddr, bool have_acc, int tc, float (&v)[64]) const {
+    if (have_acc) {
+      uint32_t r[64];
+      // BN is a multiple of 64: never past this accumulator
+      tmem_load_64cols(taddr + (MGG_IN_BOUNDS(p.status, tc + 64 <= BN, 204, tc) ? tc : 0), r);
+#pragma unroll
+      for (int k = 0; k < 64; ++k) v[k] = __uint_as_float(r[k]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 64; ++k) v[k] = 0.f;
+    }
+  }
+
+  __device__ void epilogue(const TileWork& w, long long t, uint32_t taddr, bool have_acc, const EpiCtx& ctx,
+                           AccRelease rel) const {
+    const int lane = ctx.lane;
+    const int e = w.expert;
+    const int ncols = p.inter - w.n0 < BN ? p.inter - w.n0 : BN;
+    const bool discrete = p.out_maps != nullptr;
+    const CUtensorMap* map = discrete ? p.out_maps + e : &p.tmap_out;
+    if (discrete && lane == 0 && ctx.acq.first_use(e)) tmap_acquire(map);
+    // one TMEM load per 64 accumulator columns (tcgen05.ld 32x32b.x64), the accumulator freed
+    // after the last load
+#pragma unroll 1
+    for (int tc = 0; tc < ncols; tc += 64) {
+      float v[64];
+      load64(taddr, have_acc, tc, v);
+      if (have_acc && tc + 64 >= ncols) rel(lane);
+      drain64(w, ctx, v, tc, ncols - tc, map);
+    }
     // one entry per CTA tile of 128 rows (a pair's tile logs two)
     const long long idx = PAIR ? 2 * t + ctx.rank : t;
-    if (p.tile_log != nullptr && q == 0 && lane == 0 && idx < p.tile_log_cap) {
+    if (p.tile_log != nullptr && ctx.q == 0 && lane == 0 && idx < p.tile_log_cap) {
       int32_t* l = p.tile_log + 4 * idx;
       l[0] = e;
       l[1] = w.m0 + ctx.rank * BM;
