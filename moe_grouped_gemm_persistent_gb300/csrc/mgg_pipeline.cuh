@@ -46,10 +46,12 @@ constexpr int BM = 128;        // accumulator rows per CTA (UMMA M per CTA)
 constexpr int BK = 64;         // K elements per ring slot: one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;     // K of one kind::f16 MMA
 constexpr int kSchedRing = 8;  // published tiles in flight from the scheduler to the other roles
-// The scheduler claims tile n + 1 once the producer has kClaimLeadKb (or fewer) k-slices of tile n
-// left to issue: early enough to hide the claim's atomic and decode, late enough to keep the
-// dynamic schedule's load balance (a tile claimed long before it starts cannot move).
-constexpr int kClaimLeadKb = 6;
+// The scheduler claims the next tile once the producer has kClaimLeadKb (or fewer) k-slices of the
+// tiles already published left to issue: early enough to hide the claim's atomic and decode (about
+// 1.5 us), so that a run of short tiles does not stall the producer at every tile boundary, and
+// late enough to keep the dynamic schedule's load balance (a tile claimed long before it starts
+// cannot move).
+constexpr int kClaimLeadKb = 10;
 constexpr int kSchedEntry = 32; // bytes of one published tile: index + TileWork
 constexpr int kMaxExperts = 1024;
 constexpr int kAcqWords = kMaxExperts / 32;  // one bit per expert
@@ -94,7 +96,7 @@ constexpr int kMaxSmemBytes = 232448;  // dynamic shared memory per block (227 K
 // Dynamic shared memory of one CTA (the same arithmetic as SmemLayout below).
 __host__ __device__ constexpr int smem_bytes(int bn_load, int stages, int epi_warps, int stg, int nacc) {
   return ((stages * (BM + bn_load) * BK * 2 + epi_warps * stg +
-           (2 * stages + 2 * nacc + 1 + 3 * kSchedRing + 4 * epi_warps) * 8 + 15) / 16 * 16) +
+           (2 * stages + 2 * nacc + 1 + 2 * kSchedRing + 4 * epi_warps) * 8 + 15) / 16 * 16) +
          kSchedRing * kSchedEntry + (1 + epi_warps) * kAcqWords * 4 + 16 + 1024;
 }
 
@@ -112,11 +114,11 @@ struct SmemLayout {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * STG;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1 + 3 * kSchedRing + 4 * EPI_WARPS;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1 + 2 * kSchedRing + 4 * EPI_WARPS;
   static constexpr int SCHED_OFF = (BAR_OFF + NUM_BARS * 8 + 15) / 16 * 16;
   static constexpr int ACQ_OFF = SCHED_OFF + kSchedRing * kSchedEntry;  // producer, then each epilogue warp
   static constexpr int MISC_OFF = ACQ_OFF + (1 + EPI_WARPS) * kAcqWords * 4;
-  static constexpr int BYTES = MISC_OFF + 16;  // TMEM address, abort flag, skip flag
+  static constexpr int BYTES = MISC_OFF + 16;  // TMEM address, abort flag, skip flag, issued k-slices
   static constexpr int DYN_BYTES = BYTES + 1024;  // slack to align the ring to 1024 B
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "ring slots must stay 1024-byte aligned");
   static_assert(SCHED_OFF % 16 == 0, "16-byte aligned published tiles");
@@ -167,6 +169,24 @@ static __device__ __noinline__ void mbar_wait_drain(uint64_t* bar, uint32_t pari
   }
 }
 
+// Spins (sleeping briefly between looks) until the producer has at most kClaimLeadKb of the
+// `published` k-slices left to issue (`issued` is the producer's running count, modulo 2^32).
+// Bounded like the mbarrier waits: an abort of the CTA or the time limit ends it with false.
+static __device__ __noinline__ bool wait_claim_lead(const volatile uint32_t* issued, uint32_t published, WaitGuard g,
+                                                    int where) {
+  if ((int)(published - *issued) <= kClaimLeadKb) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while ((int)(published - *issued) > kClaimLeadKb) {
+    if (*g.abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_timeout(g, where);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
 // Every lane of the warp waits; the warp proceeds only if all lanes saw the phase.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, WaitGuard g, int where) {
@@ -194,11 +214,12 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   uint64_t* done_bar = tempty_bar + NACC;
   uint64_t* sfull_bar = done_bar + 1;             // [kSchedRing] a tile was published
   uint64_t* sempty_bar = sfull_bar + kSchedRing;  // [kSchedRing] every consumer has read it
-  uint64_t* taken_bar = sempty_bar + kSchedRing;  // [kSchedRing] the (even CTA's) producer started it
-  uint64_t* epi_bars = taken_bar + kSchedRing;    // [4 * kEpiWarps] owned by the epilogue warps
+  uint64_t* epi_bars = sempty_bar + kSchedRing;   // [4 * kEpiWarps] owned by the epilogue warps
   const uint32_t sched_ring = smem_u32(smem + S::SCHED_OFF);  // [kSchedRing] x {t, TileWork}
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 4);
+  // k-slices the (even CTA's) producer has issued so far, read by the scheduler thread
+  volatile uint32_t* issued_kb = reinterpret_cast<volatile uint32_t*>(smem + S::MISC_OFF + 12);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -231,12 +252,12 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     for (int r = 0; r < kSchedRing; ++r) {
       mbar_init(&sfull_bar[r], 1);
       mbar_init(&sempty_bar[r], kSchedConsumers);
-      mbar_init(&taken_bar[r], 1);
     }
     for (int b = 0; b < 4 * kEpiWarps; ++b) mbar_init(&epi_bars[b], 1);
     uint32_t* acq = reinterpret_cast<uint32_t*>(smem + S::ACQ_OFF);
     for (int i = 0; i < (1 + kEpiWarps) * kAcqWords; ++i) acq[i] = 0u;
     *abort_flag = 0;
+    *issued_kb = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -306,16 +327,15 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
     // ---------------------------------------------------------------- scheduler (even CTA)
     // Claims tiles (static or from the counter), decodes them and publishes them to every role,
     // so the producer does not wait for a claim's atomic or for the offsets the decode reads.
-    // Tile n is claimed when the producer is about to finish issuing tile n - 1 (kClaimLeadKb).
+    // The next tile is claimed once the producer has at most kClaimLeadKb k-slices of the
+    // published tiles left to issue.
     if (lane == 0 && leader) {
       int* counter = p.status + 3;
+      uint32_t published_kb = 0;  // k-slices of every tile published so far (modulo 2^32)
       for (long long n = 0;; ++n) {
         const int r = (int)(n % kSchedRing);
         const uint32_t eph = (uint32_t)(((n / kSchedRing) & 1) ^ 1);
-        if (n >= 1) {
-          const long long m = n - 1;
-          if (!mbar_wait(&taken_bar[m % kSchedRing], (uint32_t)((m / kSchedRing) & 1), wg, 8)) break;
-        }
+        if (n >= 1 && !wait_claim_lead(issued_kb, published_kb, wg, 8)) break;
         // in a pair the odd CTA's consumers release the slot remotely: acquire at cluster scope
         if (!(PAIR ? mbar_wait_cluster(&sempty_bar[r], eph, wg, 5) : mbar_wait(&sempty_bar[r], eph, wg, 5))) break;
         long long t = dynamic ? (long long)atomicAdd(counter, 1) : unit + n * units;
@@ -338,6 +358,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
           mbar_arrive_remote(mapa_shared(smem_u32(&sfull_bar[r]), 1));
         }
         mbar_arrive(&sfull_bar[r]);
+        if (w.active) published_kb += (uint32_t)w.num_kb;
         if (t >= p.total_tiles) break;
       }
     }
@@ -354,13 +375,8 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       TileWork w;
       for (long long t = consume_tile(n_tile++, false, w); t < p.total_tiles && ok;
            t = consume_tile(n_tile++, false, w)) {
-        // k-slices issued before the scheduler may claim the next tile (the even CTA decides)
-        const int lead = (w.active && w.num_kb > kClaimLeadKb) ? w.num_kb - kClaimLeadKb : 0;
-        uint64_t* const taken = &taken_bar[(n_tile - 1) % kSchedRing];
-        if (leader && lead == 0) mbar_arrive(taken);
         if (!w.active) continue;
         for (int kb = 0; kb < w.num_kb; ++kb) {
-          if (leader && kb == lead && kb > 0) mbar_arrive(taken);
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wg, 1)) {
             ok = false;
             break;
@@ -370,6 +386,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
           const uint32_t bar = PAIR ? mapa_shared(smem_u32(&full_bar[stage]), 0) : smem_u32(&full_bar[stage]);
           p.issue_loads(w, kb, sa, sa + S::A_BYTES, bar, (int)rank, acq_producer);
           ++issued;
+          if (leader) *issued_kb = (uint32_t)issued;  // the scheduler's claim lead
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
