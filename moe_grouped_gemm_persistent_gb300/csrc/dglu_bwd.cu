@@ -102,6 +102,9 @@ struct DgluPolicy {
   int a_mn, b_mn;
   int dynamic;
   mutable uint32_t c_uses = 0;  // TMA path: C boxes this warp has consumed (ring position)
+  // The scheduler thread's decode cache: the expert found last and its row range, so consecutive
+  // tiles of one expert skip the binary search over the offsets (dependent global loads).
+  mutable int c_g = -1, c_begin = 0, c_end = 0;
 
   __device__ DgluPolicy(const DgluParams& prm)
       : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(0), b_mn(prm.b_mn), dynamic(prm.dynamic) {}
@@ -112,15 +115,20 @@ struct DgluPolicy {
   // row floor(t / num_n) * kTileM (its tiles occupy [begin/kTileM * num_n, end/kTileM * num_n)).
   __device__ TileWork tile(long long t) const {
     const int row = (int)(t / p.num_n) * kTileM;
-    int lo = 0, hi = p.L - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(p.offsets + mid) > row) hi = mid;
-      else lo = mid + 1;
+    if (c_g < 0 || row < c_begin || row >= c_end) {
+      int lo = 0, hi = p.L - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(p.offsets + mid) > row) hi = mid;
+        else lo = mid + 1;
+      }
+      c_g = lo;
+      c_begin = lo ? __ldg(p.offsets + lo - 1) : 0;
+      c_end = __ldg(p.offsets + lo);
     }
-    const int g = lo;
-    const int begin = g ? __ldg(p.offsets + g - 1) : 0;
-    const int mblocks = (__ldg(p.offsets + g) - begin) / kTileM;
+    const int g = c_g;
+    const int begin = c_begin;
+    const int mblocks = (c_end - begin) / kTileM;
     const long long u = t - (long long)(begin / kTileM) * p.num_n;
     TileWork w;
     w.active = 1;

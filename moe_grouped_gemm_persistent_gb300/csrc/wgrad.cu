@@ -69,6 +69,23 @@ struct WgradPolicy {
   int* status;
   int a_mn, b_mn;
   int dynamic;
+  // The scheduler thread's decode cache: the expert slot last decoded at each end of the LPT order
+  // (the dynamic schedule alternates between the two ends, the static one uses end 0) with its
+  // expert and token range, so consecutive tiles of one expert read no global memory.
+  struct ExpertRange {
+    int slot = -1, e = 0, begin = 0, end = 0;
+  };
+  mutable ExpertRange c_long, c_short;
+
+  // Expert slot `slot` of the order with its token range, from the cache `c` or global memory.
+  __device__ __forceinline__ void decode(ExpertRange& c, int slot, bool slot_ok) const {
+    if (slot == c.slot) return;
+    const int e = slot_ok ? __ldg(p.order + slot) : 0;
+    c.slot = slot;
+    c.e = e;
+    c.begin = (e > 0 && e < p.L) ? __ldg(p.offsets + e - 1) : 0;
+    c.end = (e >= 0 && e < p.L) ? __ldg(p.offsets + e) : 0;
+  }
 
   // The tiles of the experts that have work (all of them when overwriting; in accumulate mode the
   // preparation kernel counts the non-empty ones, which the LPT order puts first), so the two ends
@@ -88,13 +105,18 @@ struct WgradPolicy {
     TileWork w;
     // checked build: an expert slot or order entry outside [0, L) makes the tile a skipped one
     const bool slot_ok = MGG_IN_BOUNDS(p.status, slot >= 0 && slot < p.L, 411, slot);
-    const int e = slot_ok ? __ldg(p.order + slot) : 0;
+    int e, begin, end;
+    if (p.dynamic && (t & 1)) {  // the short end of the order
+      decode(c_short, slot, slot_ok);
+      e = c_short.e, begin = c_short.begin, end = c_short.end;
+    } else {
+      decode(c_long, slot, slot_ok);
+      e = c_long.e, begin = c_long.begin, end = c_long.end;
+    }
     if (!MGG_IN_BOUNDS(p.status, e >= 0 && e < p.L, 412, e) || !slot_ok) {
       w = TileWork{0, 0, 0, 0, 0, 0};
       return w;
     }
-    const int begin = e ? __ldg(p.offsets + e - 1) : 0;
-    const int end = __ldg(p.offsets + e);
     w.expert = e;
     w.active = (end > begin) || !p.accumulate;
     w.m0 = (local / p.tiles_n) * kTileM;
