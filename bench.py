@@ -48,6 +48,7 @@ WORKLOAD_TEXT = {
     "mixtral_s": "profiling copy of mixtral with L=2 experts, 8192 tokens",
     "geglu_s": "profiling copy of geglu with 12288 tokens",
     "deepseek_s": "profiling copy of deepseek with L=32 experts, 16384 tokens",
+    "dsrelu_s": "profiling copy of dsrelu with L=2 experts, 8192 tokens",
 }
 
 

@@ -109,10 +109,15 @@ struct DgluPolicy {
   __device__ DgluPolicy(const DgluParams& prm)
       : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(0), b_mn(prm.b_mn), dynamic(prm.dynamic) {}
 
-  // Tile order: expert-major; inside an expert, column panels of BN, and inside a panel
-  // the expert's row blocks (kTileM rows; experts are 256-row aligned), so concurrently running
-  // CTAs share one B panel and the expert's A rows in L2.  Tile t belongs to the expert containing
-  // row floor(t / num_n) * kTileM (its tiles occupy [begin/kTileM * num_n, end/kTileM * num_n)).
+  // Tile order: expert-major (tile t belongs to the expert containing row floor(t / num_n) *
+  // kTileM; its tiles occupy [begin/kTileM * num_n, end/kTileM * num_n)).  Inside an expert the
+  // operand that is re-read across the expert's tiles stays in L2 while the other one streams
+  // through once: an expert with at most N rows (A_g no larger than B_g) runs column panel by
+  // column panel, each panel over all of the expert's row blocks (A_g re-read per panel from L2,
+  // each B panel read once); an expert with more rows runs row block by row block, each over all
+  // column panels (B_g re-read per row block from L2, each block of A rows read once).  (Panel
+  // order for a DeepSeek-shaped expert of 21248 rows re-read its 304 MB of A rows from DRAM for
+  // every one of its 8 panels.)
   __device__ TileWork tile(long long t) const {
     const int row = (int)(t / p.num_n) * kTileM;
     if (c_g < 0 || row < c_begin || row >= c_end) {
@@ -133,8 +138,13 @@ struct DgluPolicy {
     TileWork w;
     w.active = 1;
     w.expert = g;
-    w.n0 = (int)(u / mblocks) * BN;
-    w.m0 = begin + (int)(u % mblocks) * kTileM;
+    if (c_end - begin <= p.N) {  // panel by panel
+      w.n0 = (int)(u / mblocks) * BN;
+      w.m0 = begin + (int)(u % mblocks) * kTileM;
+    } else {  // row block by row block
+      w.n0 = (int)(u % p.num_n) * BN;
+      w.m0 = begin + (int)(u / p.num_n) * kTileM;
+    }
     w.k0 = 0;
     w.num_kb = p.num_kb;
     // checked build: a tile outside the call's extents is skipped by every role

@@ -175,6 +175,9 @@ def workload_specs(name: str):
         counts = dgrad_counts(0, 16, 12288, 1.1, n_empty=2)
         return DgluSpec("geglu_s", L=16, K=2048, N=5632, counts=counts, act="dgeglu", b_mode="discrete",
                         b_major="n", c_std=4.0, d_dtype="fp32", dbias=True), None
+    if name == "dsrelu_s":
+        counts = dgrad_counts(0, 2, 8192, None)
+        return DgluSpec("dsrelu_s", L=2, K=4096, N=14336, counts=counts, b_std=0.02, act="dsrelu"), None
     if name == "deepseek_s":
         counts = dgrad_counts(0, 32, 16384, 1.0)
         d = DgluSpec("deepseek_s", L=32, K=7168, N=2048, counts=counts)
@@ -185,7 +188,7 @@ def workload_specs(name: str):
 
 
 WORKLOADS = ("tiny", "mixtral", "geglu", "wgrad64", "deepseek")
-PROFILE_WORKLOADS = ("mixtral_s", "geglu_s", "deepseek_s")
+PROFILE_WORKLOADS = ("mixtral_s", "geglu_s", "deepseek_s", "dsrelu_s")
 
 
 # --------------------------------------------------------------------------------------
