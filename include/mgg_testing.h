@@ -41,6 +41,13 @@ mgg_status mgg_test_tmap_replace(const void* tmpl128, void* out_dev128, const vo
  * issues no TMA copy and no MMA.  Queued on `stream`; read the word with mgg_read_device_status. */
 mgg_status mgg_test_wait_timeout(void* status_dev, int64_t limit_ns, int32_t where, int32_t cluster, void* stream);
 
+/* Runs, in one thread, the index check the kernels make on a computed index: `value` against
+ * [0, limit).  In the bounds-checked build a value outside records MGG_ERR_DEVICE_BOUNDS in
+ * status_dev (device int32[4], 16-byte aligned, zeroed by the caller): [0] = 8, [1] = 501,
+ * [2] = the value; and the guarded write of [3] = 1 is skipped.  In the normal build the check
+ * compiles away and [3] = 1 is always written.  Queued on `stream`. */
+mgg_status mgg_test_bounds_check(void* status_dev, int64_t value, int64_t limit, void* stream);
+
 /* Build flags of the loaded library: bit 0 set for the bounds-checked build (-DMGG_CHECKED), whose
  * kernels test every computed global index, tensor-map slot and TMEM column against the call's
  * extents and record MGG_ERR_DEVICE_BOUNDS (where, value) instead of making the access. */

@@ -92,6 +92,7 @@ SIGNATURES = [
     ("mgg_test_tmap_replace", c_int, [c_void_p, c_void_p, c_void_p, c_uint32, c_uint64, c_int, c_void_p]),
     ("mgg_test_wait_timeout", c_int, [c_void_p, c_int64, c_int32, c_int32, c_void_p]),
     ("mgg_test_build_flags", c_int, []),
+    ("mgg_test_bounds_check", c_int, [c_void_p, c_int64, c_int64, c_void_p]),
 ]
 
 _lib = None

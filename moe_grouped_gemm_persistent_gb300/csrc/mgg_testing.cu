@@ -47,10 +47,33 @@ __global__ void wait_timeout_probe_kernel(int* status, unsigned long long limit_
   status[3] = (ok1 ? 0 : 1) | ((!ok2 && quick) ? 2 : 0) | (status[1] == where_after_first ? 4 : 0);
 }
 
+// One thread checks `value` against [0, limit) exactly as the kernels check their indices: in the
+// bounds-checked build a value outside records MGG_ERR_DEVICE_BOUNDS (where 501, the value) and the
+// guarded "access" (status[3] = 1) is skipped; in the normal build the check compiles away.
+__global__ void bounds_probe_kernel(int* status, long long value, long long limit) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  if (MGG_IN_BOUNDS(status, value >= 0 && value < limit, 501, value)) status[3] = 1;
+}
+
 }  // namespace
 }  // namespace mgg
 
 using namespace mgg;
+
+extern "C" mgg_status mgg_test_bounds_check(void* status_dev, int64_t value, int64_t limit, void* stream) {
+  if (status_dev == nullptr || (reinterpret_cast<uintptr_t>(status_dev) & 15u) != 0) {
+    set_last_error("status_dev must be a 16-byte aligned device buffer of 4 int32");
+    return MGG_ERR_VALUE;
+  }
+  bounds_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<int*>(status_dev),
+                                                                       (long long)value, (long long)limit);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_last_error(std::string("bounds probe launch: ") + cudaGetErrorString(e));
+    return MGG_ERR_RUNTIME;
+  }
+  return MGG_OK;
+}
 
 extern "C" mgg_status mgg_test_wait_timeout(void* status_dev, int64_t limit_ns, int32_t where, int32_t cluster,
                                             void* stream) {

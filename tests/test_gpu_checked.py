@@ -25,6 +25,20 @@ SUBSET = " or ".join([
 ])
 
 
+# in range (value 5 < 10): status stays 0 and the guarded write happens; out of range (77 >= 10):
+# MGG_ERR_DEVICE_BOUNDS, where 501, value 77, and the guarded write is skipped
+BOUNDS_SNIPPET = """
+import torch
+from moe_grouped_gemm_persistent_gb300 import _lib
+lib = _lib.load()
+for v in (5, 77):
+    st = torch.zeros(4, dtype=torch.int32, device="cuda")
+    _lib.check(lib.mgg_test_bounds_check(st.data_ptr(), v, 10, None))
+    torch.cuda.synchronize()
+    print(*st.cpu().tolist())
+"""
+
+
 @pytest.mark.timeout(1800)
 def test_parity_subset_under_the_bounds_checked_build():
     build(checked=True)
@@ -33,6 +47,11 @@ def test_parity_subset_under_the_bounds_checked_build():
                             "print(_lib.load().mgg_test_build_flags())"], cwd=ROOT, env=env, capture_output=True,
                            text=True, timeout=300)
     assert probe.returncode == 0 and probe.stdout.strip() == "1", probe.stderr[-2000:]
+    # the check itself: an index outside its range is recorded (where 501, the value) and not used
+    check = subprocess.run([sys.executable, "-c", BOUNDS_SNIPPET], cwd=ROOT, env=env, capture_output=True, text=True,
+                           timeout=300)
+    assert check.returncode == 0 and check.stdout.split() == ["0", "0", "0", "1", "8", "501", "77", "0"], \
+        (check.stdout, check.stderr[-2000:])
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-k", SUBSET,
                         "tests/test_gpu_parity.py", "tests/test_gpu_dsrelu.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=1700)
