@@ -546,6 +546,9 @@ struct DgluPolicy {
     }
   }
 
+  // Every dgrad tile runs full-width MMAs.
+  __device__ __forceinline__ bool narrow(const TileWork&) const { return false; }
+
   __device__ void prologue(const TileWork& w, long long, const EpiCtx& ctx) const {
     if constexpr (Cfg::kTmaC) {
       if (*ctx.wg.abort_flag) return;  // the CTA is stopping: start no copies that nobody would wait for

@@ -25,6 +25,9 @@
 //   issue_loads(w, kb, sa, sb, bar, rank, acq)      producer thread; `bar` is the address the
 //                                                   loads complete on (the even CTA's in a pair);
 //                                                   `acq` records the maps it has acquired
+//   bool narrow(w)                                  the tile's valid columns fit in BN/2: its MMAs
+//                                                   have N = BN/2 (accumulator columns [0, BN/2);
+//                                                   in a pair each CTA then supplies BN/4 of them)
 //   EPI_WARPS, STG_BYTES                            epilogue warps (multiple of 4), bytes per warp
 //   prologue(w, t, ctx)                             one epilogue warp, before it waits for the
 //                                                   tile's accumulator (e.g. to start input loads)
@@ -404,7 +407,8 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (even CTA)
     if (lane == 0 && leader) {
-      const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, p.a_mn, p.b_mn);
+      const uint32_t idesc_full = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, p.a_mn, p.b_mn);
+      const uint32_t idesc_half = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN / 2, p.a_mn, p.b_mn);
       const uint32_t a_lbo = p.a_mn ? 8192u : 16u, a_kstep = p.a_mn ? 2048u : 32u;
       const uint32_t b_lbo = p.b_mn ? 8192u : 16u, b_kstep = p.b_mn ? 2048u : 32u;
       int stage = 0;
@@ -419,6 +423,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
         if (!mbar_wait(&tempty_bar[acc], (use & 1u) ^ 1u, wg, 2)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t idesc = p.narrow(w) ? idesc_half : idesc_full;
         for (int kb = 0; kb < w.num_kb; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, wg, 3)) {
             ok = false;

@@ -137,12 +137,14 @@ struct WgradPolicy {
     else tma_load_3d(dst, map, bar, x, y, z);
   }
 
-  // This CTA's 128 rows of A (m0 + 128 * rank) and its kBLoad columns of B (n0 + kBLoad * rank).
+  // This CTA's 128 rows of A (m0 + 128 * rank) and its kBLoad columns of B (n0 + kBLoad * rank;
+  // a narrow tile's N = BN/2 MMA takes BN/4 columns from each CTA of a pair, so the odd CTA's
+  // start at n0 + BN/4; the loads keep their full box sizes, the columns past those unused).
   __device__ void issue_loads(const TileWork& w, int kb, uint32_t sa, uint32_t sb, uint32_t bar, int rank,
                               const MapAcquired& acq) const {
     const int k = w.k0 + kb * BK;
     const int mrow = w.m0 + rank * BM;
-    const int ncol = w.n0 + rank * kBLoad;
+    const int ncol = w.n0 + rank * (narrow(w) ? kBLoad / 2 : kBLoad);
     if (kb == 0 && (p.a_maps != nullptr || p.b_maps != nullptr) && acq.first_use(w.expert)) {
       if (p.a_maps != nullptr) tmap_acquire(p.a_maps + w.expert);
       if (p.b_maps != nullptr) tmap_acquire(p.b_maps + w.expert);
@@ -169,6 +171,10 @@ struct WgradPolicy {
       load2(sb, &p.tmap_b, bar, k, ncol);
     }
   }
+
+  // The last column tile of an output whose width leaves at most 128 columns there (inter % 256 in
+  // (0, 128]) runs N = 128 MMAs: half the tensor work of a full tile for the same result.
+  __device__ __forceinline__ bool narrow(const TileWork& w) const { return BN == 256 && p.inter - w.n0 <= BN / 2; }
 
   __device__ void prologue(const TileWork&, long long, const EpiCtx&) const {}
 

@@ -265,6 +265,13 @@ WGRAD_CASES = {
     "out_blocked_ragged_discrete": dict(input_order="tensor_ragged", out_mode="discrete", inter=320),
     "out_blocked_acc": dict(accumulate=True, inter=384),
     "out_blocked_discrete_acc": dict(out_mode="discrete", accumulate=True, inter=256),
+    # inter % 256 in (0, 128]: the last column tile runs N = 128 MMAs (in a pair each CTA supplies
+    # 64 of its columns), through every B path: K-major, ragged K-major, N-major in 64-column
+    # boxes and N-major blocked; with 16-bit and FP32 outputs
+    "narrow_k_k": dict(b_major="k", inter=384),
+    "narrow_ragged_k_k_bf16": dict(input_order="tensor_ragged", b_major="k", inter=640, out_dtype="bf16"),
+    "narrow_k_n_352": dict(inter=352),
+    "narrow_m_n_blocked_acc": dict(a_major="m", hidden=256, inter=320, accumulate=True),
 }
 
 
