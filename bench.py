@@ -334,69 +334,76 @@ def time_steps(prob: "Problem", steps: int, warmup: int, world: int):
     return total_ms, per, clocks
 
 
-def _io_tensors(prob: "Problem"):
-    """The device inputs a step reads and the outputs it writes."""
+def _io_parts(prob: "Problem"):
+    """Per part of the step (dgrad, wgrad): the device inputs it reads, the outputs it writes and
+    the call that runs it."""
     import torch
-    ins, outs = [], []
+    parts = []
     if prob.dspec is not None:
         x = prob.d
         bs = [x["b"]] if isinstance(x["b"], torch.Tensor) else list(x["b"])
-        ins += [x["a"], x["c"], x["alpha"], x["beta"], x["prob"], x["padded_offsets"], *bs]
-        outs += [prob.d_row, prob.dprob] + ([prob.dbias] if prob.dbias is not None else [])
+        ins = [x["a"], x["c"], x["alpha"], x["beta"], x["prob"], x["padded_offsets"], *bs]
+        outs = [prob.d_row, prob.dprob] + ([prob.dbias] if prob.dbias is not None else [])
+        parts.append((ins, outs, prob.dgrad))
     if prob.wspec is not None:
         y = prob.w
-        ins += [y["a"], y["b"], y["offsets"]]
-        outs += [prob.w_out]
-    return ins, outs
+        parts.append(([y["a"], y["b"], y["offsets"]], [prob.w_out], prob.wgrad))
+    return parts
 
 
 def time_e2e(prob: "Problem", steps: int, warmup: int):
     """Same step through the public API with pinned host buffers: every step copies all its inputs
     host -> device and all its outputs device -> host inside the timed region.  The copies in and
-    out and the two ABI calls run on three CUDA streams, with two device buffer sets used by
-    alternate steps, so step i's results leave while step i + 1's inputs arrive and compute (the
-    host link carries both directions at once).  The timed region runs from the first input copy
-    to the end of the last output copy."""
+    out and the ABI calls run on three CUDA streams, with two device buffer sets used by alternate
+    steps, so step i's results leave while step i + 1's inputs arrive and compute (the host link
+    carries both directions at once).  Each part waits only for its own inputs, and its outputs
+    leave as soon as it is done.  The timed region runs from the first input copy to the end of
+    the last output copy."""
     import torch
     dev = prob.dev
     sets = [prob, Problem(prob.workload, dev, prob.sched, prob.cta)]
-    io = [_io_tensors(p) for p in sets]
-    host_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in io[0][0]]
-    for h, t in zip(host_in, io[0][0]):
-        h.copy_(t)
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in io[0][1]]
-    bi = sum(t.numel() * t.element_size() for t in io[0][0])
-    bo = sum(t.numel() * t.element_size() for t in io[0][1])
+    io = [_io_parts(p) for p in sets]
+    host_in = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins] for ins, _, _ in io[0]]
+    for hs, (ins, _, _) in zip(host_in, io[0]):
+        for h, t in zip(hs, ins):
+            h.copy_(t)
+    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _, outs, _ in io[0]]
+    bi = sum(t.numel() * t.element_size() for ins, _, _ in io[0] for t in ins)
+    bo = sum(t.numel() * t.element_size() for _, outs, _ in io[0] for t in outs)
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    nparts = len(io[0])
 
     def run(n):
-        cmp_done, out_done = [None, None], [None, None]
+        # per part and buffer set: the last compute and the last output copy issued on it
+        cmp_done = [[None, None] for _ in range(nparts)]
+        out_done = [[None, None] for _ in range(nparts)]
         for i in range(n):
             k = i % 2
-            p, (ins, outs) = sets[k], io[k]
+            in_done = []
             with torch.cuda.stream(s_in):
-                if cmp_done[k] is not None:  # step i - 2 has finished reading this set's inputs
-                    s_in.wait_event(cmp_done[k])
-                for h, t in zip(host_in, ins):
-                    t.copy_(h, non_blocking=True)
-                in_done = torch.cuda.Event()
-                in_done.record(s_in)
+                for j, (ins, _, _) in enumerate(io[k]):
+                    if cmp_done[j][k] is not None:  # step i - 2 has finished reading these inputs
+                        s_in.wait_event(cmp_done[j][k])
+                    for h, t in zip(host_in[j], ins):
+                        t.copy_(h, non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(s_in)
+                    in_done.append(e)
             with torch.cuda.stream(s_cmp):
-                s_cmp.wait_event(in_done)
-                if out_done[k] is not None:  # step i - 2's outputs have left this set
-                    s_cmp.wait_event(out_done[k])
-                if p.dspec is not None:
-                    p.dgrad()
-                if p.wspec is not None:
-                    p.wgrad()
-                cmp_done[k] = torch.cuda.Event()
-                cmp_done[k].record(s_cmp)
+                for j, (_, _, fn) in enumerate(io[k]):
+                    s_cmp.wait_event(in_done[j])
+                    if out_done[j][k] is not None:  # step i - 2's outputs have left this set
+                        s_cmp.wait_event(out_done[j][k])
+                    fn()
+                    cmp_done[j][k] = torch.cuda.Event()
+                    cmp_done[j][k].record(s_cmp)
             with torch.cuda.stream(s_out):
-                s_out.wait_event(cmp_done[k])
-                for h, t in zip(host_out, outs):
-                    h.copy_(t, non_blocking=True)
-                out_done[k] = torch.cuda.Event()
-                out_done[k].record(s_out)
+                for j, (_, outs, _) in enumerate(io[k]):
+                    s_out.wait_event(cmp_done[j][k])
+                    for h, t in zip(host_out[j], outs):
+                        h.copy_(t, non_blocking=True)
+                    out_done[j][k] = torch.cuda.Event()
+                    out_done[j][k].record(s_out)
 
     run(max(warmup, 2))
     torch.cuda.synchronize(dev)
@@ -539,7 +546,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="mgg", choices=["mgg", "reference"])
     ap.add_argument("--workload", default="deepseek", choices=sorted(WORKLOAD_TEXT))
-    ap.add_argument("--e2e-steps", type=int, default=4)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--sched", default="dynamic", choices=["static", "dynamic"])
     ap.add_argument("--cta", default="auto", choices=["auto", "single", "pair"],
                     help="tile-to-SM mapping: one CTA per 128-row tile, or a CTA pair per 256-row tile")
