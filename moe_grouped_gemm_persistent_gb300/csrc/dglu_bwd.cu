@@ -109,6 +109,9 @@ struct DgluPolicy {
   __device__ DgluPolicy(const DgluParams& prm)
       : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(0), b_mn(prm.b_mn), dynamic(prm.dynamic) {}
 
+  // Nothing of the preparation kernel's output is cached in the policy.
+  __device__ void on_prep_done() {}
+
   // Tile order: expert-major (tile t belongs to the expert containing row floor(t / num_n) *
   // kTileM; its tiles occupy [begin/kTileM * num_n, end/kTileM * num_n)).  Inside an expert the
   // operand that is re-read across the expert's tiles stays in L2 while the other one streams
@@ -786,7 +789,7 @@ struct DgluPolicy {
 template <int BN, int CS, int DS, bool TMAC, bool PAIR, int OP, int EPI>
 __global__ void __launch_bounds__(cta_threads(DgluCfg<CS, DS, TMAC, PAIR, EPI>::kEpiWarps), 1)
     dglu_bwd_kernel(const __grid_constant__ DgluParams prm) {
-  const DgluPolicy<BN, CS, DS, TMAC, PAIR, OP, EPI> pol(prm);
+  DgluPolicy<BN, CS, DS, TMAC, PAIR, OP, EPI> pol(prm);
   persistent_gemm<BN, DgluCfg<CS, DS, TMAC, PAIR, EPI>::kStages, PAIR>(pol);
 }
 
@@ -806,6 +809,7 @@ static cudaError_t launch_dglu_variant(const DgluParams& prm, int num_sms, int d
 __global__ void dglu_prep_kernel(const int32_t* offsets, int L, long long M, const int64_t* b_ptrs,
                                  const __grid_constant__ CUtensorMap tmpl, CUtensorMap* maps, int* status,
                                  float* amax, int n_amax) {
+  griddep_launch_dependents();  // the GEMM kernel may launch now; it waits for this kernel's results
   bool bad_off = false, bad_ptr = false;
   for (int e = threadIdx.x; e < L; e += blockDim.x) {
     const int prev = e ? offsets[e - 1] : 0;
@@ -841,6 +845,7 @@ __global__ void dglu_prep_kernel(const int32_t* offsets, int L, long long M, con
 
 // dbias (bf16) = bf16(dbias + fp32 partial sums): a single rounding of old + sum.
 __global__ void dbias_finalize_kernel(const float* ws, __nv_bfloat16* dbias, long long n, const int* status) {
+  griddep_wait();  // launched to overlap the GEMM kernel's tail: its partial sums are complete from here
   if (*status != 0) return;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
     dbias[i] = __float2bfloat16_rn(__bfloat162float(dbias[i]) + ws[i]);
@@ -878,20 +883,23 @@ static cudaError_t launch_epi_gemm(const DgluLaunch& Lc, const EpiCall& a, cudaS
   CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(ws + kWsHeaderBytes);
   float* dbias_ws = reinterpret_cast<float*>(ws + kWsHeaderBytes + kTmapBytes * (size_t)a.L);
 
-  dglu_prep_kernel<<<1, 1024, 0, stream>>>(a.offsets, (int)a.L, (long long)a.M, a.b_ptrs, Lc.tmap_b, maps, status,
-                                          a.amax, (int)(a.L * (OP == kOpGlu ? 2 : 1)));
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  // stream order: the fills, the preparation kernel, then the GEMM kernel, which may launch while
+  // the preparation kernel runs, then the dbias finalisation
+  cudaError_t err;
   if (a.dbias != nullptr) {
     err = cudaMemsetAsync(dbias_ws, 0, sizeof(float) * (size_t)a.L * 2 * (size_t)a.N, stream);
     if (err != cudaSuccess) return err;
   }
-  const long long num_n = (a.N + BN - 1) / BN;
-  const long long total = (a.M / (Lc.pair ? 2 * BM : BM)) * num_n;  // M is a multiple of 256
   if (a.tile_log != nullptr && a.tile_log_capacity > 0) {
     err = cudaMemsetAsync(a.tile_log, 0xff, sizeof(int32_t) * 4 * (size_t)a.tile_log_capacity, stream);
     if (err != cudaSuccess) return err;
   }
+  dglu_prep_kernel<<<1, 1024, 0, stream>>>(a.offsets, (int)a.L, (long long)a.M, a.b_ptrs, Lc.tmap_b, maps, status,
+                                          a.amax, (int)(a.L * (OP == kOpGlu ? 2 : 1)));
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const long long num_n = (a.N + BN - 1) / BN;
+  const long long total = (a.M / (Lc.pair ? 2 * BM : BM)) * num_n;  // M is a multiple of 256
   if (total > 0) {
     DgluParams prm;
     prm.tmap_a = Lc.tmap_a;
@@ -966,9 +974,17 @@ static cudaError_t launch_epi_gemm(const DgluLaunch& Lc, const EpiCall& a, cudaS
   if (a.dbias != nullptr) {
     const long long n = a.L * 2 * a.N;
     const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
-    dbias_finalize_kernel<<<blocks > 0 ? blocks : 1, 256, 0, stream>>>(dbias_ws, static_cast<__nv_bfloat16*>(a.dbias),
-                                                                       n, status);
-    err = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)(blocks > 0 ? blocks : 1), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, dbias_finalize_kernel, (const float*)dbias_ws,
+                             static_cast<__nv_bfloat16*>(a.dbias), n, (const int*)status);
   }
   return err;
 }

@@ -21,6 +21,8 @@
 // The operation supplies a policy object P with
 //   total_tiles, status, a_mn, b_mn, dynamic        status[3] is the dynamic scheduler's tile
 //                                                   counter (zeroed by the preparation kernel)
+//   on_prep_done()                                  every thread, once the preparation kernel's
+//                                                   writes are visible (before any other use)
 //   TileWork tile(long long t)                      called once per tile, by the scheduler thread
 //   issue_loads(w, kb, sa, sb, bar, rank, acq)      producer thread; `bar` is the address the
 //                                                   loads complete on (the even CTA's in a pair);
@@ -198,7 +200,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, WaitGu
 }
 
 template <int BN, int STAGES, bool PAIR, class P>
-__device__ __forceinline__ void persistent_gemm(const P& p) {
+__device__ __forceinline__ void persistent_gemm(P& p) {
   constexpr int kEpiWarps = P::EPI_WARPS;
   static_assert(kEpiWarps % 4 == 0, "whole TMEM sub-partitions");
   constexpr int kBLoad = PAIR ? BN / 2 : BN;
@@ -228,15 +230,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   const int lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const bool leader = rank == 0;
-  // The preparation kernel of this call found invalid device-side arguments: nothing to do.  A
-  // single CTA leaves at once; the CTAs of a pair must agree, so the even CTA's reading decides
-  // for both (another pair's timeout may set the word between the two readings).
   volatile int* skip_flag = reinterpret_cast<volatile int*>(smem + S::MISC_OFF + 8);
-  if constexpr (!PAIR) {
-    if (*reinterpret_cast<volatile int*>(p.status) != 0) return;
-  } else if (leader && threadIdx.x == 0) {
-    *skip_flag = *reinterpret_cast<volatile int*>(p.status);
-  }
   // consumers of one published tile: the producer and MMA threads and the epilogue warps of this
   // CTA, plus in a pair the peer's producer thread and epilogue warps (the peer's MMA and
   // scheduler warps are idle)
@@ -272,6 +266,14 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       tmem_relinquish();
     }
   }
+  // The launch may overlap the preparation kernel of this call (programmatic stream
+  // serialization): the set-up above needs none of its results; what follows does.
+  griddep_wait();
+  p.on_prep_done();
+  // The preparation kernel found invalid device-side arguments: nothing to do.  The CTAs of a
+  // pair must agree, so the even CTA's reading decides for both (another pair's timeout may set
+  // the word between the two readings).
+  if (threadIdx.x == 0 && leader) *skip_flag = *reinterpret_cast<volatile int*>(p.status);
   tc_fence_before();
   if constexpr (PAIR) cluster_sync_all();  // barriers of both CTAs initialised before any remote use
   else __syncthreads();
@@ -284,6 +286,9 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
       if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
       return;
     }
+  } else if (*skip_flag != 0) {
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    return;
   }
   const WaitGuard wg{abort_flag, p.status};
   const bool dynamic = p.dynamic != 0;
@@ -487,6 +492,7 @@ __device__ __forceinline__ void persistent_gemm(const P& p) {
   }
 
   __syncwarp();  // the role branches above split warps 0 and 1; the barriers below are warp-aligned
+  griddep_launch_dependents();  // a kernel that reads this one's results may start launching
   tc_fence_before();
   if constexpr (PAIR) cluster_sync_all();  // the pair's MMAs are retired and no peer still signals us
   else __syncthreads();
@@ -515,16 +521,16 @@ inline cudaError_t launch_persistent(void (*kern)(Prm), const Prm& prm, long lon
                                      bool pair, int threads, int smem, std::atomic<int>* max_units,
                                      cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3((unsigned)threads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
+  cfg.attrs = attr;
   if (pair) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
   int units = max_units != nullptr ? max_units->load(std::memory_order_relaxed) : 0;
@@ -541,6 +547,10 @@ inline cudaError_t launch_persistent(void (*kern)(Prm), const Prm& prm, long lon
   }
   if (total_tiles < units) units = (int)total_tiles;
   cfg.gridDim = dim3((unsigned)(pair ? 2 * units : units), 1, 1);
+  // start while the preparation kernel before it still runs (the kernel waits for its results)
+  attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+  ++cfg.numAttrs;
   return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 

@@ -87,13 +87,16 @@ struct WgradPolicy {
     c.end = (e >= 0 && e < p.L) ? __ldg(p.offsets + e) : 0;
   }
 
+  __device__ WgradPolicy(const WgradParams& prm)
+      : p(prm), total_tiles(prm.total_tiles), status(prm.status), a_mn(prm.a_mn), b_mn(prm.b_mn),
+        dynamic(prm.dynamic) {}
+
   // The tiles of the experts that have work (all of them when overwriting; in accumulate mode the
   // preparation kernel counts the non-empty ones, which the LPT order puts first), so the two ends
   // of the dynamic schedule are a long and a short tile with work rather than skipped ones.
-  __device__ WgradPolicy(const WgradParams& prm)
-      : p(prm),
-        total_tiles(min(prm.total_tiles, (long long)__ldcg(prm.status + kWgradActiveWord) * prm.tiles_per_expert)),
-        status(prm.status), a_mn(prm.a_mn), b_mn(prm.b_mn), dynamic(prm.dynamic) {}
+  __device__ void on_prep_done() {
+    total_tiles = min(p.total_tiles, (long long)__ldcg(p.status + kWgradActiveWord) * p.tiles_per_expert);
+  }
 
   // Tiles in LPT order (experts by decreasing token count).  The dynamic schedule hands them out
   // alternately from the long end and the short end, so each SM interleaves MMA-bound long
@@ -317,7 +320,7 @@ struct WgradPolicy {
 
 template <int BN, int STAGES, int OS, bool PAIR>
 __global__ void __launch_bounds__(cta_threads(kWgradEpiWarps), 1) wgrad_kernel(const __grid_constant__ WgradParams prm) {
-  const WgradPolicy<BN, OS, PAIR> pol(prm);
+  WgradPolicy<BN, OS, PAIR> pol(prm);
   persistent_gemm<BN, STAGES, PAIR>(pol);
 }
 
@@ -329,6 +332,7 @@ __global__ void wgrad_prep_kernel(const int32_t* offsets, int L, long long T, co
                                   int hidden, int inter, int a_ragged, int b_ragged, CUtensorMap* a_maps,
                                   CUtensorMap* b_maps, CUtensorMap* out_maps, int32_t* order, int* status,
                                   int accumulate) {
+  griddep_launch_dependents();  // the GEMM kernel may launch now; it waits for this kernel's results
   __shared__ int s_cnt[1024];
   bool bad_off = false, bad_ptr = false;
   for (int e = threadIdx.x; e < L; e += blockDim.x) {
@@ -429,21 +433,24 @@ cudaError_t launch_wgrad(const WgradLaunch& Lc, cudaStream_t stream) {
   CUtensorMap* out_maps = b_maps + a.L;
   int32_t* order = reinterpret_cast<int32_t*>(ws + kWsHeaderBytes + 3 * kTmapBytes * (size_t)a.L);
 
+  // stream order: the optional tile-log fill, the preparation kernel, then the GEMM kernel, which
+  // may launch while the preparation kernel runs
+  cudaError_t err;
+  if (a.tile_log != nullptr && a.tile_log_capacity > 0) {
+    err = cudaMemsetAsync(a.tile_log, 0xff, sizeof(int32_t) * 4 * (size_t)a.tile_log_capacity, stream);
+    if (err != cudaSuccess) return err;
+  }
   wgrad_prep_kernel<<<1, 1024, 0, stream>>>(a.offsets, (int)a.L, (long long)a.tokens_sum, a.out_ptrs, Lc.tmap_a,
                                             Lc.tmap_b, Lc.tmap_out, a.a, a.b, (int)a.hidden, (int)a.inter,
                                             Lc.a_ragged, Lc.b_ragged, a_maps, b_maps, out_maps, order, status,
                                             a.accumulate ? 1 : 0);
-  cudaError_t err = cudaGetLastError();
+  err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
   const int BN = Lc.tile_n;
   const long long tiles_m = Lc.pair ? a.hidden / (2 * BM) : (a.hidden + BM - 1) / BM;  // pair: hidden % 256 == 0
   const long long tiles_n = (a.inter + BN - 1) / BN;
   const long long total = a.L * tiles_m * tiles_n;
-  if (a.tile_log != nullptr && a.tile_log_capacity > 0) {
-    err = cudaMemsetAsync(a.tile_log, 0xff, sizeof(int32_t) * 4 * (size_t)a.tile_log_capacity, stream);
-    if (err != cudaSuccess) return err;
-  }
   if (total == 0) return cudaSuccess;
   WgradParams prm;
   prm.tmap_a = Lc.tmap_a;
