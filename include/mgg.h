@@ -24,7 +24,14 @@
  *   pointer after a call returns and allocates no device memory; scratch space is
  *   the caller's `workspace` (size from the *_workspace_size functions).
  * - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work of a
- *   call is queued on it; the call does not synchronise.
+ *   call is queued on it; the call does not synchronise.  Inside a call the GEMM
+ *   kernel may start while the call's preparation kernel still runs (programmatic
+ *   dependent launch) and waits for its results.  The GEMM kernel also lets a
+ *   kernel that the caller queues after it WITH programmatic stream serialization
+ *   start launching as its tiles finish: such a kernel must wait for its
+ *   prerequisites (griddepcontrol.wait / cudaGridDependencySynchronize) before it
+ *   reads this call's outputs.  Ordinary launches, copies and events see the call's
+ *   outputs complete, as with any stream-ordered work.
  * - Arguments are validated on the host before anything is queued.  A violation
  *   returns a status != MGG_OK, queues nothing and leaves every output untouched
  *   (mgg_last_error() holds a message).  Offsets and pointer-array CONTENTS live on
