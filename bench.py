@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import glob
 import json
 import os
@@ -137,8 +138,13 @@ KERNEL_SOURCES = {
 SHARED_SOURCES = ("mgg_pipeline.cuh", "mgg_ptx.cuh", "mgg_internal.h", "mgg_api.cu")
 
 
+_COMMENTS = re.compile(r"/\*.*?\*/|//[^\n]*", re.S)
+
+
 def source_sha(kernel: str = None) -> str:
-    """Hash of the CUDA sources: all of them, or those `kernel` is built from."""
+    """Hash of the code of the CUDA sources (all of them, or those `kernel` is built from) and of
+    the ABI headers: comments and whitespace are left out, so that a profile stays matched to
+    the code it measured when only the documentation changes."""
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "moe_grouped_gemm_persistent_gb300", "csrc")
     if kernel is None:
@@ -147,8 +153,9 @@ def source_sha(kernel: str = None) -> str:
         files = [os.path.join(csrc, f) for f in KERNEL_SOURCES[kernel] + SHARED_SOURCES]
     files = sorted(files + glob.glob(os.path.join(ROOT, "include", "*.h")))
     for f in files:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8", errors="replace") as fh:
+            code = " ".join(_COMMENTS.sub(" ", fh.read()).split())
+        h.update(os.path.basename(f).encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 
