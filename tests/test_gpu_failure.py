@@ -52,11 +52,21 @@ def test_wait_timeout_hook_validates_arguments(dev):
     assert lib.mgg_test_wait_timeout(status.data_ptr(), 1000, 1, 2, None) == _lib.MGG_ERR_VALUE
 
 
-def test_wgrad_bad_offsets_leave_outputs_untouched(dev):
+@pytest.mark.parametrize("cta", ["single", "pair"])
+def test_wgrad_bad_offsets_leave_outputs_untouched(dev, cta):
+    # the GEMM kernel reads the preparation kernel's verdict after its set-up (it may launch while
+    # that kernel runs) and leaves at once, freeing its TMEM, in both CTA modes
     spec = synth.small_wgrad_spec("badoff", hidden=256)
     x = synth.make_wgrad_inputs(spec)
     out = torch.full((spec.L, spec.hidden, spec.inter), 3.0, dtype=torch.float32, device=dev)
     offs = torch.tensor([512, 512, 700, 1536], dtype=torch.int32, device=dev)  # 188 is not a multiple of 256
-    ws = api.wgrad(a=x["a"].to(dev), b=x["b"].to(dev), offsets=offs, hidden=spec.hidden, inter=spec.inter, out=out)
+    ws = api.wgrad(a=x["a"].to(dev), b=x["b"].to(dev), offsets=offs, hidden=spec.hidden, inter=spec.inter, out=out,
+                   cta=cta)
     assert api.read_device_status(ws) == _lib.MGG_ERR_DEVICE_OFFSETS
     assert (out == 3.0).all()
+    # the next call on the same workspace runs normally
+    good = torch.tensor([512, 512, 768, 1536], dtype=torch.int32, device=dev)
+    ws = api.wgrad(a=x["a"].to(dev), b=x["b"].to(dev), offsets=good, hidden=spec.hidden, inter=spec.inter, out=out,
+                   cta=cta, workspace=ws)
+    assert api.read_device_status(ws) == 0
+    assert not (out == 3.0).all()
