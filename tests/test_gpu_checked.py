@@ -5,7 +5,8 @@ tested against the call's extents before the access; a failure would record
 MGG_ERR_DEVICE_BOUNDS in the workspace status word, which every parity test asserts to be 0.
 The subset runs in a child process with MGG_LIB_VARIANT=checked, so the checked library is the
 one loaded there; it covers both operations, single CTAs and pairs, both schedules, dense,
-discrete and ragged operands, the register and TMA C paths, fp32 D with dbias and accumulate."""
+discrete and ragged operands, the register and TMA C paths, fp32 D with dbias and accumulate,
+and the half-width last column tiles of the wgrad."""
 import os
 import subprocess
 import sys
@@ -21,7 +22,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUBSET = " or ".join([
     "swiglu_dense", "geglu_value_fp32d_dbias", "discrete_n_geglu", "regpath_geglu_fp32d_dbias", "situglu",
     "k_n_fp32", "k_n_fp16_acc", "ragged_k_n_discrete", "out_blocked_acc", "many_experts", "m_n_blocked",
-    "exact_ties",
+    "exact_ties", "narrow",
 ])
 
 
