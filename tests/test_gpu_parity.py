@@ -84,6 +84,16 @@ DGLU_CASES = {
 DGLU_SCHED = [(c, "static") for c in DGLU_CASES] + [("swiglu_dense", "dynamic"), ("discrete_n_geglu", "dynamic"),
                                                       ("many_experts", "dynamic")]
 DGLU_CASES["many_experts"] = dict(K=128, N=64, counts=(256, 0, 0, 512, 256, 0, 768, 256, 256, 0, 512))
+# the operation's maximum of 1024 experts, most of them empty: 1024 per-expert weight maps built on
+# the device, the expert search over 1024 offsets, dbias partial sums for every expert (zero rows
+# for the empty ones) and the dGeGLU filters, through discrete N-major weights
+_MAX_COUNTS = [0] * 1024
+for _g in (0, 1, 300, 511, 512, 777, 1022, 1023):
+    _MAX_COUNTS[_g] = 256
+_MAX_COUNTS[300] = 512
+DGLU_CASES["max_experts_discrete"] = dict(K=128, N=64, counts=tuple(_MAX_COUNTS), b_mode="discrete", b_major="n",
+                                          act="dgeglu", c_std=4.0, dbias=True)
+DGLU_SCHED += [("max_experts_discrete", "static"), ("max_experts_discrete", "dynamic")]
 
 
 # "single": 128-row tiles, one CTA per SM; "pair": 256-row tiles on CTA pairs (cta_group::2).
@@ -280,6 +290,14 @@ WGRAD_SCHED = [(c, "static") for c in WGRAD_CASES] + [("k_n_fp32", "dynamic"), (
                                                         ("out_blocked_ragged_discrete", "dynamic"),
                                                         ("out_blocked_discrete_acc", "dynamic")]
 WGRAD_CASES["many_experts"] = dict(hidden=256, inter=128, counts=(256, 0, 2048, 0, 512, 256, 0, 768, 256, 1024))
+# 1024 experts (the maximum), most of them empty: the expert order over 1024 counts, 1024 ragged
+# per-expert maps, zero outputs for the empty experts, and the long/short alternation of the
+# dynamic schedule over a very uneven order
+_WMAX = [0] * 1024
+for _e, _c in ((0, 256), (5, 1024), (400, 256), (511, 512), (512, 256), (900, 768), (1023, 256)):
+    _WMAX[_e] = _c
+WGRAD_CASES["max_experts_ragged"] = dict(hidden=256, inter=128, counts=tuple(_WMAX), input_order="tensor_ragged")
+WGRAD_SCHED += [("max_experts_ragged", "static"), ("max_experts_ragged", "dynamic")]
 
 
 @pytest.mark.parametrize("cta", CTAS)
