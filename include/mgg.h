@@ -23,6 +23,9 @@
  *   valid until the work queued on `stream` has completed.  The library keeps no
  *   pointer after a call returns and allocates no device memory; scratch space is
  *   the caller's `workspace` (size from the *_workspace_size functions).
+ *   Required pointers are non-NULL, except the per-row tensors of a call without
+ *   rows (M == 0: a, c, prob, dprob, d_row) or tokens (tokens_sum == 0: a, b),
+ *   which may be NULL: nothing is read from or written to them.
  * - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work of a
  *   call is queued on it; the call does not synchronise.  Inside a call the GEMM
  *   kernel may start while the call's preparation kernel still runs (programmatic

@@ -25,6 +25,10 @@ mgg_status fail(mgg_status s, const std::string& msg) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// `p`, or the (always valid) workspace when `p` is NULL: the base of a tensor map that no copy uses.
+const void* or_ws(const void* p, const void* workspace) { return p != nullptr ? p : workspace; }
+void* or_ws(void* p, void* workspace) { return p != nullptr ? p : workspace; }
+
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
 // ---------------------------------------------------------------- driver entry point
@@ -138,7 +142,9 @@ mgg_status validate_dglu(const mgg_dglu_bwd_args& a) {
     return fail(MGG_ERR_VALUE, "cta_mode out of range");
   const void* req[] = {a.a, a.c, a.padded_offsets, a.alpha, a.beta, a.prob, a.dprob, a.d_row, a.workspace};
   const char* names[] = {"a", "c", "padded_offsets", "alpha", "beta", "prob", "dprob", "d_row", "workspace"};
+  const bool per_row[] = {true, true, false, false, false, true, true, true, false};
   for (int i = 0; i < 9; ++i) {
+    if (req[i] == nullptr && per_row[i] && a.M == 0) continue;  // no rows: nothing is read or written there
     if (req[i] == nullptr) return fail(MGG_ERR_VALUE, std::string(names[i]) + " must not be NULL");
     if (!aligned16(req[i])) return fail(MGG_ERR_VALUE, std::string(names[i]) + " must be 16-byte aligned");
   }
@@ -181,7 +187,9 @@ mgg_status validate_dsrelu(const mgg_dsrelu_bwd_args& a) {
   if (a.reserved != 0) return fail(MGG_ERR_VALUE, "reserved field must be 0");
   const void* req[] = {a.a, a.c, a.padded_offsets, a.alpha, a.prob, a.dprob, a.d_row, a.workspace};
   const char* names[] = {"a", "c", "padded_offsets", "alpha", "prob", "dprob", "d_row", "workspace"};
+  const bool per_row[] = {true, true, false, false, true, true, true, false};
   for (int i = 0; i < 8; ++i) {
+    if (req[i] == nullptr && per_row[i] && a.M == 0) continue;  // no rows: nothing is read or written there
     if (req[i] == nullptr) return fail(MGG_ERR_VALUE, std::string(names[i]) + " must not be NULL");
     if (!aligned16(req[i])) return fail(MGG_ERR_VALUE, std::string(names[i]) + " must be 16-byte aligned");
   }
@@ -229,6 +237,7 @@ mgg_status validate_wgrad(const mgg_wgrad_args& a) {
   const void* req[] = {a.a, a.b, a.offsets, a.workspace};
   const char* names[] = {"a", "b", "offsets", "workspace"};
   for (int i = 0; i < 4; ++i) {
+    if (req[i] == nullptr && i < 2 && a.tokens_sum == 0) continue;  // no tokens: the operands are never read
     if (req[i] == nullptr) return fail(MGG_ERR_VALUE, std::string(names[i]) + " must not be NULL");
     if (!aligned16(req[i])) return fail(MGG_ERR_VALUE, std::string(names[i]) + " must be 16-byte aligned");
   }
@@ -464,8 +473,10 @@ mgg_status mgg_dglu_bwd(const mgg_dglu_bwd_args* args, void* stream) {
   Lc.device = dev.device;
   Lc.tile_n = kDgluTileN;
   Lc.pair = dglu_pair(a);
-  if ((s = build_epi_maps(Lc, a.a, a.b, a.b_ptrs, a.b_major, a.c, a.c_dtype, a.d_row, a.d_col, a.d_dtype, a.M, a.K,
-                          a.N, a.L, 2 * (uint64_t)a.N)) != MGG_OK)
+  // with no rows (M == 0) the per-row operands may be NULL: their maps, never used, point at the workspace
+  if ((s = build_epi_maps(Lc, or_ws(a.a, a.workspace), a.b, a.b_ptrs, a.b_major, or_ws(a.c, a.workspace), a.c_dtype,
+                          or_ws(a.d_row, a.workspace), a.d_col, a.d_dtype, a.M, a.K, a.N, a.L,
+                          2 * (uint64_t)a.N)) != MGG_OK)
     return s;
   return from_cuda(launch_dglu_bwd(Lc, static_cast<cudaStream_t>(stream)), "mgg_dglu_bwd launch");
 }
@@ -487,8 +498,9 @@ mgg_status mgg_dsrelu_bwd(const mgg_dsrelu_bwd_args* args, void* stream) {
   Lc.device = dev.device;
   Lc.tile_n = kDgluTileN;
   Lc.pair = a.cta_mode != MGG_CTA_SINGLE;  // AUTO: pairs, as for the dGLU dgrad
-  if ((s = build_epi_maps(Lc, a.a, a.b, a.b_ptrs, a.b_major, a.c, a.c_dtype, a.d_row, a.d_col, a.d_dtype, a.M, a.K,
-                          a.N, a.L, (uint64_t)a.N)) != MGG_OK)
+  if ((s = build_epi_maps(Lc, or_ws(a.a, a.workspace), a.b, a.b_ptrs, a.b_major, or_ws(a.c, a.workspace), a.c_dtype,
+                          or_ws(a.d_row, a.workspace), a.d_col, a.d_dtype, a.M, a.K, a.N, a.L,
+                          (uint64_t)a.N)) != MGG_OK)
     return s;
   return from_cuda(launch_dsrelu_bwd(Lc, a, static_cast<cudaStream_t>(stream)), "mgg_dsrelu_bwd launch");
 }
@@ -514,6 +526,9 @@ mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {
   Lc.a_ragged = ragged && a.a_major == MGG_MAJOR_K;
   Lc.b_ragged = ragged && a.b_major == MGG_MAJOR_K;
   const uint64_t T = (uint64_t)(a.tokens_sum > 0 ? a.tokens_sum : 256), H = (uint64_t)a.hidden, I = (uint64_t)a.inter;
+  // with no tokens the operands may be NULL: their maps, never used, point at the workspace
+  const void* A = or_ws(a.a, a.workspace);
+  const void* B = or_ws(a.b, a.workspace);
   // An MN-major operand whose MN extent is a multiple of 64 is also a 3-D tensor of 64-wide
   // blocks: dims {64, T, extent/64}, strides {extent*2, 128} bytes.  One box of that map fills a
   // whole ring slot (its 64 x 64 blocks land 8 KB apart, as the MMA descriptors expect), so the
@@ -531,23 +546,23 @@ mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {
   if (a.a_major == MGG_MAJOR_K) {  // (hidden, T), T contiguous
     const uint64_t dims[2] = {T, H}, strides[1] = {T * 2};
     const uint32_t box[2] = {64, 128};
-    if ((s = encode_bf16(&Lc.tmap_a, a.a, 2, dims, strides, box, "A (K-major)")) != MGG_OK) return s;
-  } else if (!(Lc.a_blocked = blocked(&Lc.tmap_a, a.a, H, 2, "A (M-major, blocked)"))) {
+    if ((s = encode_bf16(&Lc.tmap_a, A, 2, dims, strides, box, "A (K-major)")) != MGG_OK) return s;
+  } else if (!(Lc.a_blocked = blocked(&Lc.tmap_a, A, H, 2, "A (M-major, blocked)"))) {
     // (hidden, T) with hidden contiguous: rows of T
     const uint64_t dims[2] = {H, T}, strides[1] = {H * 2};
     const uint32_t box[2] = {64, 64};
-    if ((s = encode_bf16(&Lc.tmap_a, a.a, 2, dims, strides, box, "A (M-major)")) != MGG_OK) return s;
+    if ((s = encode_bf16(&Lc.tmap_a, A, 2, dims, strides, box, "A (M-major)")) != MGG_OK) return s;
   }
   if (a.b_major == MGG_MAJOR_MN) {  // (T, inter), inter contiguous
-    if (!(Lc.b_blocked = blocked(&Lc.tmap_b, a.b, I, b_cols / 64, "B (N-major, blocked)"))) {
+    if (!(Lc.b_blocked = blocked(&Lc.tmap_b, B, I, b_cols / 64, "B (N-major, blocked)"))) {
       const uint64_t dims[2] = {I, T}, strides[1] = {I * 2};
       const uint32_t box[2] = {64, 64};
-      if ((s = encode_bf16(&Lc.tmap_b, a.b, 2, dims, strides, box, "B (N-major)")) != MGG_OK) return s;
+      if ((s = encode_bf16(&Lc.tmap_b, B, 2, dims, strides, box, "B (N-major)")) != MGG_OK) return s;
     }
   } else {  // (T, inter) with T contiguous: rows of T
     const uint64_t dims[2] = {T, I}, strides[1] = {T * 2};
     const uint32_t box[2] = {64, b_cols};
-    if ((s = encode_bf16(&Lc.tmap_b, a.b, 2, dims, strides, box, "B (K-major)")) != MGG_OK) return s;
+    if ((s = encode_bf16(&Lc.tmap_b, B, 2, dims, strides, box, "B (K-major)")) != MGG_OK) return s;
   }
   {  // outputs: 32-row boxes of one 128-byte row of columns
     const uint64_t esz = a.out_dtype == MGG_FP32 ? 4 : 2, L = (uint64_t)a.L;
@@ -564,7 +579,7 @@ mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {
       } else {
         const uint64_t dims[3] = {32, H, I / 32}, strides[2] = {I * 4, 128};
         const uint32_t box[3] = {32, 32, 2};
-        Lc.out_blocked = encode_map(&Lc.tmap_out, a.out_dtype, a.a, 3, dims, strides, box, "per-expert output (blocked)") == MGG_OK;
+        Lc.out_blocked = encode_map(&Lc.tmap_out, a.out_dtype, A, 3, dims, strides, box, "per-expert output (blocked)") == MGG_OK;
       }
       if (!Lc.out_blocked) g_err = saved;  // the driver refused the blocked view: the plain map is used
     }
@@ -576,7 +591,7 @@ mgg_status mgg_wgrad(const mgg_wgrad_args* args, void* stream) {
     } else if (!Lc.out_blocked) {  // per-expert template; the preparation kernel substitutes each expert's address
       const uint64_t dims[2] = {I, H}, strides[1] = {I * esz};
       const uint32_t box[2] = {cw, 32};
-      if ((s = encode_map(&Lc.tmap_out, a.out_dtype, a.a, 2, dims, strides, box, "per-expert output")) != MGG_OK)
+      if ((s = encode_map(&Lc.tmap_out, a.out_dtype, A, 2, dims, strides, box, "per-expert output")) != MGG_OK)
         return s;
     }
   }

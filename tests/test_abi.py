@@ -166,6 +166,25 @@ def test_valid_args_without_device_report_arch(lib):
     assert lib.mgg_wgrad(wgrad_args(), None) == _lib.MGG_ERR_ARCH
 
 
+def test_empty_calls_accept_null_per_row_tensors(lib):
+    """Without rows (M == 0) or tokens (tokens_sum == 0) the per-row tensors may be NULL: the host
+    check passes them (no device here: the call then reports MGG_ERR_ARCH); with rows they may not."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rows = dict(a=None, c=None, prob=None, dprob=None, d_row=None)
+    assert lib.mgg_dglu_bwd(dglu_args(M=0, **rows), None) == _lib.MGG_ERR_ARCH
+    assert lib.mgg_dsrelu_bwd(dsrelu_args(M=0, **rows), None) == _lib.MGG_ERR_ARCH
+    assert lib.mgg_wgrad(wgrad_args(tokens_sum=0, a=None, b=None), None) == _lib.MGG_ERR_ARCH
+    for f in rows:
+        assert lib.mgg_dglu_bwd(dglu_args(**{f: None}), None) == _lib.MGG_ERR_VALUE, f
+    assert lib.mgg_wgrad(wgrad_args(a=None), None) == _lib.MGG_ERR_VALUE
+    assert lib.mgg_wgrad(wgrad_args(b=None), None) == _lib.MGG_ERR_VALUE
+    # the rest stays required without rows
+    assert lib.mgg_dglu_bwd(dglu_args(M=0, padded_offsets=None), None) == _lib.MGG_ERR_VALUE
+    assert lib.mgg_wgrad(wgrad_args(tokens_sum=0, offsets=None), None) == _lib.MGG_ERR_VALUE
+
+
 @pytest.mark.parametrize("over,expect", [
     (dict(L=0), 1), (dict(M=1000), 1), (dict(K=100), 1), (dict(N=48), 1), (dict(b_ptrs=FAKE), 1), (dict(b=None), 1),
     (dict(b_major=1), 1), (dict(c_dtype=2), 2), (dict(c_dtype=7), 1), (dict(d_dtype=-1), 1), (dict(a=FAKE + 8), 1),

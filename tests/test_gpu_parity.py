@@ -245,6 +245,45 @@ def test_dglu_tiny_workload(dev):
 
 
 @pytest.mark.parametrize("cta", CTAS)
+def test_dglu_all_experts_empty(dev, cta):
+    """M = 0 (every expert empty; torch gives the empty per-row tensors NULL data pointers): the
+    call succeeds, launches no GEMM tiles, and dbias (accumulated into) keeps its values."""
+    L, K, N = 4, 128, 64
+    a = torch.empty(0, K, dtype=torch.bfloat16, device=dev)
+    c = torch.empty(0, 2 * N, dtype=torch.bfloat16, device=dev)
+    prob, dprob = torch.empty(0, device=dev), torch.empty(0, device=dev)
+    d_row = torch.empty(0, 2 * N, dtype=torch.bfloat16, device=dev)
+    b = torch.randn(L, N, K, device=dev).to(torch.bfloat16)
+    alpha = torch.ones(L, device=dev)
+    beta = torch.ones(L, device=dev)
+    offs = torch.zeros(L, dtype=torch.int32, device=dev)
+    dbias = torch.full((L, 2 * N), 1.5, dtype=torch.bfloat16, device=dev)
+    ws = api.dglu_bwd(a=a, c=c, padded_offsets=offs, alpha=alpha, beta=beta, prob=prob, dprob=dprob, d_row=d_row,
+                      b=b, dbias=dbias, act="dgeglu", cta=cta)
+    assert api.read_device_status(ws) == 0
+    assert (dbias == 1.5).all()
+
+
+@pytest.mark.parametrize("cta", CTAS)
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_wgrad_all_experts_empty(dev, cta, accumulate):
+    """T = 0 (every expert empty; the empty operands have NULL data pointers): overwrite writes zeros
+    into every output, accumulate leaves every output as it was."""
+    L, h, i = 3, 256, 128
+    a = torch.empty(0, h, dtype=torch.bfloat16, device=dev)
+    b = torch.empty(0, i, dtype=torch.bfloat16, device=dev)
+    offs = torch.zeros(L, dtype=torch.int32, device=dev)
+    out = torch.full((L, h, i), 2.5, dtype=torch.float32, device=dev)
+    ws = api.wgrad(a=a, b=b, offsets=offs, hidden=h, inter=i, out=out, accumulate=accumulate, cta=cta,
+                   input_order="tensor_ragged")
+    assert api.read_device_status(ws) == 0
+    if accumulate:
+        assert (out == 2.5).all()
+    else:
+        assert (out == 0).all()
+
+
+@pytest.mark.parametrize("cta", CTAS)
 def test_dglu_bad_offsets_report_and_leave_outputs(dev, cta):
     spec = synth.small_dglu_spec("bad")
     x = synth.make_dglu_inputs(spec)
