@@ -84,6 +84,9 @@ DGLU_CASES = {
 DGLU_SCHED = [(c, "static") for c in DGLU_CASES] + [("swiglu_dense", "dynamic"), ("discrete_n_geglu", "dynamic"),
                                                       ("many_experts", "dynamic")]
 DGLU_CASES["many_experts"] = dict(K=128, N=64, counts=(256, 0, 0, 512, 256, 0, 768, 256, 256, 0, 512))
+# one expert (L = 1): the grouped call is a plain alpha^2 A B^T with the dGLU epilogue
+DGLU_CASES["single_expert"] = dict(K=192, N=96, counts=(768,))
+DGLU_SCHED += [("single_expert", "static"), ("single_expert", "dynamic")]
 # the operation's maximum of 1024 experts, most of them empty: 1024 per-expert weight maps built on
 # the device, the expert search over 1024 offsets, dbias partial sums for every expert (zero rows
 # for the empty ones) and the dGeGLU filters, through discrete N-major weights
@@ -336,6 +339,9 @@ _WMAX = [0] * 1024
 for _e, _c in ((0, 256), (5, 1024), (400, 256), (511, 512), (512, 256), (900, 768), (1023, 256)):
     _WMAX[_e] = _c
 WGRAD_CASES["max_experts_ragged"] = dict(hidden=256, inter=128, counts=tuple(_WMAX), input_order="tensor_ragged")
+# one expert (L = 1): A @ B over all tokens
+WGRAD_CASES["single_expert"] = dict(hidden=256, inter=192, counts=(1280,))
+WGRAD_SCHED += [("single_expert", "static"), ("single_expert", "dynamic")]
 WGRAD_SCHED += [("max_experts_ragged", "static"), ("max_experts_ragged", "dynamic")]
 
 
