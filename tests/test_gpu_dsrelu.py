@@ -108,6 +108,23 @@ def test_dsrelu_accumulates_dprob_and_optional_outputs_off(dev):
     check_close("dprob", to_np(gpu["dprob"]), ref["dprob"], TOL_DPROB)
 
 
+@pytest.mark.parametrize("cta", ["single", "pair"])
+def test_dsrelu_all_experts_empty(dev, cta):
+    """M = 0 (every expert empty; the per-row tensors are empty, with NULL data pointers): the call
+    succeeds and the per-expert amax, which the call overwrites, is zero."""
+    L, K, N = 3, 128, 128
+    empty = dict(a=torch.empty(0, K, dtype=torch.bfloat16, device=dev),
+                 c=torch.empty(0, N, dtype=torch.bfloat16, device=dev),
+                 prob=torch.empty(0, device=dev), dprob=torch.empty(0, device=dev),
+                 d_row=torch.empty(0, N, dtype=torch.bfloat16, device=dev))
+    amax = torch.full((L,), 3.0, device=dev)
+    ws = api.dsrelu_bwd(b=torch.randn(L, N, K, device=dev).to(torch.bfloat16),
+                        padded_offsets=torch.zeros(L, dtype=torch.int32, device=dev),
+                        alpha=torch.ones(L, device=dev), amax=amax, cta=cta, **empty)
+    assert api.read_device_status(ws) == 0
+    assert (amax == 0).all()
+
+
 def test_dsrelu_bad_offsets_report_and_leave_outputs(dev):
     spec = synth.small_dglu_spec("bad", act="dsrelu")
     x = synth.make_dglu_inputs(spec)
