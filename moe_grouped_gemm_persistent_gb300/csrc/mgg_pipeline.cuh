@@ -10,6 +10,11 @@
 //               +31 of its CTA's rows), reads the accumulator with tcgen05.ld and hands it to the
 //               operation's epilogue while the MMA already accumulates the next tile.
 //
+// The kernel is launched with programmatic stream serialization behind its call's preparation
+// kernel: it initialises its barriers and allocates TMEM while that kernel may still run, then
+// waits for it (griddepcontrol.wait) before reading anything it wrote, and lets the next
+// programmatically launched kernel start once its roles have finished.
+//
 // Single CTA (PAIR = false): one CTA per SM computes 128 x BN tiles with cta_group::1.
 // CTA pair (PAIR = true): a cluster of two CTAs on two SMs computes 256 x BN tiles with
 // cta_group::2 MMAs issued by the even CTA; each CTA loads its own 128 rows of A and half of the
