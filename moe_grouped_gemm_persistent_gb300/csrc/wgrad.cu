@@ -8,7 +8,7 @@
 //
 // Scheduling: the preparation kernel orders experts by decreasing token count; the
 // persistent CTAs walk the (expert, hidden tile, inter tile) space in that order
-// (longest-processing-time-first), the dynamic schedule alternating between its two ends.
+// (longest-processing-time-first), the dynamic schedule drawing from both of its ends.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -70,7 +70,7 @@ struct WgradPolicy {
   int a_mn, b_mn;
   int dynamic;
   // The scheduler thread's decode cache: the expert slot last decoded at each end of the LPT order
-  // (the dynamic schedule alternates between the two ends, the static one uses end 0) with its
+  // (the dynamic schedule draws from both ends, the static one uses end 0) with its
   // expert and token range, so consecutive tiles of one expert read no global memory.
   struct ExpertRange {
     int slot = -1, e = 0, begin = 0, end = 0;
@@ -99,17 +99,24 @@ struct WgradPolicy {
   }
 
   // Tiles in LPT order (experts by decreasing token count).  The dynamic schedule hands them out
-  // alternately from the long end and the short end, so each SM interleaves MMA-bound long
-  // reductions with store-bound short ones; the static schedule deals them round-robin.
+  // from both ends of that order, so each SM interleaves MMA-bound long reductions with
+  // epilogue-bound short ones: one tile from the long end, then kShortPerLong from the short end.
+  // When overwriting, one short tile per long one; when accumulating, five: the epilogue's
+  // reduce-add also reads every output tile, and spreading the short tiles' read-modify-write
+  // traffic over the whole run beats leaving a tail of short tiles only.  The static schedule
+  // deals the tiles round-robin.
   __device__ TileWork tile(long long t) const {
-    const long long idx = !p.dynamic ? t : (t & 1) ? total_tiles - 1 - (t >> 1) : (t >> 1);
+    const long long per = p.accumulate ? 6 : 2;  // claims per long-end tile (1 + kShortPerLong)
+    const long long grp = t / per, j = t - grp * per;
+    const bool short_end = j != 0;
+    const long long idx = !p.dynamic ? t : short_end ? total_tiles - 1 - (grp * (per - 1) + j - 1) : grp;
     const int slot = (int)(idx / p.tiles_per_expert);
     const int local = (int)(idx % p.tiles_per_expert);
     TileWork w;
     // checked build: an expert slot or order entry outside [0, L) makes the tile a skipped one
     const bool slot_ok = MGG_IN_BOUNDS(p.status, slot >= 0 && slot < p.L, 411, slot);
     int e, begin, end;
-    if (p.dynamic && (t & 1)) {  // the short end of the order
+    if (p.dynamic && short_end) {  // the short end of the order
       decode(c_short, slot, slot_ok);
       e = c_short.e, begin = c_short.begin, end = c_short.end;
     } else {
