@@ -564,7 +564,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="mgg", choices=["mgg", "reference"])
     ap.add_argument("--workload", default="deepseek", choices=sorted(WORKLOAD_TEXT))
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=16)
     ap.add_argument("--sched", default="dynamic", choices=["static", "dynamic"])
     ap.add_argument("--cta", default="auto", choices=["auto", "single", "pair"],
                     help="tile-to-SM mapping: one CTA per 128-row tile, or a CTA pair per 256-row tile")
