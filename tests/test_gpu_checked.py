@@ -6,7 +6,8 @@ MGG_ERR_DEVICE_BOUNDS in the workspace status word, which every parity test asse
 The subset runs in a child process with MGG_LIB_VARIANT=checked, so the checked library is the
 one loaded there; it covers both operations, single CTAs and pairs, both schedules, dense,
 discrete and ragged operands, the register and TMA C paths, fp32 D with dbias and accumulate,
-and the half-width last column tiles of the wgrad."""
+the half-width last column tiles of the wgrad, and the seeded random sweep of option
+combinations."""
 import os
 import subprocess
 import sys
@@ -22,7 +23,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUBSET = " or ".join([
     "swiglu_dense", "geglu_value_fp32d_dbias", "discrete_n_geglu", "regpath_geglu_fp32d_dbias", "situglu",
     "k_n_fp32", "k_n_fp16_acc", "ragged_k_n_discrete", "out_blocked_acc", "many_experts", "m_n_blocked",
-    "exact_ties", "narrow",
+    "exact_ties", "narrow", "sweep",
 ])
 
 
@@ -54,7 +55,7 @@ def test_parity_subset_under_the_bounds_checked_build():
     assert check.returncode == 0 and check.stdout.split() == ["0", "0", "0", "1", "8", "501", "77", "0"], \
         (check.stdout, check.stderr[-2000:])
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-k", SUBSET,
-                        "tests/test_gpu_parity.py", "tests/test_gpu_dsrelu.py"],
+                        "tests/test_gpu_parity.py", "tests/test_gpu_dsrelu.py", "tests/test_gpu_sweep.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=1700)
     tail = (r.stdout + r.stderr)[-3000:]
     assert r.returncode == 0, tail
