@@ -24,6 +24,16 @@ def _ranges(spec):
     return oracle.expert_ranges(np.cumsum(spec.counts))
 
 
+def test_binding_queues_on_the_current_stream(dev):
+    """The binding's default stream is torch's current stream of the current device, inside and
+    outside a stream context."""
+    assert api._stream(None) == torch.cuda.current_stream().cuda_stream
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        assert api._stream(None) == s.cuda_stream == torch.cuda.current_stream().cuda_stream
+    assert api._stream(s) == s.cuda_stream and api._stream(s.cuda_stream) == s.cuda_stream
+
+
 # ------------------------------------------------------------------------------ tensor maps
 def test_tensormap_replace_matches_host_encoding(dev):
     """Device-side rewriting of a descriptor equals the driver's encoding of the target (bytes)."""
