@@ -409,3 +409,81 @@ def test_wgrad_bad_pointer_reports(dev, cta):
                    out_ptrs=ptrs, out_dtype="fp32", cta=cta)
     assert api.read_device_status(ws) == 6
     assert all((o == 0).all() for o in outs)
+
+
+# ------------------------------------------------------------------------------ concurrency
+def test_calls_on_two_streams_at_once(dev):
+    """The ABI keeps no state between calls: dgrad and wgrad calls queued on two streams at once,
+    each with its own workspace, give the oracle's results (three rounds, nothing synchronised
+    between the calls of a round)."""
+    d1 = synth.small_dglu_spec("conc_d1", L=3, counts=(512, 256, 768), K=256, N=320)
+    d2 = synth.small_dglu_spec("conc_d2", L=4, counts=(256, 0, 512, 256), K=192, N=160, act="dgeglu", c_std=4.0,
+                               b_mode="discrete", b_major="n", d_dtype="fp32", dbias=True, seed=1)
+    w1 = synth.small_wgrad_spec("conc_w1", counts=(512, 0, 1024, 256), hidden=512, inter=384,
+                                input_order="tensor_ragged", out_mode="discrete")
+    xd1, xd2, xw1 = synth.make_dglu_inputs(d1), synth.make_dglu_inputs(d2), synth.make_wgrad_inputs(w1)
+    ref_d1, ref_d2, ref_w1 = run_dglu_oracle(d1, xd1), run_dglu_oracle(d2, xd2), run_wgrad_oracle(w1, xw1)
+
+    def dglu_call(spec, x):
+        g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+        keep = None
+        if spec.b_mode == "dense":
+            b_kw = dict(b=g["b"])
+        else:
+            keep = [t.to(dev) for t in x["b"]]
+            b_kw = dict(b_ptrs=api.pointer_array(keep, dev), b_major=spec.b_major, N=spec.N)
+        out = dict(d_row=torch.full((spec.M, 2 * spec.N), float("nan"), dtype=synth.torch_dtype(spec.d_dtype),
+                                    device=dev),
+                   dprob=torch.zeros(spec.M, device=dev),
+                   dbias=torch.zeros(spec.L, 2 * spec.N, dtype=torch.bfloat16, device=dev) if spec.dbias else None,
+                   ws=api.new_workspace(api.dglu_bwd_workspace_size(spec.L, spec.N), dev))
+
+        def run():
+            out["dprob"].zero_()
+            if out["dbias"] is not None:
+                out["dbias"].zero_()
+            api.dglu_bwd(a=g["a"], c=g["c"], padded_offsets=g["padded_offsets"], alpha=g["alpha"], beta=g["beta"],
+                         prob=g["prob"], dprob=out["dprob"], d_row=out["d_row"], dbias=out["dbias"], act=spec.act,
+                         workspace=out["ws"], **b_kw)
+        return run, out, keep
+
+    def wgrad_call(spec, x):
+        a, b, offs = x["a"].to(dev), x["b"].to(dev), x["offsets"].to(dev)
+        outs = [torch.full((spec.hidden, spec.inter), float("nan"), device=dev) for _ in range(spec.L)]
+        ptrs = api.pointer_array(outs, dev)
+        out = dict(outs=outs, ws=api.new_workspace(api.wgrad_workspace_size(spec.L), dev))
+
+        def run():
+            api.wgrad(a=a, b=b, offsets=offs, hidden=spec.hidden, inter=spec.inter, out_ptrs=ptrs, out_dtype="fp32",
+                      input_order=spec.input_order, workspace=out["ws"])
+        return run, out, (a, b, offs, ptrs)
+
+    r_d1, o_d1, k1 = dglu_call(d1, xd1)
+    r_d2, o_d2, k2 = dglu_call(d2, xd2)
+    r_w1, o_w1, k3 = wgrad_call(w1, xw1)
+    r_w2, o_w2, k4 = wgrad_call(w1, xw1)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    for _ in range(3):
+        s1.wait_stream(torch.cuda.current_stream(dev))
+        s2.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s1):
+            r_d1()
+            r_w1()
+        with torch.cuda.stream(s2):
+            r_w2()
+            r_d2()
+        torch.cuda.current_stream(dev).wait_stream(s1)
+        torch.cuda.current_stream(dev).wait_stream(s2)
+        torch.cuda.synchronize(dev)
+        for o in (o_d1, o_d2, o_w1, o_w2):
+            assert api.read_device_status(o["ws"]) == 0
+        for spec, o, ref in ((d1, o_d1, ref_d1), (d2, o_d2, ref_d2)):
+            rows = _ranges(spec)
+            check_close("d_row", to_np(o["d_row"]), ref["d_row"], TOL[spec.d_dtype], rows)
+            check_close("dprob", to_np(o["dprob"]), ref["dprob"], TOL_DPROB, rows)
+            if spec.dbias:
+                check_close("dbias", to_np(o["dbias"]), ref["dbias"], TOL["bf16"])
+        for o in (o_w1, o_w2):
+            for e in range(w1.L):
+                check_close(f"wgrad[{e}]", to_np(o["outs"][e]), ref_w1[e], TOL["fp32"])
+    del k1, k2, k3, k4
