@@ -120,3 +120,78 @@ def test_graph_replay_with_new_values_and_new_offsets(dev, sched, cta):
     assert api.read_device_status(ws_s) == 0
     _check(spec_d2, spec_w2, x, y, d_row, dprob, out)
     _check_srelu(x, c_s, d_s, dprob_s, amax_s)
+
+
+@pytest.mark.parametrize("cta", ["single", "pair"])
+def test_graph_replay_with_pointer_arrays_rewritten(dev, cta):
+    """Discrete weights and per-expert outputs under replay: the per-expert tensor maps are rebuilt
+    on the device from the pointer arrays at every replay, so rewriting the arrays in place (here:
+    the experts' weight and output buffers exchanged) redirects the replayed calls.  The dgrad is
+    the dGeGLU with N-major weights, fp32 D_row and dbias; the wgrad reads ragged K-major operands
+    and writes one FP32 matrix per expert."""
+    counts = np.array([256, 512, 0, 256], dtype=np.int64)
+    spec_d = synth.small_dglu_spec("gp", L=4, counts=counts, K=128, N=64, act="dgeglu", c_std=4.0,
+                                   b_mode="discrete", b_major="n", d_dtype="fp32", dbias=True)
+    spec_w = synth.small_wgrad_spec("gp", L=4, counts=counts, hidden=256, inter=192, input_order="tensor_ragged",
+                                    out_mode="discrete")
+    x = synth.make_dglu_inputs(spec_d)
+    y = synth.make_wgrad_inputs(spec_w)
+    M, N, L = spec_d.M, spec_d.N, spec_d.L
+    d = {k: v.to(dev) for k, v in x.items() if isinstance(v, torch.Tensor)}
+    weights = [t.to(dev) for t in x["b"]]
+    b_ptrs = api.pointer_array(weights, dev)
+    d_row = torch.empty(M, 2 * N, dtype=torch.float32, device=dev)
+    dprob = torch.zeros(M, dtype=torch.float32, device=dev)
+    dbias = torch.zeros(L, 2 * N, dtype=torch.bfloat16, device=dev)
+    wa, wb, woffs = y["a"].to(dev), y["b"].to(dev), y["offsets"].to(dev)
+    outs = [torch.full((spec_w.hidden, spec_w.inter), float("nan"), device=dev) for _ in range(L)]
+    out_ptrs = api.pointer_array(outs, dev)
+    ws_d = api.new_workspace(api.dglu_bwd_workspace_size(L, N), dev)
+    ws_w = api.new_workspace(api.wgrad_workspace_size(L), dev)
+
+    def step(stream):
+        dprob.zero_()
+        dbias.zero_()
+        api.dglu_bwd(a=d["a"], b_ptrs=b_ptrs, b_major="n", N=N, c=d["c"], padded_offsets=d["padded_offsets"],
+                     alpha=d["alpha"], beta=d["beta"], prob=d["prob"], dprob=dprob, d_row=d_row, dbias=dbias,
+                     act="dgeglu", workspace=ws_d, stream=stream, cta=cta)
+        api.wgrad(a=wa, b=wb, offsets=woffs, hidden=spec_w.hidden, inter=spec_w.inter, out_ptrs=out_ptrs,
+                  out_dtype="fp32", input_order="tensor_ragged", workspace=ws_w, stream=stream, cta=cta)
+
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        step(s)
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(s)
+
+    def check(perm_w, perm_o):
+        # the experts' weights as the pointer array now lists them; outputs as it now places them
+        ref = oracle.dglu_bwd(to_np(x["a"]), lambda gg: to_np(x["b"][perm_w[gg]]).T, to_np(x["c"]),
+                              x["padded_offsets"].numpy(), x["alpha"].numpy(), x["beta"].numpy(),
+                              x["prob"].numpy(), act="dgeglu")
+        assert rel_fro(to_np(d_row.cpu()), ref["d_row"]) <= TOL["fp32"]
+        assert rel_fro(to_np(dprob.cpu()), ref["dprob"]) <= TOL_DPROB
+        assert rel_fro(to_np(dbias.cpu()), ref["dbias"]) <= TOL["bf16"]
+        wref = oracle.wgrad(to_np(y["a"]), to_np(y["b"]), y["offsets"].numpy(), spec_w.hidden, spec_w.inter,
+                            input_order="tensor_ragged")
+        for e in range(L):
+            assert rel_fro(to_np(outs[perm_o[e]].cpu()), wref[e]) <= TOL["fp32"], e
+
+    g.replay()
+    torch.cuda.synchronize(dev)
+    assert api.read_device_status(ws_d) == 0 and api.read_device_status(ws_w) == 0
+    check([0, 1, 2, 3], [0, 1, 2, 3])
+    # rewrite both pointer arrays in place: expert g now reads weights[perm[g]] and writes outs[perm[g]]
+    perm = [3, 0, 1, 2]
+    b_ptrs.copy_(api.pointer_array([weights[p] for p in perm], dev))
+    out_ptrs.copy_(api.pointer_array([outs[p] for p in perm], dev))
+    for o in outs:
+        o.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize(dev)
+    assert api.read_device_status(ws_d) == 0 and api.read_device_status(ws_w) == 0
+    check(perm, perm)
